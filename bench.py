@@ -1,0 +1,474 @@
+#!/usr/bin/env python
+"""Benchmark of the QSA sparse-attention step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 50k] [--impl native|reference]
+
+A step is one decode step of one QSA layer over all sequences of the
+workload: qsa_pool_update (dirty block) -> qsa_index_topk (score, select,
+expand) -> qsa_sparse_attn (split-KV attention + combine), through the C ABI
+on one stream.  Inputs are resident in HBM when the timed region starts; L2
+is flushed (a 1 GiB write) before every step, outside the per-step events.
+Prints one JSON line (rank 0).
+
+Workloads (seeded, synthetic; shapes of the qwen4exp QSA layer):
+  50k        1 seq, 50,000-cell fp16 prompt, 128 decode steps (default)
+  250k_q8    1 seq, 250,000-cell q8_0 prompt, 128 decode steps
+  5x250k_q8  5 seqs x 250,000 cells in one q8_0 cache, 5 tokens per step
+  tiny       1 seq, 4,096 cells
+  prefill    512-token ubatch on a 250,000-cell fp16 prompt
+
+--impl reference times the CPU oracle (NumPy float64) on the host cores on
+the same workload, as the slow baseline arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "QSA-layer decode tokens/s at 50k/250k ctx (1 and 5 seqs); HBM GB/s vs peak"
+FLUSH_BYTES = 1 << 30
+
+DESCR = {
+    "50k": "decode, 1 seq, 50,000-cell fp16 K/V prompt + 1 cell/step (tails cycle 1,2,3,0), "
+           "16q/2kv heads x 256, indexer 4x128, r=4, top_k=2048",
+    "250k_q8": "decode, 1 seq, 250,000-cell q8_0 K/V prompt + 1 cell/step, same heads, top_k=2048",
+    "5x250k_q8": "decode, 5 seqs x 250,000 cells in one 1.25M-cell q8_0 cache, 5 tokens/step, top_k=2048 per seq",
+    "tiny": "decode, 1 seq, 4,096 cells fp16, top_k=2048",
+    "prefill": "prefill ubatch, 512 tokens appended to a 250,000-cell fp16 prompt, 128 dirty blocks",
+}
+
+
+def _env_rank():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), \
+        int(os.environ.get("LOCAL_RANK", 0))
+
+
+def _peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        return None
+
+
+def algorithmic_bytes(wl, step_idx: int):
+    """Algorithmic bytes of each kernel for one step (what the method must
+    move at least once), by stage:
+      pool:   per dirty slot r fp16 idx-key rows (256 B) + table row + 512 B write
+      score:  per visible block a 512 B pooled row + 4 B slot id + 4 B score write,
+              plus the token's 2 KiB query and 16 B weights
+      filter: 4 B score read per visible block
+      final:  per chosen block 4 B slot + r*4 B members, + the cell list written
+      attn:   per selected cell and KV head one K and one V row (512 B each fp16,
+              272 B each q8_0), + 4 B index, + the token's 8 KiB query
+      combine: the fp32 output, 16 KiB per token"""
+    cfg = wl.cfg
+    r = cfg["compress_ratio"]
+    B = cfg["top_k"] // r
+    G = cfg["n_kv_heads"]
+    st = wl.steps[step_idx]
+    row_b = 2 * 256 if cfg["kv_type"] == "f16" else 256 + 16
+    out = dict(pool=0.0, score=0.0, filter=0.0, final=0.0, attn=0.0, combine=0.0)
+    nd = int((st.dirty >= 0).sum())
+    out["pool"] = nd * (r * 256 + 4 * r + 4 + 512)
+    for p in st.tok_pos.tolist():
+        nb = (p + 1) // r
+        tail = p + 1 - nb * r
+        nsel = min(nb, B) * r + tail
+        out["score"] += nb * (512 + 4 + 4) + 2048 + 16
+        out["filter"] += nb * 4
+        out["final"] += min(nb, B) * (4 + 4 * r) + (cfg["top_k"] + r - 1) * 4
+        out["attn"] += nsel * G * 2 * row_b + nsel * 4 + cfg["n_q_heads"] * cfg["head_dim"] * 2
+        out["combine"] += cfg["n_q_heads"] * cfg["head_dim"] * 4
+    return out
+
+
+class Clocks:
+    """nvidia-smi clock/throttle sampling around a timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.p = None
+        self.path = os.path.join("/tmp", f"qsa_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.p = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except Exception:
+            self.p.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())
+                if any(r[3].replace(".", "").isdigit() for r in rows) else None}
+
+
+# ---------------------------------------------------------------------------
+class OracleRunner:
+    """The CPU oracle as it stands, stepping through a workload: each step
+    appends the step's cells, then runs the full oracle step (pool the dirty
+    blocks, score every visible block, select, expand, attend).  For steps
+    with many tokens (prefill) a bounded sample of the tokens is attended."""
+
+    def __init__(self, wl, max_tokens_per_step: int = 8):
+        from oracle import qsa_oracle as O
+        from sparse_attention_long_qsa_gb300.layer import append_rows
+        self.O, self.append_rows, self.wl = O, append_rows, wl
+        self.cap = max_tokens_per_step
+        cfg = wl.cfg
+        self.table0 = wl.blk_cells_state(0)
+        self.pooled = O.pool_update(cfg, wl.idx_k, self.table0, wl.slot_block_idx, wl.prompt_dirty(),
+                                    wl.norm_w, np.zeros((wl.n_slots, cfg["idx_dim"]), np.float32))
+        self.table = self.table0.copy()
+        self.next = 0
+
+    def step(self, i: int) -> int:
+        """Run workload step i (steps must come in order, wrapping to 0).
+        Returns the tokens attended; only the oracle call is meant to be timed
+        by the caller via the returned duration."""
+        wl, O = self.wl, self.O
+        i %= len(wl.steps)
+        if i == 0:
+            self.table = self.table0.copy()
+        s, rows = self.append_rows(wl, i)
+        self.table[s] = rows
+        st = wl.steps[i]
+        if len(st.tok_pos) > self.cap:
+            import dataclasses
+            sel = np.linspace(0, len(st.tok_pos) - 1, self.cap).astype(int)
+            st = dataclasses.replace(st, tok_seq=st.tok_seq[sel], tok_pos=st.tok_pos[sel], q=st.q[sel],
+                                     q_idx=st.q_idx[sel], w_idx=st.w_idx[sel])
+        a = time.perf_counter()
+        self.pooled, _, _ = O.run_step(wl.cfg, wl.idx_k, wl.k_cache, wl.v_cache, wl.n_cells, self.table,
+                                       wl.slot_block_idx, wl.seq_blk_off, wl.seq_blk_slots, wl.norm_w,
+                                       self.pooled, st)
+        self.last_s = time.perf_counter() - a
+        return len(st.tok_pos)
+
+
+def cpu_oracle_rate(wl, max_seconds: float, min_steps: int = 2):
+    """Oracle tokens/s over consecutive steps until max_seconds of oracle
+    time.  Returns (tokens/s, steps run, seconds, threads)."""
+    run = OracleRunner(wl)
+    tokens = steps = 0
+    elapsed = 0.0
+    while steps < min_steps or elapsed < max_seconds:
+        tokens += run.step(steps)
+        elapsed += run.last_s
+        steps += 1
+    return tokens / elapsed, steps, elapsed, _blas_threads()
+
+
+def _blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [d.get("num_threads", 1) for d in threadpool_info() if d.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return len(os.sched_getaffinity(0))
+
+
+# ---------------------------------------------------------------------------
+def run_reference(args, rank, world):
+    """--impl reference: the CPU oracle on the host cores (rank 0 only):
+    W untimed then exactly K timed workload steps."""
+    if rank != 0:
+        return
+    from qsa_workload import make_workload
+    wl = make_workload(args.config, seed=0)
+    run = OracleRunner(wl)
+    for n in range(args.warmup):
+        run.step(n)
+    tokens, secs = 0, 0.0
+    for n in range(args.steps):
+        tokens += run.step(args.warmup + n)
+        secs += run.last_s
+    rate = tokens / secs
+    threads = _blas_threads()
+    per = min(len(wl.steps[0].tok_pos), run.cap)
+    sample = (f"{args.steps} consecutive steps of the {args.config} workload, full oracle step each "
+              f"({per} token(s) attended per step)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": DESCR[args.config], "name": args.config},
+        "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+def measure_config(name, K, W, dev, *, e2e=True, cpu=True, cpu_seconds=10.0, clocks=None, quiet=False):
+    import torch
+    from qsa_workload import make_workload
+    from sparse_attention_long_qsa_gb300 import qsa
+    from sparse_attention_long_qsa_gb300.layer import QSALayer, append_rows, step_inputs
+
+    t_gen = time.perf_counter()
+    wl = make_workload(name, seed=0)
+    t_gen = time.perf_counter() - t_gen
+    n_steps = len(wl.steps)
+    L = QSALayer.from_workload(wl, 0, device=dev)
+    tbl0 = L.blk_cells.clone()
+    L.warm(torch.from_numpy(wl.prompt_dirty()).to(dev))
+    inputs = [step_inputs(st, device=dev) for st in wl.steps]
+    appends = []
+    for i in range(n_steps):
+        s, rows = append_rows(wl, i)
+        appends.append((torch.from_numpy(s).to(dev), torch.from_numpy(rows).to(dev)))
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    toks_per_step = [len(st.tok_pos) for st in wl.steps]
+    alg = [algorithmic_bytes(wl, i) for i in range(n_steps)]
+
+    def do_append(i):
+        if i == 0:
+            L.blk_cells.copy_(tbl0)
+        s, rows = appends[i]
+        L.blk_cells[s] = rows
+
+    kernels = list(qsa.KERNELS)
+
+    def loop(nsteps, start, hook=None, e2e_bufs=None):
+        """Run nsteps steps from step index `start` (mod n_steps); returns
+        per-step device ms and the hooked kernels' per-launch ms."""
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(nsteps)]
+        hk = {k: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(nsteps)] for k in (hook or [])}
+        idx = []
+        L.blk_cells.copy_(tbl0)
+        for i in range(start % n_steps):
+            do_append(i)
+        for n in range(nsteps):
+            i = (start + n) % n_steps
+            idx.append(i)
+            do_append(i)
+            flush.fill_(float(n))
+            for k in hk:
+                qsa.profile_kernel(k, *hk[k][n])
+            evs[n][0].record()
+            if e2e_bufs is None:
+                L.step(**inputs[i])
+            else:
+                h = e2e_bufs[i]
+                d = inputs[i]
+                for key in ("tok_seq", "tok_pos", "q", "q_idx", "w_idx", "dirty"):
+                    d[key].copy_(h[key], non_blocking=True)
+                L.step(**d)
+                h["out"].copy_(L.out[:toks_per_step[i]], non_blocking=True)
+            evs[n][1].record()
+        for k in hk:
+            qsa.profile_kernel(k, None, None)
+        torch.cuda.synchronize()
+        ms = [a.elapsed_time(b) for a, b in evs]
+        kms = {k: [a.elapsed_time(b) for a, b in hk[k]] for k in hk}
+        return idx, ms, kms
+
+    # warm-up, then a per-kernel breakdown pass (all kernels hooked, untimed for the headline)
+    loop(max(W, 1), 0)
+    bidx, _, kms = loop(min(n_steps, max(K, 8)), W, hook=kernels)
+    kern_us = {k: 1e3 * float(np.mean(v)) for k, v in kms.items()}
+    dominant = max(kern_us, key=kern_us.get)
+
+    # headline: K timed steps, the dominant kernel hooked for the roofline
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.start()
+    wall0 = time.perf_counter()
+    idx, ms, dk = loop(K, W, hook=[dominant])
+    wall = time.perf_counter() - wall0
+    dev_ms = float(np.sum(ms))
+    tokens = sum(toks_per_step[i] for i in idx)
+    value = tokens / (dev_ms / 1e3)
+    dom_ms = float(np.mean(dk[dominant]))
+    dom_bytes = float(np.mean([alg[i][dominant] for i in idx]))
+    kbytes = {k: float(np.mean([alg[i][k] for i in bidx])) for k in kernels}
+
+    res = dict(value=value, ms_per_step=dev_ms / K, tokens=tokens, wall_s=wall,
+               dominant=dominant, dom_ms=dom_ms, dom_bytes=dom_bytes, kern_us=kern_us,
+               kern_gbs={k: kbytes[k] / (kern_us[k] * 1e-6) / 1e9 for k in kernels if kern_us[k] > 0},
+               gen_s=t_gen, wl=wl, step_bytes=float(np.mean([sum(alg[i].values()) for i in idx])))
+
+    if e2e:
+        # same steps through the public API from pinned host buffers
+        bufs = []
+        hb = 0
+        for i, st in enumerate(wl.steps):
+            h = {k: torch.from_numpy(np.ascontiguousarray(getattr(st, k))).pin_memory()
+                 for k in ("tok_seq", "tok_pos", "q", "q_idx", "w_idx", "dirty")}
+            h["out"] = torch.empty((toks_per_step[i], 16, 256), dtype=torch.float32).pin_memory()
+            bufs.append(h)
+        idx2, ms2, _ = loop(K, W, e2e_bufs=bufs)
+        h2d = float(np.mean([sum(bufs[i][k].numel() * bufs[i][k].element_size()
+                                 for k in ("tok_seq", "tok_pos", "q", "q_idx", "w_idx", "dirty")) for i in idx2]))
+        d2h = float(np.mean([bufs[i]["out"].numel() * 4 for i in idx2]))
+        tok2 = sum(toks_per_step[i] for i in idx2)
+        res["e2e"] = {"value": tok2 / (float(np.sum(ms2)) / 1e3), "unit": "tokens/s",
+                      "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+    res["clocks"] = clocks.stop() if clocks else None
+    st, flags = qsa.debug_check()
+    if st != 0:
+        raise RuntimeError(f"device error word set during the bench: {flags:#x}")
+    del L, flush
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_native(args, rank, world, local):
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = f"cuda:{local}"
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl", device_id=torch.device(dev))
+    peaks = _peaks()
+    hbm = peaks["hbm_gbs"] if peaks else 6800.0
+    peak_src = "of measured" if peaks else "of fallback"
+
+    clocks = Clocks(local)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    res = measure_config(args.config, args.steps, args.warmup, dev, clocks=clocks)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+        t = torch.tensor([res["ms_per_step"] * args.steps], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        max_ms = float(t.item())
+    else:
+        max_ms = res["ms_per_step"] * args.steps
+    value = world * res["tokens"] / (max_ms / 1e3)
+
+    secondary = {}
+    if args.secondary and rank == 0:
+        for name in args.secondary.split(","):
+            if name == args.config or not name:
+                continue
+            r2 = measure_config(name, min(args.steps, 128), args.warmup, dev, e2e=False)
+            secondary[name] = {
+                "workload": DESCR[name], "value": r2["value"], "unit": "tokens/s",
+                "ms_per_step": r2["ms_per_step"],
+                "kernels_us": {k: round(v, 3) for k, v in r2["kern_us"].items()},
+                "kernels_gbs": {k: round(v, 1) for k, v in r2["kern_gbs"].items()},
+                "dominant": r2["dominant"],
+                "dominant_frac_of_hbm": r2["dom_bytes"] / (r2["dom_ms"] * 1e-3) / 1e9 / hbm,
+            }
+
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        rate, steps, secs, threads = cpu_oracle_rate(res["wl"], args.cpu_seconds)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"{steps} consecutive decode steps of the {args.config} workload, full oracle "
+                         f"step each (pool dirty block, score all blocks, select, expand, attend), "
+                         f"{secs:.1f} s"}
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+    wl = res["wl"]
+    achieved = res["dom_bytes"] / (res["dom_ms"] * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16" if wl.cfg["kv_type"] == "f16" else "q8_0",
+        "data": "synthetic (seeded N(0,1) K/V/keys, U(0,1) weights)",
+        "config": {"workload": DESCR[args.config], "name": args.config,
+                   "tokens_per_step": len(wl.steps[0].tok_pos),
+                   "l2": "flushed before every step (1 GiB write), outside the step's events",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"kernel": res["dominant"], "bound": "hbm", "achieved": achieved,
+                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "peak_source": f"hbm_gbs {peak_src}",
+                     "bytes_per_launch": res["dom_bytes"], "us_per_launch": res["dom_ms"] * 1e3,
+                     "traffic": None},
+        "kernels_us": {k: round(v, 3) for k, v in res["kern_us"].items()},
+        "kernels_gbs": {k: round(v, 1) for k, v in res["kern_gbs"].items()},
+        "step_bytes": res["step_bytes"],
+        "step_gbs": res["step_bytes"] / (res["ms_per_step"] * 1e-3) / 1e9,
+        "cpu_baseline": cpu,
+        "e2e": res.get("e2e"),
+        "gpu_launches": 6 * args.steps,
+        "clocks": res["clocks"],
+        "secondary": secondary or None,
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1024)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--config", default="50k", choices=list(DESCR))
+    ap.add_argument("--secondary", default="250k_q8,5x250k_q8",
+                    help="comma list of further workloads timed on rank 0 (empty: none)")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    rank, world, local = _env_rank()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_native(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,216 @@
+/*
+ * qsa.h - C ABI of libqsa: the QSA sparse-attention step on one GB300 (sm_103a).
+ *
+ * The step has four parts, described in llama.cpp issue #28734 ("Eval bug:
+ * qwen4exp (Qwen3.8-Flash-Next) CUDA: decode slows linearly with context"),
+ * in the fix summary's sections lever1, lever2, lever2b, lever3 and sparse256:
+ *
+ *   qsa_pool_update   persistent pooled block-key cache (lever2, lever2b)
+ *   qsa_index_topk    indexer block scores, block-granular top-k, block -> cell
+ *                     expansion with the tail cells carried along (lever3)
+ *   qsa_sparse_attn   split-KV flash-decode over only the selected cells,
+ *                     fp16 or q8_0 K/V dequantised after the gather (lever1,
+ *                     sparse256, and the author's q8-compact follow-up)
+ *
+ * Conventions for every call:
+ *  - Pointers named as device buffers are DEVICE pointers owned by the caller.
+ *    The library never allocates, frees or keeps them.
+ *  - Calls are asynchronous on `stream` and never synchronise it (only
+ *    qsa_debug_check does).  Results are deterministic: identical inputs give
+ *    bit-identical outputs.
+ *  - Arguments are validated on the host before any launch; an invalid call
+ *    returns a negative status and launches nothing.  A failed launch returns
+ *    QSA_ERR_CUDA.  Indices read from device buffers (cells, slots) are
+ *    range-checked by the kernels: an out-of-range index is skipped (treated
+ *    as absent / masked) and recorded in a device error word that
+ *    qsa_debug_check reads.  No kernel traps or spin-waits.
+ *  - Shapes: one instantiated geometry, the qwen4exp QSA layer: head_dim 256,
+ *    8 query heads per KV head (n_q_heads = 8 * n_kv_heads), idx_dim 128,
+ *    n_idx_heads 4, compress_ratio 4, top_k a multiple of compress_ratio.
+ *    Anything else returns QSA_ERR_UNSUPPORTED.
+ *
+ * Data layout in device memory:
+ *   idx_k          fp16  [n_cells][idx_dim]             indexer key of each cell
+ *   k/v cache f16  fp16  [n_cells][n_kv_heads][head_dim]
+ *   k/v cache q8_0 bytes: qs int8 [n_cells][n_kv_heads][head_dim], then at byte
+ *                  offset n_cells*n_kv_heads*head_dim the scales d fp16
+ *                  [n_cells][n_kv_heads][head_dim/32]; value = d[c][g][i/32]*qs[c][g][i]
+ *   blk_cells      int32 [n_slots][compress_ratio]  cell of position j*r+i of the
+ *                  slot's block, -1 = not (yet) present
+ *   slot_block_idx int32 [n_slots]  block index j of the slot within its sequence
+ *   pooled         fp32  [n_slots][idx_dim]
+ *   seq_blk_off    int64 [n_seq+1], seq_blk_slots int32 [seq_blk_off[n_seq]]:
+ *                  block j of sequence s lives in slot seq_blk_slots[seq_blk_off[s]+j]
+ *   tok_seq/tok_pos int32 [T]: sequence and position p of each query token; the
+ *                  token's own cell is present, positions 0..p are visible
+ *   q_idx fp32 [T][n_idx_heads][idx_dim], w_idx fp32 [T][n_idx_heads]
+ *   q     fp16 [T][n_q_heads][head_dim],  out fp32 [T][n_q_heads][head_dim]
+ *   cells int32 [T][qsa_cells_per_token(cfg)], count int32 [T]
+ */
+#ifndef QSA_H
+#define QSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* qsa_stream_t;
+
+typedef enum {
+  QSA_OK = 0,
+  QSA_ERR_INVALID_ARG = -1,    /* null pointer, negative size, bad enum */
+  QSA_ERR_SHAPE = -2,          /* sizes inconsistent with each other */
+  QSA_ERR_UNSUPPORTED = -3,    /* configuration outside the instantiated geometry */
+  QSA_ERR_WORKSPACE = -4,      /* workspace null, misaligned (256 B) or too small */
+  QSA_ERR_CUDA = -5,           /* a CUDA call or launch failed */
+  QSA_ERR_DEVICE_BOUNDS = -6   /* qsa_debug_check: a kernel met an out-of-range index */
+} qsa_status;
+
+typedef enum { QSA_KV_F16 = 0, QSA_KV_Q8_0 = 1 } qsa_kv_type;
+
+typedef struct {
+  int32_t n_q_heads;       /* 16 */
+  int32_t n_kv_heads;      /* 2: query head h reads KV head h / 8 */
+  int32_t head_dim;        /* 256 (DKQ = DV) */
+  int32_t n_idx_heads;     /* 4 */
+  int32_t idx_dim;         /* 128 */
+  int32_t compress_ratio;  /* r = 4 cells per block */
+  int32_t top_k;           /* 2048 cells = top_k / r whole blocks */
+  float rope_theta;        /* 1e6 */
+  float rms_eps;           /* 1e-6 */
+  float attn_scale;        /* 1 / sqrt(head_dim) */
+  int32_t kv_type;         /* qsa_kv_type */
+} qsa_config;
+
+/* Fill *cfg with the qwen4exp QSA layer: 16/2 heads of 256, indexer 4 x 128,
+ * r = 4, top_k = 2048, theta 1e6, eps 1e-6, scale 1/16, fp16 K/V. */
+qsa_status qsa_config_init(qsa_config* cfg);
+
+/* Cells a token may attend: top_k + r - 1 (512 whole blocks plus at most r-1
+ * tail cells; llama.cpp issue #28734, goodbadwolf's comment: n_kv_max =
+ * min(n_kv, indexer_top_k + r - 1) = 2051).  Row pitch of `cells`. */
+int32_t qsa_cells_per_token(const qsa_config* cfg);
+
+/* ---------------------------------------------------------------------------
+ * S1  qsa_pool_update  (issue #28734, fix summary, lever2 and lever2b)
+ * For each dirty slot s (entries < 0 are skipped; the caller pads the list to
+ * a power of two >= 4 so a captured graph keeps its shape):
+ *   m   = mean of idx_k[c] over the present cells c of blk_cells[s]
+ *   x   = m / sqrt(mean(m^2) + rms_eps) * norm_w
+ *   out = NeoX RoPE of x at position slot_block_idx[s] * r, theta = rope_theta
+ *         (pair (d, d + idx_dim/2) turns by pos * theta^(-2d/idx_dim))
+ *   pooled[s] = out (fp32).  A slot with no present cell gets zeros.
+ * Only the dirty rows of `pooled` are written.  Computed in fp64, rounded once.
+ * Errors: QSA_ERR_INVALID_ARG (null pointer with n_dirty > 0, negative sizes),
+ * QSA_ERR_UNSUPPORTED (geometry).  A dirty slot >= n_slots or a member cell
+ * >= n_cells is skipped and flagged in the device error word. */
+qsa_status qsa_pool_update(const qsa_config* cfg,
+                           const void* idx_k, int64_t n_cells,
+                           const int32_t* blk_cells, const int32_t* slot_block_idx,
+                           int64_t n_slots,
+                           const int32_t* dirty, int32_t n_dirty,
+                           const float* norm_w, float* pooled,
+                           qsa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * S2  qsa_index_scores  (indexer score as the build defines it; the pages name
+ * build_qsa_top_k only - issue #28734, wussh's item 3)
+ * For token t of sequence s = tok_seq[t] at position p = tok_pos[t], and each
+ * block j < floor((p+1)/r) of s:
+ *   scores[t][j] = sum_h w_idx[t][h] * max(0, q_idx[t][h] . pooled[slot(s,j)])
+ * fp32, fixed summation order (the same kernel qsa_index_topk runs).  Entries
+ * j >= floor((p+1)/r) of the row (pitch max_blocks) are written as -inf.
+ * max_blocks: host upper bound on floor((p+1)/r) over the tokens; a token
+ * beyond it is clamped and flagged.  Exposed so the scores can be checked on
+ * their own; the decode path calls qsa_index_topk. */
+qsa_status qsa_index_scores(const qsa_config* cfg, int32_t n_tokens,
+                            const float* q_idx, const float* w_idx,
+                            const int32_t* tok_seq, const int32_t* tok_pos,
+                            const float* pooled, int64_t n_slots,
+                            const int64_t* seq_blk_off, const int32_t* seq_blk_slots,
+                            int32_t n_seq, int64_t max_blocks,
+                            float* scores, qsa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * S2+S3+S4  qsa_index_topk  (issue #28734, fix summary, lever3 and lever2b)
+ * Per token: scores as in qsa_index_scores; the B = top_k / r blocks of
+ * largest score among j < floor((p+1)/r) (ties to the lower j; all of them if
+ * there are fewer); then
+ *   cells[t] = r member cells of each chosen block, blocks ascending, then the
+ *              tail cells of block floor((p+1)/r) at positions <= p
+ *   count[t] = (#chosen blocks) * r + ((p + 1) mod r)
+ * Entries of the row beyond count[t] are set to -1.  Blocks not yet complete
+ * for the token are never scored (-inf in the reference description).
+ * workspace: >= qsa_index_topk_workspace_size(cfg, n_tokens, max_blocks) bytes,
+ * 256-byte aligned, contents on entry irrelevant (the call clears what it
+ * needs).  Selection is exact on the fp32 scores: a radix select on their bit
+ * patterns. */
+size_t qsa_index_topk_workspace_size(const qsa_config* cfg, int32_t n_tokens,
+                                     int64_t max_blocks);
+qsa_status qsa_index_topk(const qsa_config* cfg, int32_t n_tokens,
+                          const float* q_idx, const float* w_idx,
+                          const int32_t* tok_seq, const int32_t* tok_pos,
+                          const float* pooled, const int32_t* blk_cells, int64_t n_slots,
+                          const int64_t* seq_blk_off, const int32_t* seq_blk_slots,
+                          int32_t n_seq, int64_t max_blocks, int64_t n_cells,
+                          int32_t* cells, int32_t* count,
+                          void* workspace, size_t ws_bytes, qsa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * S5+S6  qsa_sparse_attn  (issue #28734, fix summary, lever1 and sparse256;
+ * q8_0: the author's q8-compact follow-up in the same issue)
+ * For token t, query head h, KV head g = h / (n_q_heads / n_kv_heads):
+ *   out[t][h] = sum_{i < count[t]} softmax_i(attn_scale * q[t][h] . K[c_i][g]) V[c_i][g]
+ * with c_i = cells[t][i] (row pitch qsa_cells_per_token).  Split-KV: each CTA
+ * owns a range of the token's cells and writes a partial (max, sum, o); a
+ * combine pass merges them with log-sum-exp weights.  fp32 accumulation.
+ * count[t] == 0 gives zeros.  A cell outside [0, n_cells) is masked and
+ * flagged.  workspace: >= qsa_sparse_attn_workspace_size(cfg, n_tokens) bytes,
+ * 256-byte aligned. */
+size_t qsa_sparse_attn_workspace_size(const qsa_config* cfg, int32_t n_tokens);
+qsa_status qsa_sparse_attn(const qsa_config* cfg, int32_t n_tokens,
+                           const void* q, const void* k_cache, const void* v_cache,
+                           int64_t n_cells, const int32_t* cells, const int32_t* count,
+                           float* out, void* workspace, size_t ws_bytes,
+                           qsa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Host helpers (no GPU).
+ *
+ * qsa_blocks_dirty (issue #28734, fix summary, lever2: "host-side structural
+ * compare of member cells", dirty count bucketed to a power of two >= 4):
+ * compares two host block tables [n_slots][r]; writes the slots whose rows
+ * differ, ascending, padded with -1 to the next power of two >= pad_pow2_min
+ * (0 = no padding), into out_dirty (capacity `cap`), and the padded length to
+ * *n_dirty.  QSA_ERR_SHAPE if cap is too small (nothing written but *n_dirty). */
+qsa_status qsa_blocks_dirty(const int32_t* old_tbl, const int32_t* new_tbl,
+                            int64_t n_slots, int32_t r, int32_t* out_dirty,
+                            int32_t cap, int32_t* n_dirty, int32_t pad_pow2_min);
+
+/* Synchronises `stream`, reads and clears the device error word of the
+ * current device.  QSA_ERR_DEVICE_BOUNDS if a kernel met an out-of-range
+ * index since the last check; *flags (if non-null) receives the bit set:
+ * 1 slot, 2 cell, 4 block list too short, 8 token position beyond max_blocks,
+ * 16 token with a sequence id outside [0, n_seq) or a negative position. */
+qsa_status qsa_debug_check(qsa_stream_t stream, uint32_t* flags);
+
+/* Measurement hook (host state, process-wide, not for concurrent use from
+ * several host threads).  While set, each launch of kernel `kernel` is
+ * bracketed by cudaEventRecord(before) and cudaEventRecord(after) on the
+ * launch's stream, so cudaEventElapsedTime gives that launch's device time.
+ * Kernel ids: 0 pool update (qsa_pool_update), 1 block scores, 2 threshold
+ * filter, 3 final select + expansion (qsa_index_topk), 4 split attention,
+ * 5 split combine (qsa_sparse_attn).  `before`/`after` are cudaEvent_t
+ * handles; NULL clears.  QSA_ERR_INVALID_ARG for an unknown id. */
+qsa_status qsa_profile_kernel(int32_t kernel, void* before, void* after);
+
+const char* qsa_status_string(qsa_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QSA_H */

@@ -1,0 +1,125 @@
+"""Device-resident state of one QSA layer and its step.
+
+QSALayer owns the caller-side buffers of include/qsa.h (caches, block tables,
+the pooled block-key cache, workspaces, outputs) as torch CUDA tensors and
+runs a step as the three C-ABI calls on one stream:
+
+    pool_update(dirty) -> index_topk(tokens) -> sparse_attn(tokens)
+
+It holds no arithmetic of its own.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import qsa
+
+
+def _dev(x, dtype=None, device="cuda"):
+    t = torch.from_numpy(np.ascontiguousarray(x))
+    if dtype is not None:
+        t = t.to(dtype)
+    return t.to(device)
+
+
+class QSALayer:
+    def __init__(self, cfg: dict, idx_k, k_cache, v_cache, n_cells: int, blk_cells, slot_block_idx,
+                 seq_blk_off, seq_blk_slots, norm_w, max_blocks: int, max_tokens: int,
+                 device: str = "cuda"):
+        self.cfgd = dict(cfg)
+        self.cfg = qsa.config_from_dict(cfg)
+        self.device = device
+        self.n_cells = int(n_cells)
+        self.max_blocks = max(int(max_blocks), 1)
+        self.max_tokens = int(max_tokens)
+        self.idx_k = _dev(idx_k, device=device)
+        kv_dtype = torch.float16 if cfg["kv_type"] == "f16" else torch.uint8
+        self.k_cache = _dev(k_cache, device=device).view(kv_dtype)
+        self.v_cache = _dev(v_cache, device=device).view(kv_dtype)
+        self.blk_cells = _dev(blk_cells, device=device)
+        self.slot_block_idx = _dev(slot_block_idx, device=device)
+        self.seq_blk_off = _dev(seq_blk_off, device=device)
+        self.seq_blk_slots = _dev(seq_blk_slots, device=device)
+        self.norm_w = _dev(norm_w, device=device)
+        self.n_slots = int(self.blk_cells.shape[0])
+        self.pooled = torch.zeros((self.n_slots, cfg["idx_dim"]), dtype=torch.float32, device=device)
+        self.pitch = qsa.cells_per_token(self.cfg)
+        T = self.max_tokens
+        self.cells = torch.full((T, self.pitch), -1, dtype=torch.int32, device=device)
+        self.count = torch.zeros(T, dtype=torch.int32, device=device)
+        self.out = torch.zeros((T, cfg["n_q_heads"], cfg["head_dim"]), dtype=torch.float32, device=device)
+        self.ws_index = torch.empty(qsa.index_topk_workspace_size(self.cfg, T, self.max_blocks),
+                                    dtype=torch.uint8, device=device)
+        self.ws_attn = torch.empty(qsa.sparse_attn_workspace_size(self.cfg, T),
+                                   dtype=torch.uint8, device=device)
+
+    @classmethod
+    def from_workload(cls, wl, step: int = 0, max_tokens: Optional[int] = None, device="cuda"):
+        """Upload a qsa_workload.Workload with the block table as it stands
+        before steps[step] (that step's cells not yet appended)."""
+        T = max_tokens or max(len(s.tok_pos) for s in wl.steps)
+        return cls(wl.cfg, wl.idx_k, wl.k_cache, wl.v_cache, wl.n_cells, wl.blk_cells_state(step),
+                   wl.slot_block_idx, wl.seq_blk_off, wl.seq_blk_slots, wl.norm_w,
+                   wl.max_blocks(), T, device=device)
+
+    # ---- the three calls
+    def pool_update(self, dirty, stream=None):
+        d = dirty if isinstance(dirty, torch.Tensor) else _dev(np.asarray(dirty, dtype=np.int32), device=self.device)
+        qsa.pool_update(self.cfg, self.idx_k, self.blk_cells, self.slot_block_idx, d, self.norm_w,
+                        self.pooled, stream)
+
+    def index_topk(self, tok_seq, tok_pos, q_idx, w_idx, stream=None):
+        T = int(tok_pos.numel())
+        qsa.index_topk(self.cfg, q_idx, w_idx, tok_seq, tok_pos, self.pooled, self.blk_cells,
+                       self.seq_blk_off, self.seq_blk_slots, self.max_blocks, self.n_cells,
+                       self.cells[:T], self.count[:T], self.ws_index, stream)
+
+    def sparse_attn(self, q, n_tokens: int, stream=None):
+        T = int(n_tokens)
+        qsa.sparse_attn(self.cfg, q, self.k_cache, self.v_cache, self.n_cells, self.cells[:T],
+                        self.count[:T], self.out[:T], self.ws_attn, stream)
+
+    def step(self, tok_seq, tok_pos, q, q_idx, w_idx, dirty, stream=None):
+        """One QSA step for T tokens; returns the out[:T] view (fp32)."""
+        self.pool_update(dirty, stream)
+        self.index_topk(tok_seq, tok_pos, q_idx, w_idx, stream)
+        self.sparse_attn(q, int(tok_pos.numel()), stream)
+        return self.out[:int(tok_pos.numel())]
+
+    def set_cells(self, slots, rows):
+        """Write block-table rows (the append of new cells), device side."""
+        s = _dev(np.asarray(slots, dtype=np.int64), device=self.device)
+        self.blk_cells[s] = _dev(np.asarray(rows, dtype=np.int32), device=self.device)
+
+    def warm(self, dirty_all):
+        """Pool every listed slot (cold start / rebuild from the key cache)."""
+        self.pool_update(dirty_all)
+
+
+def step_inputs(st, device="cuda"):
+    """Device tensors of a qsa_workload.Step."""
+    return dict(tok_seq=_dev(st.tok_seq, device=device), tok_pos=_dev(st.tok_pos, device=device),
+                q=_dev(st.q, device=device), q_idx=_dev(st.q_idx, device=device),
+                w_idx=_dev(st.w_idx, device=device), dirty=_dev(st.dirty, device=device))
+
+
+def append_rows(wl, step: int):
+    """Block-table rows changed by steps[step]: (slots, rows) of the state
+    after the step's cells are appended (only the blocks the step touches)."""
+    r = wl.r
+    lens = wl.seq_len_after(step + 1)
+    slots, rows = [], []
+    for s, ps in enumerate(wl.steps[step].new_pos):
+        if len(ps) == 0:
+            continue
+        off = int(wl.seq_blk_off[s])
+        for j in sorted({int(p) // r for p in ps}):
+            row = np.full(r, -1, dtype=np.int32)
+            hi = min(lens[s], (j + 1) * r)
+            row[:hi - j * r] = wl.seq_cells[s][j * r:hi]
+            slots.append(int(wl.seq_blk_slots[off + j]))
+            rows.append(row)
+    return np.array(slots, dtype=np.int64), np.array(rows, dtype=np.int32).reshape(-1, r)

@@ -1,0 +1,115 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every symbol
+include/qsa.h declares, and rejects invalid calls on the host before any CUDA
+work.  No compute call is made here."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from sparse_attention_long_qsa_gb300 import build as qbuild
+from sparse_attention_long_qsa_gb300 import qsa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qsa.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    qbuild.build()
+    return qsa.lib()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qsa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = _declared()
+    assert names == sorted(qsa.EXPORTS)
+    out = os.popen(f"nm -D --defined-only {qsa.LIB_PATH}").read()
+    exported = set(re.findall(r" T (qsa_[a-z0-9_]+)", out))
+    for n in names:
+        assert n in exported, n
+        assert hasattr(L, n)
+
+
+def test_config_defaults_and_pitch(L):
+    c = qsa.config()
+    assert (c.n_q_heads, c.n_kv_heads, c.head_dim, c.n_idx_heads, c.idx_dim) == (16, 2, 256, 4, 128)
+    assert (c.compress_ratio, c.top_k, c.kv_type) == (4, 2048, 0)
+    assert c.rope_theta == 1e6 and abs(c.rms_eps - 1e-6) < 1e-12 and c.attn_scale == 1 / 16
+    assert qsa.cells_per_token(c) == 2051
+    assert qsa.cells_per_token(qsa.config(top_k=16)) == 19
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(head_dim=128), -3), (dict(idx_dim=64), -3), (dict(n_q_heads=12), -3),
+    (dict(top_k=2050), -3), (dict(compress_ratio=0), -1), (dict(kv_type=7), -1),
+    (dict(n_idx_heads=2), -3), (dict(rope_theta=-1.0), -1),
+])
+def test_config_rejected_before_launch(L, over, status):
+    c = qsa.config(**over)
+    fake = ctypes.c_void_p(0x10000)
+    st = L.qsa_pool_update(ctypes.byref(c), fake, 10, fake, fake, 10, fake, 4, fake, fake, None)
+    assert st == status
+    assert L.qsa_cells_per_token(ctypes.byref(c)) == -1
+
+
+def test_null_and_workspace_checks(L):
+    c = qsa.config()
+    fake = ctypes.c_void_p(0x10000)
+    # null pointer with work to do
+    assert L.qsa_pool_update(ctypes.byref(c), None, 10, fake, fake, 10, fake, 4, fake, fake, None) == -1
+    # nothing to do: no pointer is read
+    assert L.qsa_pool_update(ctypes.byref(c), None, 10, None, None, 10, None, 0, None, None, None) == 0
+    # negative sizes
+    assert L.qsa_pool_update(ctypes.byref(c), fake, -1, fake, fake, 10, fake, 4, fake, fake, None) == -1
+    need = L.qsa_index_topk_workspace_size(ctypes.byref(c), 5, 62_532)
+    assert need > 5 * 62_532 * 4
+    args = [ctypes.byref(c), 5] + [fake] * 6 + [100, fake, fake, 1, 62_532, 1000, fake, fake]
+    assert L.qsa_index_topk(*args, fake, need - 1, None) == -4
+    assert L.qsa_index_topk(*args, ctypes.c_void_p(0x10010), need, None) == -4   # misaligned
+    assert L.qsa_index_topk(*args, None, need, None) == -4
+    wa = L.qsa_sparse_attn_workspace_size(ctypes.byref(c), 5)
+    assert wa > 0
+    aargs = [ctypes.byref(c), 5, fake, fake, fake, 1000, fake, fake, fake]
+    assert L.qsa_sparse_attn(*aargs, fake, wa - 1, None) == -4
+    # misaligned K cache
+    bad = [ctypes.byref(c), 5, fake, ctypes.c_void_p(0x10002), fake, 1000, fake, fake, fake]
+    assert L.qsa_sparse_attn(*bad, fake, wa, None) == -1
+    assert L.qsa_index_topk(ctypes.byref(c), 70_000, *([fake] * 6), 100, fake, fake, 1, 10, 10,
+                            fake, fake, fake, need, None) == -3
+    assert L.qsa_status_string(-4) == b"workspace null, misaligned or too small"
+
+
+def test_blocks_dirty_host_helper(L):
+    rng = np.random.default_rng(0)
+    old = rng.integers(-1, 1000, (300, 4)).astype(np.int32)
+    new = old.copy()
+    for s in (3, 77, 78, 299):
+        new[s, rng.integers(0, 4)] += 1
+    got = qsa.blocks_dirty(old, new, 4)
+    np.testing.assert_array_equal(got, [3, 77, 78, 299])
+    new[5, 0] = -7
+    got = qsa.blocks_dirty(old, new, 4)
+    np.testing.assert_array_equal(got, [3, 5, 77, 78, 299, -1, -1, -1])
+    np.testing.assert_array_equal(qsa.blocks_dirty(old, old, 4), [-1, -1, -1, -1])
+    np.testing.assert_array_equal(qsa.blocks_dirty(old, old, 0), np.zeros(0, dtype=np.int32))
+    # capacity too small: status -2 and the needed length
+    n = ctypes.c_int32(0)
+    buf = np.zeros(2, dtype=np.int32)
+    st = L.qsa_blocks_dirty(old.ctypes.data, new.ctypes.data, 300, 4, buf.ctypes.data, 2, ctypes.byref(n), 4)
+    assert st == -2 and n.value == 8
+
+
+def test_binding_refuses_cpu_tensors(L):
+    import torch
+    c = qsa.config()
+    t = torch.zeros(4, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA"):
+        qsa.pool_update(c, torch.zeros((4, 128), dtype=torch.float16), torch.zeros((1, 4), dtype=torch.int32),
+                        torch.zeros(1, dtype=torch.int32), t, torch.ones(128), torch.zeros((1, 128)))
