@@ -36,7 +36,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "QSA-layer decode tokens/s at 50k/250k ctx (1 and 5 seqs); HBM GB/s vs peak"
-FLUSH_BYTES = 1 << 30
+FLUSH_BYTES = [1 << 30]   # L2 flush buffer (--flush-mb)
 
 DESCR = {
     "50k": "decode, 1 seq, 50,000-cell fp16 K/V prompt + 1 cell/step (tails cycle 1,2,3,0), "
@@ -247,7 +247,11 @@ def run_reference(args, rank, world):
 
 
 # ---------------------------------------------------------------------------
-def measure_config(name, K, W, dev, *, e2e=True, cpu=True, cpu_seconds=10.0, clocks=None, quiet=False):
+def measure_config(name, K, W, dev, *, e2e=True, clocks=None):
+    """Time K decode steps of workload `name`.  Each workload step is captured
+    once as a CUDA graph of the three C-ABI calls (pool_update, index_topk,
+    sparse_attn); a timed step is: append the step's block-table rows and
+    flush L2 (outside the events), record, replay, record."""
     import torch
     from qsa_workload import make_workload
     from sparse_attention_long_qsa_gb300 import qsa
@@ -263,96 +267,119 @@ def measure_config(name, K, W, dev, *, e2e=True, cpu=True, cpu_seconds=10.0, clo
     inputs = [step_inputs(st, device=dev) for st in wl.steps]
     appends = []
     for i in range(n_steps):
-        s, rows = append_rows(wl, i)
-        appends.append((torch.from_numpy(s).to(dev), torch.from_numpy(rows).to(dev)))
-    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    toks_per_step = [len(st.tok_pos) for st in wl.steps]
+        s_, rows = append_rows(wl, i)
+        appends.append((torch.from_numpy(s_).to(dev), torch.from_numpy(rows).to(dev)))
+    flush = torch.empty(FLUSH_BYTES[0] // 4, dtype=torch.float32, device=dev)
+    toks = [len(st.tok_pos) for st in wl.steps]
     alg = [algorithmic_bytes(wl, i) for i in range(n_steps)]
+    kernels = list(qsa.KERNELS)
 
     def do_append(i):
         if i == 0:
             L.blk_cells.copy_(tbl0)
-        s, rows = appends[i]
-        L.blk_cells[s] = rows
+        s_, rows = appends[i]
+        L.blk_cells[s_] = rows
 
-    kernels = list(qsa.KERNELS)
+    def order(start, n):
+        return [(start + k) % n_steps for k in range(n)]
 
-    def loop(nsteps, start, hook=None, e2e_bufs=None):
-        """Run nsteps steps from step index `start` (mod n_steps); returns
-        per-step device ms and the hooked kernels' per-launch ms."""
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(nsteps)]
-        hk = {k: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                  for _ in range(nsteps)] for k in (hook or [])}
-        idx = []
+    def set_state(start):
         L.blk_cells.copy_(tbl0)
         for i in range(start % n_steps):
             do_append(i)
-        for n in range(nsteps):
-            i = (start + n) % n_steps
-            idx.append(i)
+
+    # eager warm-up: loads the module and sets kernel attributes before capture
+    set_state(0)
+    for i in order(0, max(W, 1)):
+        do_append(i)
+        L.step(**inputs[i])
+    torch.cuda.synchronize()
+
+    def new_ev():
+        e = torch.cuda.Event(enable_timing=True)
+        e.record()
+        return e
+
+    host = None
+    if e2e:
+        host = []
+        for i, st in enumerate(wl.steps):
+            h = {k: torch.from_numpy(np.ascontiguousarray(getattr(st, k))).pin_memory()
+                 for k in ("tok_seq", "tok_pos", "q", "q_idx", "w_idx", "dirty")}
+            h["out"] = torch.empty((toks[i], wl.cfg["n_q_heads"], wl.cfg["head_dim"]),
+                                   dtype=torch.float32).pin_memory()
+            host.append(h)
+
+    def capture(i, hook, with_io=False):
+        evs = {k: (new_ev(), new_ev()) for k in hook}
+        torch.cuda.synchronize()
+        for k, (a, b) in evs.items():
+            qsa.profile_kernel(k, a, b)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            d = inputs[i]
+            if with_io:
+                for key in ("tok_seq", "tok_pos", "q", "q_idx", "w_idx", "dirty"):
+                    d[key].copy_(host[i][key], non_blocking=True)
+            L.step(**d)
+            if with_io:
+                host[i]["out"].copy_(L.out[:toks[i]], non_blocking=True)
+        for k in evs:
+            qsa.profile_kernel(k, None, None)
+        return g, evs
+
+    def replay(graphs, idx):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in idx]
+        set_state(idx[0])
+        for n, i in enumerate(idx):
             do_append(i)
             flush.fill_(float(n))
-            for k in hk:
-                qsa.profile_kernel(k, *hk[k][n])
             evs[n][0].record()
-            if e2e_bufs is None:
-                L.step(**inputs[i])
-            else:
-                h = e2e_bufs[i]
-                d = inputs[i]
-                for key in ("tok_seq", "tok_pos", "q", "q_idx", "w_idx", "dirty"):
-                    d[key].copy_(h[key], non_blocking=True)
-                L.step(**d)
-                h["out"].copy_(L.out[:toks_per_step[i]], non_blocking=True)
+            graphs[i][0].replay()
             evs[n][1].record()
-        for k in hk:
-            qsa.profile_kernel(k, None, None)
         torch.cuda.synchronize()
-        ms = [a.elapsed_time(b) for a, b in evs]
-        kms = {k: [a.elapsed_time(b) for a, b in hk[k]] for k in hk}
-        return idx, ms, kms
+        return [a.elapsed_time(b) for a, b in evs]
 
-    # warm-up, then a per-kernel breakdown pass (all kernels hooked, untimed for the headline)
-    loop(max(W, 1), 0)
-    bidx, _, kms = loop(min(n_steps, max(K, 8)), W, hook=kernels)
-    kern_us = {k: 1e3 * float(np.mean(v)) for k, v in kms.items()}
+    # per-kernel breakdown: every kernel hooked, each step replayed once
+    br_steps = order(W, min(n_steps, 64))
+    gb = {i: capture(i, kernels) for i in sorted(set(br_steps))}
+    replay(gb, br_steps)
+    kern_us = {k: 1e3 * float(np.mean([gb[i][1][k][0].elapsed_time(gb[i][1][k][1]) for i in gb]))
+               for k in kernels}
+    kbytes = {k: float(np.mean([alg[i][k] for i in gb])) for k in kernels}
     dominant = max(kern_us, key=kern_us.get)
+    del gb
 
-    # headline: K timed steps, the dominant kernel hooked for the roofline
+    # headline: K steps, the dominant kernel hooked
+    idx = order(W, K)
+    gh = {i: capture(i, [dominant]) for i in sorted(set(idx))}
     torch.cuda.synchronize()
     if clocks:
         clocks.start()
     wall0 = time.perf_counter()
-    idx, ms, dk = loop(K, W, hook=[dominant])
+    ms = replay(gh, idx)
     wall = time.perf_counter() - wall0
+    dom_ms = float(np.mean([gh[i][1][dominant][0].elapsed_time(gh[i][1][dominant][1]) for i in gh]))
+    dom_bytes = float(np.mean([alg[i][dominant] for i in gh]))
+    del gh
     dev_ms = float(np.sum(ms))
-    tokens = sum(toks_per_step[i] for i in idx)
-    value = tokens / (dev_ms / 1e3)
-    dom_ms = float(np.mean(dk[dominant]))
-    dom_bytes = float(np.mean([alg[i][dominant] for i in idx]))
-    kbytes = {k: float(np.mean([alg[i][k] for i in bidx])) for k in kernels}
-
-    res = dict(value=value, ms_per_step=dev_ms / K, tokens=tokens, wall_s=wall,
+    tokens = sum(toks[i] for i in idx)
+    res = dict(value=tokens / (dev_ms / 1e3), ms_per_step=dev_ms / K, tokens=tokens, wall_s=wall,
                dominant=dominant, dom_ms=dom_ms, dom_bytes=dom_bytes, kern_us=kern_us,
                kern_gbs={k: kbytes[k] / (kern_us[k] * 1e-6) / 1e9 for k in kernels if kern_us[k] > 0},
-               gen_s=t_gen, wl=wl, step_bytes=float(np.mean([sum(alg[i].values()) for i in idx])))
+               gen_s=t_gen, wl=wl, step_bytes=float(np.mean([sum(alg[i].values()) for i in idx])),
+               graph_steps=len(set(idx)))
 
     if e2e:
-        # same steps through the public API from pinned host buffers
-        bufs = []
-        hb = 0
-        for i, st in enumerate(wl.steps):
-            h = {k: torch.from_numpy(np.ascontiguousarray(getattr(st, k))).pin_memory()
-                 for k in ("tok_seq", "tok_pos", "q", "q_idx", "w_idx", "dirty")}
-            h["out"] = torch.empty((toks_per_step[i], 16, 256), dtype=torch.float32).pin_memory()
-            bufs.append(h)
-        idx2, ms2, _ = loop(K, W, e2e_bufs=bufs)
-        h2d = float(np.mean([sum(bufs[i][k].numel() * bufs[i][k].element_size()
-                                 for k in ("tok_seq", "tok_pos", "q", "q_idx", "w_idx", "dirty")) for i in idx2]))
-        d2h = float(np.mean([bufs[i]["out"].numel() * 4 for i in idx2]))
-        tok2 = sum(toks_per_step[i] for i in idx2)
-        res["e2e"] = {"value": tok2 / (float(np.sum(ms2)) / 1e3), "unit": "tokens/s",
+        # the same steps from pinned host buffers: inputs H2D and the output
+        # D2H inside each step's events
+        ge = {i: capture(i, [], with_io=True) for i in sorted(set(idx))}
+        ms2 = replay(ge, idx)
+        del ge
+        keys = ("tok_seq", "tok_pos", "q", "q_idx", "w_idx", "dirty")
+        h2d = float(np.mean([sum(host[i][k].numel() * host[i][k].element_size() for k in keys) for i in idx]))
+        d2h = float(np.mean([host[i]["out"].numel() * 4 for i in idx]))
+        res["e2e"] = {"value": tokens / (float(np.sum(ms2)) / 1e3), "unit": "tokens/s",
                       "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
     res["clocks"] = clocks.stop() if clocks else None
     st, flags = qsa.debug_check()
@@ -396,7 +423,7 @@ def run_native(args, rank, world, local):
     secondary = {}
     if args.secondary and rank == 0:
         for name in args.secondary.split(","):
-            if name == args.config or not name:
+            if name == args.config or name in ("", "none"):
                 continue
             r2 = measure_config(name, min(args.steps, 128), args.warmup, dev, e2e=False)
             secondary[name] = {
@@ -429,7 +456,8 @@ def run_native(args, rank, world, local):
         "data": "synthetic (seeded N(0,1) K/V/keys, U(0,1) weights)",
         "config": {"workload": DESCR[args.config], "name": args.config,
                    "tokens_per_step": len(wl.steps[0].tok_pos),
-                   "l2": "flushed before every step (1 GiB write), outside the step's events",
+                   "launch": "one CUDA graph per workload step (3 C-ABI calls, 6 kernels + 1 memset)",
+                   "l2": f"flushed before every step ({FLUSH_BYTES[0] >> 20} MiB write), outside the step's events",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"kernel": res["dominant"], "bound": "hbm", "achieved": achieved,
                      "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
@@ -459,10 +487,13 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--config", default="50k", choices=list(DESCR))
     ap.add_argument("--secondary", default="250k_q8,5x250k_q8",
-                    help="comma list of further workloads timed on rank 0 (empty: none)")
+                    help="comma list of further workloads timed on rank 0 ('none': no others)")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--flush-mb", type=int, default=1024,
+                    help="L2 flush write per step, MiB (must exceed the 129 MB L2)")
     args = ap.parse_args()
+    FLUSH_BYTES[0] = max(args.flush_mb, 256) << 20
     rank, world, local = _env_rank()
     if args.impl == "reference":
         run_reference(args, rank, world)

@@ -200,8 +200,10 @@ qsa_status qsa_debug_check(qsa_stream_t stream, uint32_t* flags);
 
 /* Measurement hook (host state, process-wide, not for concurrent use from
  * several host threads).  While set, each launch of kernel `kernel` is
- * bracketed by cudaEventRecord(before) and cudaEventRecord(after) on the
- * launch's stream, so cudaEventElapsedTime gives that launch's device time.
+ * bracketed by records of `before` and `after` on the launch's stream
+ * (cudaEventRecordExternal, so inside a stream capture they become event
+ * nodes that timestamp every replay), and cudaEventElapsedTime gives that
+ * launch's device time.
  * Kernel ids: 0 pool update (qsa_pool_update), 1 block scores, 2 threshold
  * filter, 3 final select + expansion (qsa_index_topk), 4 split attention,
  * 5 split combine (qsa_sparse_attn).  `before`/`after` are cudaEvent_t

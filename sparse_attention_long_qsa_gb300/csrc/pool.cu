@@ -8,11 +8,16 @@
 //
 // One warp per dirty slot.  Lane l owns dims {2l, 2l+1} and their NeoX partners
 // {64+2l, 64+2l+1}, so every rotation pair lives in one lane and a row of 128
-// fp16 keys is read as two coalesced 128-byte half2 sweeps.  The arithmetic is
-// fp64 (means of at most r fp16 values are exact; rotation angles reach
-// 2.5e5 rad at 250k context, where an fp32 angle would be off by ~1e-2 rad)
-// and the result is rounded to fp32 once.  The work is a few slots per decode
-// step, so fp64 throughput is irrelevant here.
+// fp16 keys is read as two coalesced 128-byte half2 sweeps.  Mean and RMS are
+// accumulated in fp64 (means of at most r fp16 values are exact).  Rotation
+// angles reach 2.5e5 rad at 250k context, where an fp32 angle would be off by
+// ~1e-2 rad: the angle pos * theta^(-2d/128) is formed in fp64 from
+// frequencies computed on the host in fp64, reduced to [-pi, pi] in fp64 with
+// a two-part 2*pi, and only the reduced angle (as an fp32 hi + lo pair) goes
+// through fp32 sincos, so no fp64 transcendental runs on the device (fp64
+// throughput on this part is a small fraction of fp32).
+#include <cmath>
+
 #include "qsa_internal.cuh"
 
 namespace qsa {
@@ -20,13 +25,33 @@ namespace {
 
 constexpr int kPoolWarps = 4;
 
+struct InvFreq {
+  double f[kIdxDim / 2];   // theta^(-2d/idx_dim), d < idx_dim/2
+};
+
+// cos and sin of an fp64 angle: reduction by 2*pi in fp64, then fp32 sincos of
+// the reduced angle split into hi + lo.
+__device__ __forceinline__ void sincos_reduced(double a, float* s, float* c) {
+  const double two_pi_hi = 6.283185307179586;          // fp64 nearest to 2*pi
+  const double two_pi_lo = 2.4492935982947064e-16;     // 2*pi - two_pi_hi
+  const double k = rint(a * 0.15915494309189535);      // a / (2*pi)
+  double r = fma(-k, two_pi_hi, a);
+  r = fma(-k, two_pi_lo, r);
+  const float rh = (float)r;
+  const float rl = (float)(r - (double)rh);
+  float sh, ch;
+  sincosf(rh, &sh, &ch);
+  *c = fmaf(-sh, rl, ch);
+  *s = fmaf(ch, rl, sh);
+}
+
 __global__ void __launch_bounds__(kPoolWarps * 32)
 k_pool_update(const __half* __restrict__ idx_k, int64_t n_cells,
               const int32_t* __restrict__ blk_cells,
               const int32_t* __restrict__ slot_block_idx, int64_t n_slots,
               const int32_t* __restrict__ dirty, int n_dirty,
               const float* __restrict__ norm_w, float* __restrict__ pooled,
-              int r, double theta, double eps, unsigned* err) {
+              int r, const InvFreq inv_freq, double eps, unsigned* err) {
   const int lane = threadIdx.x & 31;
   const int64_t w = (int64_t)blockIdx.x * kPoolWarps + (threadIdx.x >> 5);
   if (w >= n_dirty) return;
@@ -74,12 +99,9 @@ k_pool_update(const __half* __restrict__ idx_k, int64_t n_cells,
   // NeoX RoPE at the block's first position j*r: pair (d, d+64) turns by
   // pos * theta^(-2d/128).
   const double pos = (double)slot_block_idx[slot] * (double)r;
-  const double d0 = (double)(2 * lane), d1 = (double)(2 * lane + 1);
-  const double f0 = pow(theta, (-2.0 * d0) / (double)kIdxDim);
-  const double f1 = pow(theta, (-2.0 * d1) / (double)kIdxDim);
-  double s0, c0, s1, c1;
-  sincos(pos * f0, &s0, &c0);
-  sincos(pos * f1, &s1, &c1);
+  float s0, c0, s1, c1;
+  sincos_reduced(pos * inv_freq.f[2 * lane], &s0, &c0);
+  sincos_reduced(pos * inv_freq.f[2 * lane + 1], &s1, &c1);
   reinterpret_cast<float2*>(out)[lane] =
       make_float2((float)(x0 * c0 - y0 * s0), (float)(x1 * c1 - y1 * s1));
   reinterpret_cast<float2*>(out)[32 + lane] =
@@ -95,10 +117,13 @@ cudaError_t launch_pool_update(const qsa_config& cfg, const __half* idx_k, int64
                                cudaStream_t stream) {
   if (n_dirty <= 0) return cudaSuccess;
   const unsigned blocks = (unsigned)ceil_div(n_dirty, kPoolWarps);
+  InvFreq inv{};
+  for (int d = 0; d < kIdxDim / 2; ++d)
+    inv.f[d] = std::pow((double)cfg.rope_theta, (-2.0 * (double)d) / (double)kIdxDim);
   prof_before(kKPool, stream);
   k_pool_update<<<blocks, kPoolWarps * 32, 0, stream>>>(
       idx_k, n_cells, blk_cells, slot_block_idx, n_slots, dirty, n_dirty, norm_w, pooled,
-      cfg.compress_ratio, (double)cfg.rope_theta, (double)cfg.rms_eps, err);
+      cfg.compress_ratio, inv, (double)cfg.rms_eps, err);
   prof_after(kKPool, stream);
   return cudaGetLastError();
 }

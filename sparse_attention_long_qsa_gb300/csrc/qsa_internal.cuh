@@ -51,11 +51,13 @@ struct ProfileHook {
   cudaEvent_t after[kNumKernels];
 };
 extern ProfileHook g_profile;
+// External records, so that inside a stream capture they become event-record
+// nodes that timestamp each replay of the graph.
 inline void prof_before(int k, cudaStream_t s) {
-  if (g_profile.before[k]) cudaEventRecord(g_profile.before[k], s);
+  if (g_profile.before[k]) cudaEventRecordWithFlags(g_profile.before[k], s, cudaEventRecordExternal);
 }
 inline void prof_after(int k, cudaStream_t s) {
-  if (g_profile.after[k]) cudaEventRecord(g_profile.after[k], s);
+  if (g_profile.after[k]) cudaEventRecordWithFlags(g_profile.after[k], s, cudaEventRecordExternal);
 }
 
 // ---------------------------------------------------------------- launchers

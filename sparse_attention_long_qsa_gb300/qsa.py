@@ -24,7 +24,8 @@ STATUS = {0: "QSA_OK", -1: "QSA_ERR_INVALID_ARG", -2: "QSA_ERR_SHAPE", -3: "QSA_
 
 # Every symbol include/qsa.h declares.
 EXPORTS = ("qsa_config_init", "qsa_cells_per_token", "qsa_pool_update", "qsa_index_scores",
-           "qsa_index_topk_workspace_size", "qsa_index_topk", "qsa_sparse_attn_workspace_size",
+           "qsa_index_topk_workspace_size", "qsa_index_topk",
+           "qsa_sparse_attn_workspace_size",
            "qsa_sparse_attn", "qsa_blocks_dirty", "qsa_debug_check", "qsa_profile_kernel",
            "qsa_status_string")
 
@@ -233,6 +234,9 @@ def blocks_dirty(old_tbl: np.ndarray, new_tbl: np.ndarray, pad_pow2_min: int = 4
 def profile_kernel(kernel: str, before=None, after=None):
     """Record torch.cuda.Event `before`/`after` around each launch of the
     named kernel (pool, score, filter, final, attn, combine); None clears."""
+    for ev in (before, after):
+        if ev is not None and not ev.cuda_event:
+            ev.record()   # torch creates the CUDA event on first record
     eb = before.cuda_event if before is not None else None
     ea = after.cuda_event if after is not None else None
     _check(lib().qsa_profile_kernel(KERNELS[kernel], eb, ea), "qsa_profile_kernel")

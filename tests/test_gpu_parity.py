@@ -151,7 +151,7 @@ def test_heavy_ties_exact_on_gpu_scores():
 def test_attention_special_cases():
     """count 0 -> zeros; one cell -> its V row; identical K rows -> mean of V."""
     wl = make_workload(n_seq=1, prompt_len=300, n_steps=1, seed=9)
-    L = QSALayer.from_workload(wl, 0)
+    L = QSALayer.from_workload(wl, 0, max_tokens=3)
     q = torch.from_numpy(wl.steps[0].q).cuda().repeat(3, 1, 1)
     L.cells[:3] = -1
     L.cells[1, 0] = 17
