@@ -160,6 +160,31 @@ qsa_status qsa_index_topk(const qsa_config* cfg, int32_t n_tokens,
                           int32_t* cells, int32_t* count,
                           void* workspace, size_t ws_bytes, qsa_stream_t stream);
 
+/* qsa_index_topk_noalloc - the pages have no counterpart; this is a
+ * convenience of this library.  Same computation and outputs as
+ * qsa_index_topk, but the workspace is a static device array inside the
+ * library, so the caller passes inputs and outputs only and nothing is
+ * allocated.  It is for callers that cannot allocate device memory: plugins
+ * hosted by an engine that owns every device allocation through its own pool
+ * and gives the plugin no allocator, and code on a latency-critical path where
+ * cudaMalloc (which may synchronise the device) is not allowed.
+ * Limits: n_tokens <= 8 and max_blocks <= 262144 (1,048,576 cells per
+ * sequence at r = 4); larger calls return QSA_ERR_WORKSPACE and launch
+ * nothing.  The array takes 9 MiB on every GPU that loads the library, until
+ * the process exits.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress, with that device current) and caches it:
+ * make that first call before any stream capture.  All calls on a device share
+ * the one array: calls whose work overlaps on the GPU (other streams, other
+ * host threads) race and corrupt each other's results; serialise them.  Each
+ * call clears the part of the array that must start at zero. */
+qsa_status qsa_index_topk_noalloc(const qsa_config* cfg, int32_t n_tokens,
+                                  const float* q_idx, const float* w_idx,
+                                  const int32_t* tok_seq, const int32_t* tok_pos,
+                                  const float* pooled, const int32_t* blk_cells, int64_t n_slots,
+                                  const int64_t* seq_blk_off, const int32_t* seq_blk_slots,
+                                  int32_t n_seq, int64_t max_blocks, int64_t n_cells,
+                                  int32_t* cells, int32_t* count, qsa_stream_t stream);
+
 /* ---------------------------------------------------------------------------
  * S5+S6  qsa_sparse_attn  (issue #28734, fix summary, lever1 and sparse256;
  * q8_0: the author's q8-compact follow-up in the same issue)

@@ -3,6 +3,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "qsa_internal.cuh"
 
@@ -267,3 +268,77 @@ const char* qsa_status_string(qsa_status s) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// qsa_index_topk_noalloc: qsa_index_topk with its workspace in a static device
+// array, for callers that cannot allocate device memory themselves: plugins
+// hosted by an engine that owns every device allocation through its own pool
+// and hands the plugin no allocator, and code on a latency-critical path where
+// cudaMalloc (which may synchronise the device) is not allowed.
+//
+// The array lives in this library's device image: every GPU that loads the
+// library holds kNoAllocScratchBytes of it until the process exits.  Host code
+// cannot use the symbol as a device address, so the device address is looked
+// up once per device (with that device current) and cached.
+namespace {
+
+constexpr int kNoAllocMaxTokens = 8;
+constexpr int64_t kNoAllocMaxBlocks = 262144;        // 1,048,576 cells per sequence at r = 4
+constexpr size_t kNoAllocScratchBytes = 9u << 20;    // >= the workspace of 8 tokens x 262144 blocks
+constexpr int kNoAllocMaxDevices = 256;
+
+__device__ __align__(256) unsigned char g_qsa_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of the scratch array on the current device (set-up on the
+// first call per device).
+qsa_status noalloc_scratch(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return QSA_ERR_CUDA;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return QSA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_qsa_noalloc_scratch) != cudaSuccess || p == nullptr) return QSA_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return QSA_OK;
+}
+
+}  // namespace
+
+extern "C" qsa_status qsa_index_topk_noalloc(
+    const qsa_config* cfg, int32_t n_tokens, const float* q_idx, const float* w_idx,
+    const int32_t* tok_seq, const int32_t* tok_pos, const float* pooled, const int32_t* blk_cells,
+    int64_t n_slots, const int64_t* seq_blk_off, const int32_t* seq_blk_slots, int32_t n_seq,
+    int64_t max_blocks, int64_t n_cells, int32_t* cells, int32_t* count, qsa_stream_t stream) {
+  IndexArgs a{};
+  qsa_status st = fill_index_args(cfg, n_tokens, q_idx, w_idx, tok_seq, tok_pos, pooled, n_slots,
+                                  seq_blk_off, seq_blk_slots, n_seq, max_blocks, &a);
+  if (st != QSA_OK) return st;
+  if (n_cells < 0) return QSA_ERR_INVALID_ARG;
+  if (n_cells > kMaxI32) return QSA_ERR_UNSUPPORTED;
+  if (n_tokens == 0) return QSA_OK;
+  if (!blk_cells || !cells || !count) return QSA_ERR_INVALID_ARG;
+  const int64_t mb = max_blocks > 0 ? max_blocks : 1;
+  if (n_tokens > kNoAllocMaxTokens || mb > kNoAllocMaxBlocks ||
+      index_workspace_bytes(n_tokens, mb) > kNoAllocScratchBytes)
+    return QSA_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  st = noalloc_scratch(&scratch);
+  if (st != QSA_OK) return st;
+  a.blk_cells = blk_cells;
+  a.n_cells = n_cells;
+  unsigned* err = error_word();
+  if (err == nullptr) return QSA_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // The array keeps the previous call's contents: clear the counters and
+  // histograms that must start at zero.
+  size_t zoff = 0, zbytes = 0;
+  index_workspace_zero_range(n_tokens, mb, &zoff, &zbytes);
+  if (cudaMemsetAsync(static_cast<char*>(scratch) + zoff, 0, zbytes, s) != cudaSuccess) return QSA_ERR_CUDA;
+  return from_cuda(launch_index_topk(a, cells, count, scratch, err, s));
+}

@@ -509,6 +509,12 @@ size_t index_workspace_bytes(int n_tokens, int64_t max_blocks) {
   return carve(nullptr, n_tokens, max_blocks).total;
 }
 
+void index_workspace_zero_range(int n_tokens, int64_t max_blocks, size_t* offset, size_t* bytes) {
+  const Ws w = carve(reinterpret_cast<void*>(static_cast<uintptr_t>(256)), n_tokens, max_blocks);
+  *offset = static_cast<size_t>(static_cast<char*>(w.zero_base) - reinterpret_cast<char*>(static_cast<uintptr_t>(256)));
+  *bytes = w.zero_bytes;
+}
+
 cudaError_t launch_index_scores(const IndexArgs& a, float* scores, unsigned* err, cudaStream_t stream) {
   if (a.n_tokens <= 0 || a.max_blocks <= 0) return cudaSuccess;
   const int chunk = score_chunk(a.n_tokens, a.max_blocks);

@@ -89,6 +89,8 @@ struct IndexArgs {
 };
 
 size_t index_workspace_bytes(int n_tokens, int64_t max_blocks);
+// Byte range of the workspace that must be zero when a call starts.
+void index_workspace_zero_range(int n_tokens, int64_t max_blocks, size_t* offset, size_t* bytes);
 cudaError_t launch_index_scores(const IndexArgs& a, float* scores, unsigned* err, cudaStream_t stream);
 cudaError_t launch_index_topk(const IndexArgs& a, int32_t* cells, int32_t* count,
                               void* ws, unsigned* err, cudaStream_t stream);

@@ -24,7 +24,7 @@ STATUS = {0: "QSA_OK", -1: "QSA_ERR_INVALID_ARG", -2: "QSA_ERR_SHAPE", -3: "QSA_
 
 # Every symbol include/qsa.h declares.
 EXPORTS = ("qsa_config_init", "qsa_cells_per_token", "qsa_pool_update", "qsa_index_scores",
-           "qsa_index_topk_workspace_size", "qsa_index_topk",
+           "qsa_index_topk_workspace_size", "qsa_index_topk", "qsa_index_topk_noalloc",
            "qsa_sparse_attn_workspace_size",
            "qsa_sparse_attn", "qsa_blocks_dirty", "qsa_debug_check", "qsa_profile_kernel",
            "qsa_status_string")
@@ -78,6 +78,9 @@ def lib():
     L.qsa_index_topk.argtypes = [CP, _I32, _P, _P, _P, _P, _P, _P, _I64, _P, _P, _I32, _I64, _I64,
                                  _P, _P, _P, _SZ, _P]
     L.qsa_index_topk.restype = _I32
+    L.qsa_index_topk_noalloc.argtypes = [CP, _I32, _P, _P, _P, _P, _P, _P, _I64, _P, _P, _I32, _I64,
+                                         _I64, _P, _P, _P]
+    L.qsa_index_topk_noalloc.restype = _I32
     L.qsa_sparse_attn_workspace_size.argtypes = [CP, _I32]
     L.qsa_sparse_attn_workspace_size.restype = _SZ
     L.qsa_sparse_attn.argtypes = [CP, _I32, _P, _P, _P, _I64, _P, _P, _P, _P, _SZ, _P]
