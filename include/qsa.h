@@ -145,13 +145,18 @@ qsa_status qsa_index_scores(const qsa_config* cfg, int32_t n_tokens,
  *   count[t] = (#chosen blocks) * r + ((p + 1) mod r)
  * Entries of the row beyond count[t] are set to -1.  Blocks not yet complete
  * for the token are never scored (-inf in the reference description).
- * workspace: >= qsa_index_topk_workspace_size(cfg, n_tokens, max_blocks) bytes,
- * 256-byte aligned, contents on entry irrelevant (the call clears what it
- * needs).  Selection is exact on the fp32 scores: a radix select on their bit
- * patterns. */
-size_t qsa_index_topk_workspace_size(const qsa_config* cfg, int32_t n_tokens,
+ * Selection is exact on the fp32 scores: a radix select on their bit patterns.
+ * workspace: >= qsa_index_topk_workspace_size(cfg, max_tokens, max_blocks)
+ * bytes, 256-byte aligned, ZERO-FILLED ONCE before its first use.  Its layout
+ * depends on max_tokens only (per-token control words first, then scores), and
+ * every call leaves the control words zero again, so one workspace serves any
+ * number of calls with n_tokens <= max_tokens and any max_blocks it has room
+ * for, as long as max_tokens stays the same.  max_blocks <= 1,048,576;
+ * max_tokens <= 65535 (QSA_ERR_UNSUPPORTED beyond, QSA_ERR_SHAPE if
+ * n_tokens > max_tokens). */
+size_t qsa_index_topk_workspace_size(const qsa_config* cfg, int32_t max_tokens,
                                      int64_t max_blocks);
-qsa_status qsa_index_topk(const qsa_config* cfg, int32_t n_tokens,
+qsa_status qsa_index_topk(const qsa_config* cfg, int32_t n_tokens, int32_t max_tokens,
                           const float* q_idx, const float* w_idx,
                           const int32_t* tok_seq, const int32_t* tok_pos,
                           const float* pooled, const int32_t* blk_cells, int64_t n_slots,
@@ -190,12 +195,14 @@ qsa_status qsa_index_topk_noalloc(const qsa_config* cfg, int32_t n_tokens,
  * q8_0: the author's q8-compact follow-up in the same issue)
  * For token t, query head h, KV head g = h / (n_q_heads / n_kv_heads):
  *   out[t][h] = sum_{i < count[t]} softmax_i(attn_scale * q[t][h] . K[c_i][g]) V[c_i][g]
- * with c_i = cells[t][i] (row pitch qsa_cells_per_token).  Split-KV: each CTA
- * owns a range of the token's cells and writes a partial (max, sum, o); a
- * combine pass merges them with log-sum-exp weights.  fp32 accumulation.
- * count[t] == 0 gives zeros.  A cell outside [0, n_cells) is masked and
- * flagged.  workspace: >= qsa_sparse_attn_workspace_size(cfg, n_tokens) bytes,
- * 256-byte aligned. */
+ * with c_i = cells[t][i] (row pitch qsa_cells_per_token).  One thread-block
+ * cluster per (token, KV head): its CTAs take 128-cell tiles of the list,
+ * compute Q.K^T and P.V on tcgen05 tensor cores (fp16 operands, K/V q8_0
+ * rows dequantised to fp16 after the gather, fp32 accumulation), and merge
+ * their partial (max, sum, o) through distributed shared memory with
+ * log-sum-exp weights.  count[t] == 0 gives zeros.  A cell outside
+ * [0, n_cells) is masked and flagged.  The call needs no workspace
+ * (qsa_sparse_attn_workspace_size returns 0; `workspace` may be NULL). */
 size_t qsa_sparse_attn_workspace_size(const qsa_config* cfg, int32_t n_tokens);
 qsa_status qsa_sparse_attn(const qsa_config* cfg, int32_t n_tokens,
                            const void* q, const void* k_cache, const void* v_cache,
@@ -229,9 +236,9 @@ qsa_status qsa_debug_check(qsa_stream_t stream, uint32_t* flags);
  * (cudaEventRecordExternal, so inside a stream capture they become event
  * nodes that timestamp every replay), and cudaEventElapsedTime gives that
  * launch's device time.
- * Kernel ids: 0 pool update (qsa_pool_update), 1 block scores, 2 threshold
- * filter, 3 final select + expansion (qsa_index_topk), 4 split attention,
- * 5 split combine (qsa_sparse_attn).  `before`/`after` are cudaEvent_t
+ * Kernel ids: 0 pool update (qsa_pool_update), 1 block scores + threshold
+ * bin, 3 cluster select + expansion (qsa_index_topk), 4 attention
+ * (qsa_sparse_attn); 2 and 5 are reserved.  `before`/`after` are cudaEvent_t
  * handles; NULL clears.  QSA_ERR_INVALID_ARG for an unknown id. */
 qsa_status qsa_profile_kernel(int32_t kernel, void* before, void* after);
 

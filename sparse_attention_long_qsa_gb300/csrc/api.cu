@@ -47,7 +47,7 @@ qsa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QSA_OK : QSA_ERR
 
 constexpr int64_t kMaxI32 = 2147483647;
 
-qsa_status fill_index_args(const qsa_config* cfg, int32_t n_tokens, const float* q_idx,
+qsa_status fill_index_args(const qsa_config* cfg, int32_t n_tokens, int32_t max_tokens, const float* q_idx,
                            const float* w_idx, const int32_t* tok_seq, const int32_t* tok_pos,
                            const float* pooled, int64_t n_slots, const int64_t* seq_blk_off,
                            const int32_t* seq_blk_slots, int32_t n_seq, int64_t max_blocks,
@@ -55,14 +55,16 @@ qsa_status fill_index_args(const qsa_config* cfg, int32_t n_tokens, const float*
   qsa_status st = check_cfg(cfg);
   if (st != QSA_OK) return st;
   if (n_tokens < 0 || n_slots < 0 || n_seq < 0 || max_blocks < 0) return QSA_ERR_INVALID_ARG;
-  if (n_tokens > 65535) return QSA_ERR_UNSUPPORTED;
-  if (n_slots > kMaxI32 || max_blocks > kMaxI32 / 4) return QSA_ERR_UNSUPPORTED;
+  if (max_tokens < n_tokens) return QSA_ERR_SHAPE;
+  if (max_tokens > 65535) return QSA_ERR_UNSUPPORTED;
+  if (n_slots > kMaxI32 || max_blocks > index_max_blocks_limit()) return QSA_ERR_UNSUPPORTED;
   if (n_tokens > 0 && (!q_idx || !w_idx || !tok_seq || !tok_pos || !pooled || !seq_blk_off ||
                        !seq_blk_slots || n_seq <= 0))
     return QSA_ERR_INVALID_ARG;
   if (!aligned(q_idx, 16) || !aligned(pooled, 16) || !aligned(w_idx, 4) || !aligned(seq_blk_off, 8))
     return QSA_ERR_INVALID_ARG;
   a->n_tokens = n_tokens;
+  a->max_tokens = max_tokens;
   a->q_idx = q_idx;
   a->w_idx = w_idx;
   a->tok_seq = tok_seq;
@@ -130,7 +132,7 @@ qsa_status qsa_index_scores(const qsa_config* cfg, int32_t n_tokens, const float
                             const int32_t* seq_blk_slots, int32_t n_seq, int64_t max_blocks,
                             float* scores, qsa_stream_t stream) {
   IndexArgs a{};
-  qsa_status st = fill_index_args(cfg, n_tokens, q_idx, w_idx, tok_seq, tok_pos, pooled, n_slots,
+  qsa_status st = fill_index_args(cfg, n_tokens, n_tokens, q_idx, w_idx, tok_seq, tok_pos, pooled, n_slots,
                                   seq_blk_off, seq_blk_slots, n_seq, max_blocks, &a);
   if (st != QSA_OK) return st;
   if (n_tokens == 0 || max_blocks == 0) return QSA_OK;
@@ -140,19 +142,19 @@ qsa_status qsa_index_scores(const qsa_config* cfg, int32_t n_tokens, const float
   return from_cuda(launch_index_scores(a, scores, err, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-size_t qsa_index_topk_workspace_size(const qsa_config* cfg, int32_t n_tokens, int64_t max_blocks) {
-  if (check_cfg(cfg) != QSA_OK || n_tokens < 0 || max_blocks < 0) return 0;
-  return index_workspace_bytes(n_tokens, max_blocks > 0 ? max_blocks : 1);
+size_t qsa_index_topk_workspace_size(const qsa_config* cfg, int32_t max_tokens, int64_t max_blocks) {
+  if (check_cfg(cfg) != QSA_OK || max_tokens < 0 || max_blocks < 0) return 0;
+  return index_workspace_bytes(max_tokens, max_blocks > 0 ? max_blocks : 1);
 }
 
-qsa_status qsa_index_topk(const qsa_config* cfg, int32_t n_tokens, const float* q_idx,
+qsa_status qsa_index_topk(const qsa_config* cfg, int32_t n_tokens, int32_t max_tokens, const float* q_idx,
                           const float* w_idx, const int32_t* tok_seq, const int32_t* tok_pos,
                           const float* pooled, const int32_t* blk_cells, int64_t n_slots,
                           const int64_t* seq_blk_off, const int32_t* seq_blk_slots,
                           int32_t n_seq, int64_t max_blocks, int64_t n_cells, int32_t* cells,
                           int32_t* count, void* workspace, size_t ws_bytes, qsa_stream_t stream) {
   IndexArgs a{};
-  qsa_status st = fill_index_args(cfg, n_tokens, q_idx, w_idx, tok_seq, tok_pos, pooled, n_slots,
+  qsa_status st = fill_index_args(cfg, n_tokens, max_tokens, q_idx, w_idx, tok_seq, tok_pos, pooled, n_slots,
                                   seq_blk_off, seq_blk_slots, n_seq, max_blocks, &a);
   if (st != QSA_OK) return st;
   if (n_cells < 0) return QSA_ERR_INVALID_ARG;
@@ -160,7 +162,7 @@ qsa_status qsa_index_topk(const qsa_config* cfg, int32_t n_tokens, const float* 
   if (n_tokens == 0) return QSA_OK;
   if (!blk_cells || !cells || !count) return QSA_ERR_INVALID_ARG;
   if (workspace == nullptr || !aligned(workspace, 256) ||
-      ws_bytes < qsa_index_topk_workspace_size(cfg, n_tokens, max_blocks))
+      ws_bytes < qsa_index_topk_workspace_size(cfg, max_tokens, max_blocks))
     return QSA_ERR_WORKSPACE;
   a.blk_cells = blk_cells;
   a.n_cells = n_cells;
@@ -187,8 +189,8 @@ qsa_status qsa_sparse_attn(const qsa_config* cfg, int32_t n_tokens, const void* 
   if (!q || !k_cache || !v_cache || !cells || !count || !out) return QSA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 4))
     return QSA_ERR_INVALID_ARG;
-  if (workspace == nullptr || !aligned(workspace, 256) ||
-      ws_bytes < qsa_sparse_attn_workspace_size(cfg, n_tokens))
+  const size_t need = qsa_sparse_attn_workspace_size(cfg, n_tokens);
+  if (need > 0 && (workspace == nullptr || !aligned(workspace, 256) || ws_bytes < need))
     return QSA_ERR_WORKSPACE;
   AttnArgs a{};
   a.n_tokens = n_tokens;
@@ -315,18 +317,17 @@ extern "C" qsa_status qsa_index_topk_noalloc(
     const int32_t* tok_seq, const int32_t* tok_pos, const float* pooled, const int32_t* blk_cells,
     int64_t n_slots, const int64_t* seq_blk_off, const int32_t* seq_blk_slots, int32_t n_seq,
     int64_t max_blocks, int64_t n_cells, int32_t* cells, int32_t* count, qsa_stream_t stream) {
+  if (n_tokens > kNoAllocMaxTokens || max_blocks > kNoAllocMaxBlocks) return QSA_ERR_WORKSPACE;
   IndexArgs a{};
-  qsa_status st = fill_index_args(cfg, n_tokens, q_idx, w_idx, tok_seq, tok_pos, pooled, n_slots,
-                                  seq_blk_off, seq_blk_slots, n_seq, max_blocks, &a);
+  qsa_status st = fill_index_args(cfg, n_tokens, kNoAllocMaxTokens, q_idx, w_idx, tok_seq, tok_pos, pooled,
+                                  n_slots, seq_blk_off, seq_blk_slots, n_seq, max_blocks, &a);
   if (st != QSA_OK) return st;
   if (n_cells < 0) return QSA_ERR_INVALID_ARG;
   if (n_cells > kMaxI32) return QSA_ERR_UNSUPPORTED;
   if (n_tokens == 0) return QSA_OK;
   if (!blk_cells || !cells || !count) return QSA_ERR_INVALID_ARG;
   const int64_t mb = max_blocks > 0 ? max_blocks : 1;
-  if (n_tokens > kNoAllocMaxTokens || mb > kNoAllocMaxBlocks ||
-      index_workspace_bytes(n_tokens, mb) > kNoAllocScratchBytes)
-    return QSA_ERR_WORKSPACE;
+  if (index_workspace_bytes(kNoAllocMaxTokens, mb) > kNoAllocScratchBytes) return QSA_ERR_WORKSPACE;
   void* scratch = nullptr;
   st = noalloc_scratch(&scratch);
   if (st != QSA_OK) return st;

@@ -1,318 +1,687 @@
-// S5 + S6: split-KV sparse flash-decode over the selected cells.
+// S5 + S6: sparse flash-decode over the selected cells, on 5th-generation
+// tensor cores (tcgen05, accumulators in tensor memory), one thread-block
+// cluster per (token, KV head).
 //
 // llama.cpp issue #28734 ("decode slows linearly with context"), fix summary,
-// lever1: flash attention runs over only the top-k K/V set, so the cost is
-// O(top_k) instead of O(n_kv); sparse256: the head shape is DKQ = DV = 256
-// with 8 query heads per KV head (ncols2 = 8).  The author's q8-compact
-// follow-up keeps the sparse path for a q8_0 cache; here q8_0 rows are
-// gathered as int8 + fp16 scales and dequantised in shared memory, so the
-// whole cache is never converted (the O(n_kv) to_fp16 pass goodbadwolf's
-// comment in the same issue points at).  The API is indices-in: no mask is
-// built or re-scanned.
+// lever1: attention runs over only the top-k K/V set, so its cost is O(top_k)
+// instead of O(n_kv); sparse256: the head shape is DKQ = DV = 256 with 8 query
+// heads per KV head (ncols2 = 8).  The author's q8-compact follow-up keeps the
+// sparse path for a q8_0 cache; here q8_0 rows are dequantised after the
+// gather, so the whole cache is never converted (the O(n_kv) to_fp16 pass
+// goodbadwolf's comment in the same issue points at).  The API is indices-in:
+// no mask is built or re-scanned.
 //
-// Grid (split, KV head, token).  A CTA owns up to kCS consecutive entries of
-// the token's cell list: it gathers their K and V rows for its KV head with
-// 16-byte cp.async copies (all copies in flight at once), computes the 8
-// query heads' scores, a local softmax (max m, sum l) and the unnormalised
-// P.V, and writes the partial (m, l, o[256]) per head.  k_combine merges the
-// partials of a token with log-sum-exp weights.  fp32 accumulation.
+// Work split.  The token's cell list is cut into tiles of 128 cells; the
+// cluster's CTA r takes tiles r, r + NC, ... (NC = cluster size <= 16).  Per
+// tile a CTA
+//   1. gathers the 128 K rows and V rows of its KV head into shared memory in
+//      the 128-byte-swizzled canonical layout (16-byte cp.async for fp16; for
+//      q8_0 int8 rows + scales through registers, dequantised to fp16),
+//   2. S = K . Q^T with M = 128 cells, N = 16 (8 query heads + 8 zero rows),
+//      K = 256: 16 tcgen05.mma into tensor memory,
+//   3. reads S back (one cell per thread of warps 0-3), masks, takes the tile
+//      softmax statistics per head and writes P (fp16) to shared memory,
+//   4. O^T = V^T . P^T with M = 128 dims (two halves), N = 16, K = 128 cells:
+//      16 tcgen05.mma (V is the MN-major operand of the same swizzled tile),
+//   5. merges the tile into a running (max, sum, o) in registers.
+// Then every CTA stores its (max, sum, o) slices straight into the shared
+// memory of the CTA owning each range of dims (distributed shared memory), the
+// cluster synchronises once, and CTA r reduces dims [r*256/NC, ...) over all
+// NC partials from its own shared memory (log-sum-exp weights) and writes the
+// fp32 output.  No partials go to global memory and no second kernel runs.
+//
+// Waits on the MMA completion barrier are bounded: on timeout the CTA records
+// an error bit and keeps going through every barrier (its output is then
+// meaningless but nothing hangs).
 #include "qsa_internal.cuh"
+
+QSA_TS_DECLARE(attn)
 
 namespace qsa {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kAttnThreads = 256;
-constexpr int kCS = 64;   // cells per split
+constexpr int kThreads = 256;
+constexpr int kTile = 128;          // cells per MMA tile (M of the QK product)
+constexpr int kMaxCluster = 16;
+constexpr unsigned kErrTimeout = 32u;
+constexpr uint32_t kTmemCols = 64;  // S: cols [0,16); O half 0: [16,32); O half 1: [32,48)
 
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool pred) {
-  const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+// ---- shared-memory layout (offsets from a 1024-byte aligned base)
+constexpr uint32_t kOffK = 0;                       // 128 rows x 512 B, 4 column atoms of 16 KB
+constexpr uint32_t kOffV = kOffK + kTile * 512;     // same layout
+constexpr uint32_t kOffQ = kOffV + kTile * 512;     // 16 rows x 512 B, 4 atoms of 2 KB
+constexpr uint32_t kOffP = kOffQ + 16 * 512;        // 16 rows x 256 B, 2 atoms of 2 KB
+constexpr uint32_t kOffO = kOffP + 16 * 256;        // fp32 [NC][8][256/NC] partials pushed by the cluster
+constexpr uint32_t kOffM = kOffO + 8 * 256 * 4;     // fp32 [NC][16] their (max[8], sum[8])
+constexpr uint32_t kOffRed = kOffM + 16 * 16 * 4;   // fp32 [2][4][8] cross-warp reductions
+constexpr uint32_t kOffCell = kOffRed + 256;        // int [128]
+constexpr uint32_t kOffBar = kOffCell + kTile * 4;  // u64 mbarrier
+constexpr uint32_t kOffTmem = kOffBar + 8;          // u32 TMEM base address
+// overflow cells (past NC full tiles, at most kOvf) on CUDA cores, warps 4-7
+constexpr int kOvf = 32;
+constexpr uint32_t kOffXK = kOffTmem + 8;           // fp16 [kOvf][256] K rows
+constexpr uint32_t kOffXV = kOffXK + kOvf * 512;    // fp16 [kOvf][256] V rows
+constexpr uint32_t kOffXS = kOffXV + kOvf * 512;    // fp32 [kOvf][8] scores / probabilities
+constexpr uint32_t kOffXO = kOffXS + kOvf * 8 * 4;  // fp32 [8][256] partial output
+constexpr uint32_t kOffXM = kOffXO + 8 * 256 * 4;   // fp32 [8] max, [8] sum
+constexpr uint32_t kOffXC = kOffXM + 64;            // int [kOvf] cells
+constexpr uint32_t kSmemBytes = kOffXC + kOvf * 4 + 1024;   // + alignment slack
+
+// Byte offset of 16-byte chunk `c16` (0..31 along a 512-byte row) of row `row`
+// in a tile of `rows` rows stored as 128-byte swizzled atoms: atom column
+// c16 / 8 (64 fp16 values), row-major 128-byte rows inside it, the chunk index
+// XOR-ed with row % 8 (the 128B swizzle of the canonical UMMA layouts).
+__device__ __forceinline__ uint32_t sw128(uint32_t rows, uint32_t row, uint32_t c16) {
+  return (c16 >> 3) * rows * 128u + row * 128u + (((c16 & 7u) ^ (row & 7u)) << 4);
+}
+
+// Shared-memory matrix descriptor (tcgen05): start address, leading and stride
+// byte offsets (>> 4), descriptor version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulate, fp16 A and B,
+// M = 128, N = 16; A K-major (QK) or MN-major (PV), B K-major.
+constexpr uint32_t kIdescQK = (1u << 4) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
+constexpr uint32_t kIdescPV = kIdescQK | (1u << 15);
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t saddr, const void* gmem, bool pred) {
   const int sz = pred ? 16 : 0;
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem), "r"(sz) : "memory");
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(saddr), "l"(gmem), "r"(sz) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
 
-template <bool kQ8>
-struct AttnSmem;
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
 
-template <>
-struct AttnSmem<false> {
-  __half k[kCS][kHeadDim];
-  __half v[kCS][kHeadDim];
-  float q[kGqa][kHeadDim];
-  float p[kCS][kGqa];
-  int cell[kCS];
-  float m[kGqa], l[kGqa];
-};
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
+               : "memory");
+}
 
-template <>
-struct AttnSmem<true> {
-  int8_t k[kCS][kHeadDim];
-  int8_t v[kCS][kHeadDim];
-  __half ks[kCS][kHeadDim / 32];
-  __half vs[kCS][kHeadDim / 32];
-  float q[kGqa][kHeadDim];
-  float p[kCS][kGqa];
-  int cell[kCS];
-  float m[kGqa], l[kGqa];
-};
-
-__device__ __forceinline__ void h8_to_f(uint4 raw, float* f) {
-  const __half2* h = reinterpret_cast<const __half2*>(&raw);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 x = __half22float2(h[i]);
-    f[2 * i] = x.x;
-    f[2 * i + 1] = x.y;
+// Bounded wait on an mbarrier phase; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (int i = 0; i < (1 << 22); ++i) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (ok) return true;
   }
+  return false;
 }
 
-__device__ __forceinline__ void q8_to_f(uint2 raw, float scale, float* f) {
-  const int8_t* b = reinterpret_cast<const int8_t*>(&raw);
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float* v) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
 #pragma unroll
-  for (int i = 0; i < 8; ++i) f[i] = scale * (float)b[i];
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+
+// Barrier among the 128 threads of warps 0-3 (id 1) or of warps 4-7 (id 2).
+__device__ __forceinline__ void bar_half(int id) { asm volatile("bar.sync %0, 128;\n" ::"r"(id) : "memory"); }
+
+// 8 int8 values * scale -> 8 fp16 packed in a uint4.
+__device__ __forceinline__ uint4 dq8(uint2 raw, float s) {
+  const int8_t* b = reinterpret_cast<const int8_t*>(&raw);
+  uint4 o;
+  __half2* h = reinterpret_cast<__half2*>(&o);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(s * (float)b[2 * i], s * (float)b[2 * i + 1]);
+  return o;
 }
 
 template <bool kQ8>
-__global__ void __launch_bounds__(kAttnThreads)
-k_attn_split(const AttnArgs a, float* __restrict__ part_o, float2* __restrict__ part_ml,
-             int ns_max, unsigned* err) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  AttnSmem<kQ8>& sm = *reinterpret_cast<AttnSmem<kQ8>*>(smem_raw);
+__global__ void __launch_bounds__(kThreads, 1)
+k_attn_tc(const AttnArgs a, unsigned* err) {
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw_s = smem_u32(smem_raw);
+  const uint32_t base_s = (raw_s + 1023u) & ~1023u;
+  unsigned char* base = smem_raw + (base_s - raw_s);
+  const uint32_t sK = base_s + kOffK, sV = base_s + kOffV, sQ = base_s + kOffQ, sP = base_s + kOffP;
+  float* so = reinterpret_cast<float*>(base + kOffO);
+  float* sml = reinterpret_cast<float*>(base + kOffM);
+  float* sred = reinterpret_cast<float*>(base + kOffRed);
+  int* scell = reinterpret_cast<int*>(base + kOffCell);
+  const uint32_t bar = base_s + kOffBar;
+  uint32_t* stmem = reinterpret_cast<uint32_t*>(base + kOffTmem);
 
-  const int s = blockIdx.x, g = blockIdx.y, t = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = blockIdx.y, t = blockIdx.z;
+  const uint32_t rank = cluster_rank(), NC = cluster_size();
   const int G = a.n_kv_heads, Hq = G * kGqa;
+
+  QSA_TS(attn, 0);
+  // ---- prologue (inputs not produced by the preceding index kernels)
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(base_s + kOffTmem),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+  }
+  if (tid == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(bar) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  {
+    // Q rows 0..7 = the group's query heads, rows 8..15 zero; P rows 8..15 zero.
+    const __half* qg = a.q + ((int64_t)t * Hq + g * kGqa) * kHeadDim;
+    for (int i = tid; i < 16 * 32; i += kThreads) {
+      const int row = i >> 5, c16 = i & 31;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (row < kGqa) v = __ldg(reinterpret_cast<const uint4*>(qg + row * kHeadDim + c16 * 8));
+      *reinterpret_cast<uint4*>(base + kOffQ + sw128(16, row, c16)) = v;
+    }
+    for (int i = tid; i < 8 * 16; i += kThreads) {
+      const int row = 8 + (i >> 4), c16 = i & 15;
+      *reinterpret_cast<uint4*>(base + kOffP + sw128(16, row, c16)) = make_uint4(0, 0, 0, 0);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *stmem;
+
+  // ---- the cell list is written by the index kernels
+  QSA_TS(attn, 1);
+  grid_dep_wait();
+  grid_dep_launch();
+  QSA_TS(attn, 2);
+  const int32_t* crow = a.cells + (int64_t)t * a.cells_pitch;
+  // the first tile's cells and the count load together
+  int cfirst = -1;
+  if (tid < kTile && (int)rank * kTile + tid < a.cells_pitch) cfirst = crow[(int)rank * kTile + tid];
   int cnt = a.count[t];
   cnt = cnt < 0 ? 0 : (cnt > a.cells_pitch ? a.cells_pitch : cnt);
-  const int c0 = s * kCS;
-  if (c0 >= cnt) return;
-  const int nv = min(kCS, cnt - c0);
+  const int n_tiles = (cnt + kTile - 1) / kTile;
 
-  if (tid < kCS) {
-    int c = -1;
-    if (tid < nv) {
-      c = a.cells[(int64_t)t * a.cells_pitch + c0 + tid];
-      if (c < 0 || c >= a.n_cells) {
-        atomicOr(err, kErrCell);
-        c = -1;
+  float run_m[kGqa], run_l[kGqa], acc[2][kGqa];
+#pragma unroll
+  for (int h = 0; h < kGqa; ++h) {
+    run_m[h] = -INFINITY;
+    run_l[h] = 0.f;
+    acc[0][h] = acc[1][h] = 0.f;
+  }
+  uint32_t phase = 0;
+  bool timed_out = false;
+
+  // Cells past NC full tiles: when there are at most kOvf of them, CTA 0's
+  // warps 4-7 attend them on CUDA cores while warps 0-3 run its MMA tile;
+  // otherwise CTAs take further tiles in turn.
+  const int ovf_n = (n_tiles == (int)NC + 1) ? cnt - (int)NC * kTile : 0;
+  const bool use_ovf = ovf_n > 0 && ovf_n <= kOvf;
+  const int loop_tiles = use_ovf ? (int)NC : n_tiles;
+  const bool my_ovf = use_ovf && rank == 0;
+
+  for (int tile = (int)rank; tile < loop_tiles; tile += (int)NC) {
+    const int c0 = tile * kTile;
+    const int nv = min(kTile, cnt - c0);
+    if (tid < kTile) {
+      int c = -1;
+      if (tid < nv) {
+        c = (tile == (int)rank) ? cfirst : crow[c0 + tid];
+        if (c < 0 || c >= a.n_cells) {
+          atomicOr(err, kErrCell);
+          c = -1;
+        }
       }
+      scell[tid] = c;
     }
-    sm.cell[tid] = c;
-  }
-  {
-    const __half2* qg = reinterpret_cast<const __half2*>(a.q + ((int64_t)t * Hq + g * kGqa) * kHeadDim);
-    float* qs = &sm.q[0][0];
-    for (int i = tid; i < kGqa * kHeadDim / 2; i += kAttnThreads) {
-      const float2 f = __half22float2(qg[i]);
-      qs[2 * i] = f.x;
-      qs[2 * i + 1] = f.y;
-    }
-  }
-  __syncthreads();
+    __syncthreads();
+    QSA_TS(attn, 3 + 10 * (tile / (int)NC));
 
-  // Gather: K first (own commit group) so QK can start while V is in flight.
-  if constexpr (!kQ8) {
-    const __half* kb = static_cast<const __half*>(a.k_cache);
-    const __half* vb = static_cast<const __half*>(a.v_cache);
-    for (int id = tid; id < kCS * 32; id += kAttnThreads) {
-      const int row = id >> 5, col = id & 31, c = sm.cell[row];
-      cp_async16(&sm.k[row][col * 8], kb + ((int64_t)(c < 0 ? 0 : c) * G + g) * kHeadDim + col * 8, c >= 0);
-    }
-    cp_async_commit();
-    for (int id = tid; id < kCS * 32; id += kAttnThreads) {
-      const int row = id >> 5, col = id & 31, c = sm.cell[row];
-      cp_async16(&sm.v[row][col * 8], vb + ((int64_t)(c < 0 ? 0 : c) * G + g) * kHeadDim + col * 8, c >= 0);
-    }
-    cp_async_commit();
-  } else {
-    const int8_t* kq = static_cast<const int8_t*>(a.k_cache);
-    const int8_t* vq = static_cast<const int8_t*>(a.v_cache);
-    const int64_t nq = a.n_cells * (int64_t)G * kHeadDim;
-    const __half* kd = reinterpret_cast<const __half*>(kq + nq);
-    const __half* vd = reinterpret_cast<const __half*>(vq + nq);
-    for (int id = tid; id < kCS * 17; id += kAttnThreads) {
-      const int row = id / 17, col = id % 17, c = sm.cell[row];
+    // 1. gather K and V rows of KV head g into the swizzled tiles
+    if constexpr (!kQ8) {
+      const __half* kb = static_cast<const __half*>(a.k_cache);
+      const __half* vb = static_cast<const __half*>(a.v_cache);
+      for (int i = tid; i < kTile * 32; i += kThreads) {
+        const int row = i >> 5, c16 = i & 31, c = scell[row];
+        const int64_t off = ((int64_t)(c < 0 ? 0 : c) * G + g) * kHeadDim + c16 * 8;
+        cp_async16(sK + sw128(kTile, row, c16), kb + off, c >= 0);
+        cp_async16(sV + sw128(kTile, row, c16), vb + off, c >= 0);
+      }
+      asm volatile("cp.async.wait_all;\n" ::: "memory");
+    } else {
+      // thread -> (row, half): 128 int8 of K and of V plus their 4 scales each
+      const int8_t* kq = static_cast<const int8_t*>(a.k_cache);
+      const int8_t* vq = static_cast<const int8_t*>(a.v_cache);
+      const int64_t nq = a.n_cells * (int64_t)G * kHeadDim;
+      const __half* kd = reinterpret_cast<const __half*>(kq + nq);
+      const __half* vd = reinterpret_cast<const __half*>(vq + nq);
+      const int row = tid >> 1, half = tid & 1;
+      const int c = scell[row];
       const int64_t cg = (int64_t)(c < 0 ? 0 : c) * G + g;
-      if (col < 16) cp_async16(&sm.k[row][col * 16], kq + cg * kHeadDim + col * 16, c >= 0);
-      else cp_async16(&sm.ks[row][0], kd + cg * (kHeadDim / 32), c >= 0);
-    }
-    cp_async_commit();
-    for (int id = tid; id < kCS * 17; id += kAttnThreads) {
-      const int row = id / 17, col = id % 17, c = sm.cell[row];
-      const int64_t cg = (int64_t)(c < 0 ? 0 : c) * G + g;
-      if (col < 16) cp_async16(&sm.v[row][col * 16], vq + cg * kHeadDim + col * 16, c >= 0);
-      else cp_async16(&sm.vs[row][0], vd + cg * (kHeadDim / 32), c >= 0);
-    }
-    cp_async_commit();
-  }
-  cp_async_wait<1>();
-  __syncthreads();
-
-  // Scores: warp w owns cells 8w..8w+7, lane l owns dims 8l..8l+7.
-  {
-    float qr[kGqa][8];
+      uint4 kr[8], vr[8];
+      uint2 ks = make_uint2(0, 0), vs = make_uint2(0, 0);
+      if (c >= 0) {
+        const uint4* kp = reinterpret_cast<const uint4*>(kq + cg * kHeadDim + half * 128);
+        const uint4* vp = reinterpret_cast<const uint4*>(vq + cg * kHeadDim + half * 128);
 #pragma unroll
-    for (int h = 0; h < kGqa; ++h) {
-      const float4 x = *reinterpret_cast<const float4*>(&sm.q[h][8 * lane]);
-      const float4 y = *reinterpret_cast<const float4*>(&sm.q[h][8 * lane + 4]);
-      qr[h][0] = x.x; qr[h][1] = x.y; qr[h][2] = x.z; qr[h][3] = x.w;
-      qr[h][4] = y.x; qr[h][5] = y.y; qr[h][6] = y.z; qr[h][7] = y.w;
-    }
-    float v[64];
-#pragma unroll
-    for (int cc = 0; cc < 8; ++cc) {
-      const int cell = warp * 8 + cc;
-      float kf[8];
-      if constexpr (!kQ8) {
-        h8_to_f(*reinterpret_cast<const uint4*>(&sm.k[cell][8 * lane]), kf);
+        for (int j = 0; j < 8; ++j) {
+          kr[j] = __ldg(kp + j);
+          vr[j] = __ldg(vp + j);
+        }
+        ks = __ldg(reinterpret_cast<const uint2*>(kd + cg * 8 + half * 4));
+        vs = __ldg(reinterpret_cast<const uint2*>(vd + cg * 8 + half * 4));
       } else {
-        q8_to_f(*reinterpret_cast<const uint2*>(&sm.k[cell][8 * lane]),
-                __half2float(sm.ks[cell][lane >> 2]), kf);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) kr[j] = vr[j] = make_uint4(0, 0, 0, 0);
       }
+      const __half* ksh = reinterpret_cast<const __half*>(&ks);
+      const __half* vsh = reinterpret_cast<const __half*>(&vs);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        // 16 int8 = dims half*128 + 16j .. +15 -> two 16-byte fp16 chunks
+        const float skf = __half2float(ksh[j >> 1]), svf = __half2float(vsh[j >> 1]);
+        const int c16 = half * 16 + 2 * j;
+        *reinterpret_cast<uint4*>(base + kOffK + sw128(kTile, row, c16)) = dq8(make_uint2(kr[j].x, kr[j].y), skf);
+        *reinterpret_cast<uint4*>(base + kOffK + sw128(kTile, row, c16 + 1)) = dq8(make_uint2(kr[j].z, kr[j].w), skf);
+        *reinterpret_cast<uint4*>(base + kOffV + sw128(kTile, row, c16)) = dq8(make_uint2(vr[j].x, vr[j].y), svf);
+        *reinterpret_cast<uint4*>(base + kOffV + sw128(kTile, row, c16 + 1)) = dq8(make_uint2(vr[j].z, vr[j].w), svf);
+      }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    QSA_TS(attn, 4 + 10 * (tile / (int)NC));
+
+    if (warp < 4) {
+      // 2. S[cell][head] = K . Q^T
+      if (tid == 0) {
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+          const uint64_t ad = smem_desc(sK + (kk >> 2) * (kTile * 128) + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = smem_desc(sQ + (kk >> 2) * (16 * 128) + (kk & 3) * 32, 16, 1024);
+          mma_f16(tmem, ad, bd, kIdescQK, kk > 0);
+        }
+        mma_commit(bar);
+      }
+      if (!mbar_wait(bar, phase)) timed_out = true;
+      phase ^= 1;
+      tc_fence_after();
+      QSA_TS(attn, 5 + 10 * (tile / (int)NC));
+
+      // 3. tile softmax statistics and P (one cell per thread)
+      float sv[kGqa], tmax[kGqa], tsum[kGqa];
+      tmem_ld8(tmem + ((uint32_t)(32 * warp) << 16) + 0, sv);
+      const int cell = 32 * warp + lane;
+      const bool valid = cell < nv && scell[cell] >= 0;
 #pragma unroll
       for (int h = 0; h < kGqa; ++h) {
-        float acc = 0.f;
+        sv[h] = valid ? sv[h] * a.attn_scale : -INFINITY;
+        float m = sv[h];
 #pragma unroll
-        for (int d = 0; d < 8; ++d) acc = fmaf(qr[h][d], kf[d], acc);
-        v[cc * 8 + h] = acc;
+        for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+        if (lane == 0) sred[warp * 8 + h] = m;
+      }
+      bar_half(1);
+#pragma unroll
+      for (int h = 0; h < kGqa; ++h) {
+        tmax[h] = fmaxf(fmaxf(sred[h], sred[8 + h]), fmaxf(sred[16 + h], sred[24 + h]));
+        const float p = (tmax[h] == -INFINITY) ? 0.f : expf(sv[h] - tmax[h]);
+        const __half ph = __float2half_rn(p);
+        // the sum uses the rounded p the MMA sees
+        float e = __half2float(ph);
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) e += __shfl_xor_sync(kFull, e, o);
+        if (lane == 0) sred[32 + warp * 8 + h] = e;
+        // P row h, column `cell`: atom cell/64, chunk (cell%64)/8, element cell%8
+        const uint32_t off = (uint32_t)(cell >> 6) * (16 * 128) + h * 128 +
+                             ((((uint32_t)(cell & 63) >> 3) ^ (uint32_t)(h & 7)) << 4) + (cell & 7) * 2;
+        *reinterpret_cast<__half*>(base + kOffP + off) = ph;
+      }
+      fence_async_smem();
+      tc_fence_before();
+      bar_half(1);
+      tc_fence_after();
+#pragma unroll
+      for (int h = 0; h < kGqa; ++h)
+        tsum[h] = (sred[32 + h] + sred[40 + h]) + (sred[48 + h] + sred[56 + h]);
+      QSA_TS(attn, 6 + 10 * (tile / (int)NC));
+
+      // 4. O^T[dim][head] = V^T . P^T, two halves of 128 dims
+      if (tid == 0) {
+#pragma unroll
+        for (int mh = 0; mh < 2; ++mh) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t ad = smem_desc(sV + mh * 2 * (kTile * 128) + kk * 2048, kTile * 128, 1024);
+            const uint64_t bd = smem_desc(sP + (kk >> 2) * (16 * 128) + (kk & 3) * 32, 16, 1024);
+            mma_f16(tmem + 16 + 16 * mh, ad, bd, kIdescPV, kk > 0);
+          }
+        }
+        mma_commit(bar);
+      }
+      if (!mbar_wait(bar, phase)) timed_out = true;
+      phase ^= 1;
+      tc_fence_after();
+      QSA_TS(attn, 7 + 10 * (tile / (int)NC));
+
+      // 5. merge the tile into the running state (dims 32w+lane and +128)
+      float o0[8], o1[8];
+      tmem_ld8(tmem + ((uint32_t)(32 * warp) << 16) + 16, o0);
+      tmem_ld8(tmem + ((uint32_t)(32 * warp) << 16) + 32, o1);
+#pragma unroll
+      for (int h = 0; h < kGqa; ++h) {
+        const float mn = fmaxf(run_m[h], tmax[h]);
+        const float fa = (run_m[h] == -INFINITY) ? 0.f : expf(run_m[h] - mn);
+        const float fb = (tmax[h] == -INFINITY) ? 0.f : expf(tmax[h] - mn);
+        acc[0][h] = acc[0][h] * fa + o0[h] * fb;
+        acc[1][h] = acc[1][h] * fa + o1[h] * fb;
+        run_l[h] = run_l[h] * fa + tsum[h] * fb;
+        run_m[h] = mn;
+      }
+    } else if (my_ovf && tile == (int)rank) {
+      // Overflow cells on warps 4-7 (128 threads, tx = 0..127)
+      const int tx = tid - 128;
+      int* xc = reinterpret_cast<int*>(base + kOffXC);
+      float* xs = reinterpret_cast<float*>(base + kOffXS);
+      float* xo = reinterpret_cast<float*>(base + kOffXO);
+      float* xm = reinterpret_cast<float*>(base + kOffXM);
+      if (tx < kOvf) {
+        int c = -1;
+        if (tx < ovf_n) {
+          c = crow[(int)NC * kTile + tx];
+          if (c < 0 || c >= a.n_cells) {
+            atomicOr(err, kErrCell);
+            c = -1;
+          }
+        }
+        xc[tx] = c;
+      }
+      bar_half(2);
+      // gather the rows as plain fp16 [cell][256]
+      if constexpr (!kQ8) {
+        const __half* kb = static_cast<const __half*>(a.k_cache);
+        const __half* vb = static_cast<const __half*>(a.v_cache);
+        for (int i = tx; i < kOvf * 32; i += 128) {
+          const int row = i >> 5, c16 = i & 31, c = xc[row];
+          const int64_t off = ((int64_t)(c < 0 ? 0 : c) * G + g) * kHeadDim + c16 * 8;
+          cp_async16(base_s + kOffXK + row * 512 + c16 * 16, kb + off, c >= 0);
+          cp_async16(base_s + kOffXV + row * 512 + c16 * 16, vb + off, c >= 0);
+        }
+        asm volatile("cp.async.wait_all;\n" ::: "memory");
+      } else {
+        const int8_t* kq = static_cast<const int8_t*>(a.k_cache);
+        const int8_t* vq = static_cast<const int8_t*>(a.v_cache);
+        const int64_t nq = a.n_cells * (int64_t)G * kHeadDim;
+        const __half* kd = reinterpret_cast<const __half*>(kq + nq);
+        const __half* vd = reinterpret_cast<const __half*>(vq + nq);
+        for (int i = tx; i < kOvf * 16; i += 128) {   // (row, 16-value group)
+          const int row = i >> 4, grp = i & 15, c = xc[row];
+          uint4 kr = make_uint4(0, 0, 0, 0), vr = make_uint4(0, 0, 0, 0);
+          float sk = 0.f, svv = 0.f;
+          if (c >= 0) {
+            const int64_t cg = (int64_t)c * G + g;
+            kr = __ldg(reinterpret_cast<const uint4*>(kq + cg * kHeadDim + grp * 16));
+            vr = __ldg(reinterpret_cast<const uint4*>(vq + cg * kHeadDim + grp * 16));
+            sk = __half2float(kd[cg * 8 + (grp >> 1)]);
+            svv = __half2float(vd[cg * 8 + (grp >> 1)]);
+          }
+          uint4* kdst = reinterpret_cast<uint4*>(base + kOffXK + row * 512 + grp * 32);
+          uint4* vdst = reinterpret_cast<uint4*>(base + kOffXV + row * 512 + grp * 32);
+          kdst[0] = dq8(make_uint2(kr.x, kr.y), sk);
+          kdst[1] = dq8(make_uint2(kr.z, kr.w), sk);
+          vdst[0] = dq8(make_uint2(vr.x, vr.y), svv);
+          vdst[1] = dq8(make_uint2(vr.z, vr.w), svv);
+        }
+      }
+      bar_half(2);
+      // scores: thread -> (cell tx/4, heads 2*(tx%4), +1)
+      {
+        const int c = tx >> 2, h0 = 2 * (tx & 3);
+        const __half* kr = reinterpret_cast<const __half*>(base + kOffXK + c * 512);
+        float d0 = 0.f, d1 = 0.f;
+        for (int c16 = 0; c16 < 32; ++c16) {
+          const uint4 kv = *reinterpret_cast<const uint4*>(kr + c16 * 8);
+          const uint4 q0 = *reinterpret_cast<const uint4*>(base + kOffQ + sw128(16, h0, c16));
+          const uint4 q1 = *reinterpret_cast<const uint4*>(base + kOffQ + sw128(16, h0 + 1, c16));
+          const __half2* k2 = reinterpret_cast<const __half2*>(&kv);
+          const __half2* a2 = reinterpret_cast<const __half2*>(&q0);
+          const __half2* b2 = reinterpret_cast<const __half2*>(&q1);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 kf = __half22float2(k2[e]), af = __half22float2(a2[e]), bf = __half22float2(b2[e]);
+            d0 = fmaf(af.x, kf.x, fmaf(af.y, kf.y, d0));
+            d1 = fmaf(bf.x, kf.x, fmaf(bf.y, kf.y, d1));
+          }
+        }
+        const bool ok = c < ovf_n && xc[c] >= 0;
+        xs[c * 8 + h0] = ok ? d0 * a.attn_scale : -INFINITY;
+        xs[c * 8 + h0 + 1] = ok ? d1 * a.attn_scale : -INFINITY;
+      }
+      bar_half(2);
+      // softmax per head: 16 lanes per head, cells l and l+16
+      {
+        const int h = tx >> 4, l = tx & 15;
+        const float s0v = xs[l * 8 + h], s1v = xs[(l + 16) * 8 + h];
+        float m = fmaxf(s0v, s1v);
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+        const float p0 = (m == -INFINITY) ? 0.f : expf(s0v - m);
+        const float p1 = (m == -INFINITY) ? 0.f : expf(s1v - m);
+        float sum = p0 + p1;
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
+        xs[l * 8 + h] = p0;
+        xs[(l + 16) * 8 + h] = p1;
+        if (l == 0) {
+          xm[h] = m;
+          xm[8 + h] = sum;
+        }
+      }
+      bar_half(2);
+      // P.V: thread -> dims tx and tx + 128 for the 8 heads
+      {
+        float o[2][kGqa];
+#pragma unroll
+        for (int h = 0; h < kGqa; ++h) o[0][h] = o[1][h] = 0.f;
+        const __half* vx = reinterpret_cast<const __half*>(base + kOffXV);
+        for (int c = 0; c < ovf_n; ++c) {
+          const float v0 = __half2float(vx[c * kHeadDim + tx]);
+          const float v1 = __half2float(vx[c * kHeadDim + 128 + tx]);
+#pragma unroll
+          for (int h = 0; h < kGqa; ++h) {
+            const float p = xs[c * 8 + h];
+            o[0][h] = fmaf(p, v0, o[0][h]);
+            o[1][h] = fmaf(p, v1, o[1][h]);
+          }
+        }
+#pragma unroll
+        for (int h = 0; h < kGqa; ++h) {
+          xo[h * kHeadDim + tx] = o[0][h];
+          xo[h * kHeadDim + 128 + tx] = o[1][h];
+        }
       }
     }
-    // Reduce-scatter the 64 (cell, head) partial dots over the 32 lanes:
-    // lane L ends with entries 2L and 2L+1, i.e. cell L/4, heads 2(L%4)+{0,1}.
-#pragma unroll
-    for (int m = 16, n = 32; m >= 1; m >>= 1, n >>= 1) {
-      const bool upper = (lane & m) != 0;
-#pragma unroll
-      for (int i = 0; i < n; ++i) {
-        const float send = upper ? v[i] : v[i + n];
-        const float keep = upper ? v[i + n] : v[i];
-        v[i] = keep + __shfl_xor_sync(kFull, send, m);
-      }
-    }
-    const int cell = warp * 8 + (lane >> 2);
-    const int h0 = 2 * (lane & 3);
-    const bool valid = sm.cell[cell] >= 0;
-    sm.p[cell][h0] = valid ? v[0] * a.attn_scale : -INFINITY;
-    sm.p[cell][h0 + 1] = valid ? v[1] * a.attn_scale : -INFINITY;
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
   }
-  __syncthreads();
-
-  // Local softmax: warp h handles head h over the kCS cells.
-  {
-    const int h = warp;
-    const float x0 = sm.p[lane][h], x1 = sm.p[lane + 32][h];
-    float m = fmaxf(x0, x1);
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
-    const float e0 = (m == -INFINITY) ? 0.f : expf(x0 - m);
-    const float e1 = (m == -INFINITY) ? 0.f : expf(x1 - m);
-    float l = e0 + e1;
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) l += __shfl_xor_sync(kFull, l, o);
-    sm.p[lane][h] = e0;
-    sm.p[lane + 32][h] = e1;
-    if (lane == 0) {
-      sm.m[h] = m;
-      sm.l[h] = l;
-    }
-  }
-  cp_async_wait<0>();
-  __syncthreads();
-
-  // P.V: thread d owns output dim d for the 8 heads.
-  {
-    const int d = tid;
-    float o[kGqa];
-#pragma unroll
-    for (int h = 0; h < kGqa; ++h) o[h] = 0.f;
-    for (int c = 0; c < nv; ++c) {
-      float vv;
-      if constexpr (!kQ8) vv = __half2float(sm.v[c][d]);
-      else vv = __half2float(sm.vs[c][d >> 5]) * (float)sm.v[c][d];
-      const float4 p0 = *reinterpret_cast<const float4*>(&sm.p[c][0]);
-      const float4 p1 = *reinterpret_cast<const float4*>(&sm.p[c][4]);
-      o[0] = fmaf(p0.x, vv, o[0]); o[1] = fmaf(p0.y, vv, o[1]);
-      o[2] = fmaf(p0.z, vv, o[2]); o[3] = fmaf(p0.w, vv, o[3]);
-      o[4] = fmaf(p1.x, vv, o[4]); o[5] = fmaf(p1.y, vv, o[5]);
-      o[6] = fmaf(p1.z, vv, o[6]); o[7] = fmaf(p1.w, vv, o[7]);
-    }
+  // fold the overflow partial into warps 0-3's running state
+  if (my_ovf && warp < 4) {
+    const float* xo = reinterpret_cast<const float*>(base + kOffXO);
+    const float* xm = reinterpret_cast<const float*>(base + kOffXM);
 #pragma unroll
     for (int h = 0; h < kGqa; ++h) {
-      const int64_t row = ((int64_t)t * Hq + g * kGqa + h) * ns_max + s;
-      part_o[row * kHeadDim + d] = o[h];
-    }
-    if (tid < kGqa) {
-      const int64_t row = ((int64_t)t * Hq + g * kGqa + tid) * ns_max + s;
-      part_ml[row] = make_float2(sm.m[tid], sm.l[tid]);
+      const float mx = xm[h];
+      const float mn = fmaxf(run_m[h], mx);
+      const float fa = (run_m[h] == -INFINITY) ? 0.f : expf(run_m[h] - mn);
+      const float fb = (mx == -INFINITY) ? 0.f : expf(mx - mn);
+      acc[0][h] = acc[0][h] * fa + xo[h * kHeadDim + 32 * warp + lane] * fb;
+      acc[1][h] = acc[1][h] * fa + xo[h * kHeadDim + 128 + 32 * warp + lane] * fb;
+      run_l[h] = run_l[h] * fa + xm[8 + h] * fb;
+      run_m[h] = mn;
     }
   }
+  if (timed_out) atomicOr(err, kErrTimeout);
+
+  // ---- push this CTA's partial to the CTAs that own each dim range, then
+  // every CTA reduces its range from its own shared memory
+  const int dpc = (kHeadDim + (int)NC - 1) / (int)NC;   // dims per owner
+  if (warp < 4) {
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int d = half * 128 + 32 * warp + lane;
+      const uint32_t owner = (uint32_t)(d / dpc), e = (uint32_t)(d % dpc);
+#pragma unroll
+      for (int h = 0; h < kGqa; ++h)
+        st_dsmem_f32(dsmem_addr(&so[((int)rank * kGqa + h) * dpc + e], owner), acc[half][h]);
+    }
+  }
+  if (tid < (int)NC) {
+#pragma unroll
+    for (int h = 0; h < kGqa; ++h) {
+      st_dsmem_f32(dsmem_addr(&sml[(int)rank * 16 + h], (uint32_t)tid), run_m[h]);
+      st_dsmem_f32(dsmem_addr(&sml[(int)rank * 16 + 8 + h], (uint32_t)tid), run_l[h]);
+    }
+  }
+  QSA_TS(attn, 25);
+  cluster_sync();   // all pushes have landed; nobody touches a peer after this
+  QSA_TS(attn, 26);
+  {
+    const int d0 = (int)rank * dpc;
+    for (int i = tid; i < kGqa * dpc; i += kThreads) {
+      const int h = i / dpc, e = i % dpc, d = d0 + e;
+      if (d >= kHeadDim) continue;
+      float mx = -INFINITY;
+      for (int p = 0; p < (int)NC; ++p) mx = fmaxf(mx, sml[p * 16 + h]);
+      float num = 0.f, den = 0.f;
+      if (mx != -INFINITY) {
+        for (int p = 0; p < (int)NC; ++p) {
+          const float mp = sml[p * 16 + h];
+          const float w = (mp == -INFINITY) ? 0.f : expf(mp - mx);
+          den = fmaf(w, sml[p * 16 + 8 + h], den);
+          num = fmaf(w, so[(p * kGqa + h) * dpc + e], num);
+        }
+      }
+      a.out[((int64_t)t * Hq + g * kGqa + h) * kHeadDim + d] = den > 0.f ? num / den : 0.f;
+    }
+  }
+  QSA_TS(attn, 27);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTmemCols) : "memory");
 }
 
-__global__ void __launch_bounds__(kHeadDim)
-k_combine(const AttnArgs a, const float* __restrict__ part_o, const float2* __restrict__ part_ml, int ns_max) {
-  const int h = blockIdx.x, t = blockIdx.y, d = threadIdx.x;
-  const int Hq = a.n_kv_heads * kGqa;
-  int cnt = a.count[t];
-  cnt = cnt < 0 ? 0 : (cnt > a.cells_pitch ? a.cells_pitch : cnt);
-  const int ns = (int)ceil_div(cnt, kCS);
-  const int64_t row0 = ((int64_t)t * Hq + h) * ns_max;
-  float M = -INFINITY;
-  for (int s = 0; s < ns; ++s) M = fmaxf(M, part_ml[row0 + s].x);
-  float L = 0.f, o = 0.f;
-  if (M != -INFINITY) {
-    for (int s = 0; s < ns; ++s) {
-      const float2 ml = part_ml[row0 + s];
-      const float w = (ml.x == -INFINITY) ? 0.f : expf(ml.x - M);
-      L = fmaf(w, ml.y, L);
-      o = fmaf(w, part_o[(row0 + s) * kHeadDim + d], o);
+constexpr int kMaxDevices = 64;
+
+// Cluster size for a launch of `clusters` clusters: 16 CTAs (one per 128-cell
+// tile of the 2051-cell budget) when that many 16-CTA clusters are co-resident,
+// else the largest smaller power of two that fits them.
+template <bool kQ8>
+cudaError_t pick_cluster(const AttnArgs& a, int* nc_out) {
+  static int max_active[kMaxDevices][5];   // per device: clusters of 16, 8, 4, 2, 1
+  static bool configured[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(k_attn_tc<kQ8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_attn_tc<kQ8>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    for (int i = 0; i < 5; ++i) {
+      const int nc = 16 >> i;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)nc, 1, 1);
+      cfg.blockDim = dim3(kThreads, 1, 1);
+      cfg.dynamicSmemBytes = kSmemBytes;
+      cudaLaunchAttribute attr;
+      attr.id = cudaLaunchAttributeClusterDimension;
+      attr.val.clusterDim.x = (unsigned)nc;
+      attr.val.clusterDim.y = 1;
+      attr.val.clusterDim.z = 1;
+      cfg.attrs = &attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, k_attn_tc<kQ8>, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        n = 0;
+      }
+      max_active[dev][i] = n;
+    }
+    configured[dev] = true;
+  }
+  const int tiles = (int)ceil_div(a.cells_pitch, kTile);
+  const int want = tiles < kMaxCluster ? tiles : kMaxCluster;
+  const int clusters = a.n_tokens * a.n_kv_heads;
+  int nc = 0, largest = 1;
+  for (int i = 0; i < 5; ++i) {            // sizes 16, 8, 4, 2, 1
+    const int c = 16 >> i;
+    if (c > want || max_active[dev][i] <= 0) continue;
+    if (largest == 1 && c > 1) largest = c;
+    if (clusters <= max_active[dev][i]) {  // the largest size that runs in one wave
+      nc = c;
+      break;
     }
   }
-  a.out[((int64_t)t * Hq + h) * kHeadDim + d] = L > 0.f ? o / L : 0.f;
+  if (nc == 0) nc = largest;               // several waves either way: fewest tiles per CTA
+  *nc_out = nc;
+  return cudaSuccess;
 }
 
 template <bool kQ8>
-cudaError_t launch_split(const AttnArgs& a, float* po, float2* pml, int ns_max, unsigned* err,
-                         cudaStream_t stream) {
-  const size_t smem = sizeof(AttnSmem<kQ8>);
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(k_attn_split<kQ8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
-  const dim3 grid((unsigned)ns_max, (unsigned)a.n_kv_heads, (unsigned)a.n_tokens);
-  prof_before(kKAttn, stream);
-  k_attn_split<kQ8><<<grid, kAttnThreads, smem, stream>>>(a, po, pml, ns_max, err);
-  prof_after(kKAttn, stream);
-  return cudaGetLastError();
+cudaError_t launch_tc(const AttnArgs& a, unsigned* err, cudaStream_t stream) {
+  int nc = 1;
+  cudaError_t e = pick_cluster<kQ8>(a, &nc);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)nc, (unsigned)a.n_kv_heads, (unsigned)a.n_tokens);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)nc;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, k_attn_tc<kQ8>, a, err);
 }
 
 }  // namespace
 
-size_t attn_workspace_bytes(int n_tokens, int n_q_heads, int cells_pitch) {
-  const int64_t ns = ceil_div(cells_pitch, kCS);
-  const int64_t rows = (int64_t)n_tokens * n_q_heads * ns;
-  return (size_t)round_up(rows * kHeadDim * (int64_t)sizeof(float), 256) +
-         (size_t)round_up(rows * (int64_t)sizeof(float2), 256);
-}
+size_t attn_workspace_bytes(int, int, int) { return 0; }
 
-cudaError_t launch_sparse_attn(const AttnArgs& a, void* ws, unsigned* err, cudaStream_t stream) {
+cudaError_t launch_sparse_attn(const AttnArgs& a, void*, unsigned* err, cudaStream_t stream) {
   if (a.n_tokens <= 0) return cudaSuccess;
-  const int ns_max = (int)ceil_div(a.cells_pitch, kCS);
-  const int Hq = a.n_kv_heads * kGqa;
-  const int64_t rows = (int64_t)a.n_tokens * Hq * ns_max;
-  float* po = static_cast<float*>(ws);
-  float2* pml = reinterpret_cast<float2*>(static_cast<char*>(ws) +
-                                          round_up(rows * kHeadDim * (int64_t)sizeof(float), 256));
-  cudaError_t e = a.kv_q8 ? launch_split<true>(a, po, pml, ns_max, err, stream)
-                          : launch_split<false>(a, po, pml, ns_max, err, stream);
+  prof_before(kKAttn, stream);
+  cudaError_t e = a.kv_q8 ? launch_tc<true>(a, err, stream) : launch_tc<false>(a, err, stream);
+  prof_after(kKAttn, stream);
   if (e != cudaSuccess) return e;
-  prof_before(kKCombine, stream);
-  k_combine<<<dim3((unsigned)Hq, (unsigned)a.n_tokens), kHeadDim, 0, stream>>>(a, po, pml, ns_max);
-  prof_after(kKCombine, stream);
   return cudaGetLastError();
 }
 

@@ -14,22 +14,26 @@
 //   S[t][j] = sum_h w[t][h] * max(0, q_idx[t][h] . pooled[slot(seq, j)])
 // in fp32.
 //
-// Kernels (one call = one memset + three launches, no host round trip):
+// Two kernels, chained by programmatic dependent launch, no host round trip:
 //   k_score   streams the pooled rows of every visible block (the dominant
 //             HBM traffic at long context: 512 B per block), writes fp32
-//             scores and a 4096-bin histogram of the top 12 bits of the
-//             order-preserving score key; the last CTA of a token (atomic
-//             ticket, no waiting) locates the bin holding the B-th largest.
-//   k_filter  re-reads the (L2-resident) scores: blocks above the threshold
-//             bin go straight into a per-token selection bitmap (warp ballot,
-//             one word per 32 blocks), blocks in the bin are appended to a
-//             candidate list as unique 64-bit keys (score bits, ~index).
-//   k_final   one CTA per token: radix select among the candidates (held in
-//             registers) of exactly the number still needed - unique keys
-//             make ties resolve to the lower block index - then an ordered
-//             compaction of the bitmap (block ascending) that writes the
-//             member cells of each chosen block and the tail cells.
+//             scores and adds each block to a per-token 4096-bin histogram of
+//             the top 12 bits of the order-preserving score key.
+//   k_select  one thread-block cluster per token.  Every CTA reads the
+//             histogram and finds the bin holding the B-th largest score.
+//             Each CTA then takes a range of blocks: blocks above that bin go
+//             straight into its shared selection bitmap (warp ballots), blocks
+//             in the bin become unique 56-bit keys (low score bits,
+//             complemented index).  The cluster runs a radix select over
+//             those keys, one 8-bit digit per round, summing the CTAs' digit
+//             histograms through distributed shared memory; unique keys make
+//             ties resolve to the lower block index.  Finally every CTA writes
+//             the member cells of its chosen blocks at its offset in the
+//             token's list (blocks ascending), CTA 0 appends the tail cells
+//             and clears the histogram for the next call.
 #include "qsa_internal.cuh"
+
+QSA_TS_DECLARE(index)
 
 namespace qsa {
 namespace {
@@ -40,46 +44,29 @@ constexpr int kScoreWarps = kScoreThreads / 32;
 constexpr int kScoreUnroll = 2;
 // rows (blocks) one CTA covers per iteration: 8 warps x 4 rows x unroll
 constexpr int kRowsPerIter = kScoreWarps * 4 * kScoreUnroll;
-constexpr int kFilterThreads = 256;
-constexpr int kFilterWordsPerCta = 32;
 constexpr int kErrToken = 16;
 
-struct Ws {
-  float* scores;              // [T][max_blocks]
-  unsigned* hist;             // [T][kHistBins]   } cleared
-  unsigned* done;             // [T]              } by every
-  unsigned* cand_cnt;         // [T]              } call
-  int4* state;                // [T]              } {threshold bin, still needed, candidates, nb}
-  unsigned* bitmap;           // [T][wpitch]
-  unsigned long long* cand;   // [T][kCandCap]
-  void* zero_base;
-  size_t zero_bytes;
-  int64_t wpitch;
-  size_t total;
-};
+constexpr int kSelThreads = 512;
+constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kSelCluster = 8;
+constexpr int kSelMaxWords = 4096;        // bitmap words per CTA: 131072 blocks
+constexpr int kSelLocalCand = 2048;       // candidate keys held per CTA
+constexpr int kSelBatch = 16;             // score words a warp loads before using any
+constexpr int kSelSlots = 16384;          // slot ids a CTA prefetches (rank 0: all, when they fit)
+constexpr int kCentralBlocks = kSelMaxWords * 32 / 2;   // tokens up to 65536 blocks finish in CTA 0
+constexpr int kRankMax = 1024;            // threshold-bin keys resolved by direct ranking
+constexpr int kSelList = 2048;            // chosen blocks a CTA lists before expanding
 
-Ws carve(void* base, int T, int64_t max_blocks) {
-  Ws w{};
-  char* p = static_cast<char*>(base);
-  size_t off = 0;
-  auto take = [&](size_t bytes) {
-    char* q = p ? p + off : nullptr;
-    off += (size_t)round_up((int64_t)bytes, 256);
-    return q;
-  };
-  w.scores = reinterpret_cast<float*>(take(sizeof(float) * (size_t)T * (size_t)max_blocks));
-  const size_t zoff = off;
-  w.hist = reinterpret_cast<unsigned*>(take(sizeof(unsigned) * (size_t)T * kHistBins));
-  w.done = reinterpret_cast<unsigned*>(take(sizeof(unsigned) * (size_t)T));
-  w.cand_cnt = reinterpret_cast<unsigned*>(take(sizeof(unsigned) * (size_t)T));
-  w.state = reinterpret_cast<int4*>(take(sizeof(int4) * (size_t)T));
-  w.zero_base = p ? p + zoff : nullptr;
-  w.zero_bytes = off - zoff;
-  w.wpitch = round_up(ceil_div(max_blocks, 32), 4);
-  w.bitmap = reinterpret_cast<unsigned*>(take(sizeof(unsigned) * (size_t)T * (size_t)w.wpitch));
-  w.cand = reinterpret_cast<unsigned long long*>(take(sizeof(unsigned long long) * (size_t)T * kCandCap));
-  w.total = off;
-  return w;
+// Per-token histogram at the front of the workspace.  Zero on first use;
+// every call leaves it zero again.
+constexpr size_t kCtrlBytes = sizeof(unsigned) * kHistBins;
+
+__host__ __device__ __forceinline__ unsigned* hist_of(void* ws, int t) {
+  return reinterpret_cast<unsigned*>(static_cast<char*>(ws) + (size_t)t * kCtrlBytes);
+}
+
+__host__ __device__ __forceinline__ float* scores_of(void* ws, int max_tokens) {
+  return reinterpret_cast<float*>(static_cast<char*>(ws) + round_up((int64_t)max_tokens * kCtrlBytes, 256));
 }
 
 // Per-token geometry, validated against the caller's bounds.
@@ -157,7 +144,7 @@ __device__ __forceinline__ unsigned block_prefix_exclusive(unsigned v, unsigned*
   return x - v + below;
 }
 
-// Unique 56-bit selection key of a candidate inside the threshold bin: the 20
+// Unique 56-bit selection key of a block inside the threshold bin: the 20
 // low bits of the score key above the bitwise complement of the block index,
 // so a larger key means a larger score, or an equal score at a lower index.
 __device__ __forceinline__ unsigned long long cand_key(uint32_t key, int64_t j) {
@@ -173,27 +160,29 @@ __device__ __forceinline__ unsigned long long cand_key(uint32_t key, int64_t j) 
 // group with a reduce-scatter (6 shuffles per row in all).
 template <bool kTopk>
 __global__ void __launch_bounds__(kScoreThreads, 2)
-k_score(const IndexArgs a, float* __restrict__ scores, unsigned* __restrict__ hist,
-        unsigned* __restrict__ done, int4* __restrict__ state, int chunk, unsigned* err) {
+k_score(const IndexArgs a, void* ws, float* __restrict__ scores, int chunk, unsigned* err) {
+  // Shared histogram of this CTA's rows plus the list of bins it touched, so
+  // the flush to the token's global histogram costs one atomic per touched
+  // bin instead of a sweep of all bins.
   __shared__ unsigned s_hist[kTopk ? kHistBins : 1];
-  __shared__ unsigned s_warp[32];
-  __shared__ int s_last;
+  __shared__ unsigned short s_touched[kTopk ? kHistBins : 1];
+  __shared__ unsigned s_ntouched;
 
   const int t = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (kTopk) QSA_TS(index, 0);
+  // ---- before the wait: token geometry, query, first slot ids (not written
+  // by the pool update that precedes this kernel)
   const Tok tk = token_geometry(a, t, err, blockIdx.x == 0 && tid == 0);
   const int nb = tk.nb;
   float* srow = scores + (int64_t)t * a.max_blocks;
   const int64_t j0 = (int64_t)blockIdx.x * chunk;
   const int64_t j1 = min((int64_t)nb, j0 + chunk);
-
   if (kTopk) {
     for (int i = tid; i < kHistBins; i += kScoreThreads) s_hist[i] = 0u;
-    __syncthreads();
-  } else {
-    const int64_t f1 = min(a.max_blocks, j0 + chunk);
-    for (int64_t j = max((int64_t)nb, j0) + tid; j < f1; j += kScoreThreads) srow[j] = -INFINITY;
+    if (tid == 0) s_ntouched = 0u;
   }
+  unsigned* ghist = kTopk ? hist_of(ws, t) : nullptr;
 
   const int sub = lane & 7, grp = lane >> 3;
   float4 qv[kIdxHeads][4];
@@ -208,7 +197,28 @@ k_score(const IndexArgs a, float* __restrict__ scores, unsigned* __restrict__ hi
   const int bit2 = (lane >> 2) & 1, bit1 = (lane >> 1) & 1;
   const float wh = __ldg(a.w_idx + (int64_t)t * kIdxHeads + bit2 * 2 + bit1);
   const int32_t* slots = a.seq_blk_slots + tk.off;
+  int slot0[kScoreUnroll];
+  {
+    const int64_t base = j0 + warp * 4 * kScoreUnroll;
+#pragma unroll
+    for (int u = 0; u < kScoreUnroll; ++u) {
+      const int64_t j = base + u * 4 + grp;
+      slot0[u] = j < j1 ? __ldg(slots + j) : 0;
+    }
+  }
 
+  // ---- pooled rows are written by the pool update
+  if (kTopk) QSA_TS(index, 1);
+  grid_dep_wait();
+  grid_dep_launch();
+  if (kTopk) QSA_TS(index, 2);
+  if (!kTopk) {
+    const int64_t f1 = min(a.max_blocks, j0 + chunk);
+    for (int64_t j = max((int64_t)nb, j0) + tid; j < f1; j += kScoreThreads) srow[j] = -INFINITY;
+  }
+  if (kTopk) __syncthreads();
+
+  bool first = true;
   for (int64_t base = j0 + warp * 4 * kScoreUnroll; base < j1; base += kRowsPerIter) {
     float4 kv[kScoreUnroll][4];
     bool ok[kScoreUnroll], live[kScoreUnroll];
@@ -216,7 +226,7 @@ k_score(const IndexArgs a, float* __restrict__ scores, unsigned* __restrict__ hi
     for (int u = 0; u < kScoreUnroll; ++u) {
       const int64_t j = base + u * 4 + grp;
       live[u] = j < j1;
-      int slot = live[u] ? __ldg(slots + j) : 0;
+      int slot = first ? slot0[u] : (live[u] ? __ldg(slots + j) : 0);
       ok[u] = live[u] && slot >= 0 && slot < a.n_slots;
       if (live[u] && !ok[u] && sub == 0) atomicOr(err, kErrSlot);
       const float4* row = reinterpret_cast<const float4*>(a.pooled + (int64_t)(ok[u] ? slot : 0) * kIdxDim);
@@ -224,6 +234,7 @@ k_score(const IndexArgs a, float* __restrict__ scores, unsigned* __restrict__ hi
       for (int k = 0; k < 4; ++k)
         kv[u][k] = ok[u] ? __ldg(row + k * 8 + sub) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    first = false;
 #pragma unroll
     for (int u = 0; u < kScoreUnroll; ++u) {
       float acc[kIdxHeads];
@@ -254,141 +265,214 @@ k_score(const IndexArgs a, float* __restrict__ scores, unsigned* __restrict__ hi
         const float sc = ok[u] ? v : -INFINITY;
         const int64_t j = base + u * 4 + grp;
         srow[j] = sc;
-        if (kTopk) atomicAdd(&s_hist[score_key(sc) >> (32 - kHistBits)], 1u);
+        if (kTopk) {
+          const unsigned bin = score_key(sc) >> (32 - kHistBits);
+          if (atomicAdd(&s_hist[bin], 1u) == 0u) s_touched[atomicAdd(&s_ntouched, 1u)] = (unsigned short)bin;
+        }
       }
     }
   }
-  if (!kTopk) return;
-
-  __syncthreads();
-  unsigned* gh = hist + (int64_t)t * kHistBins;
-  for (int i = tid; i < kHistBins; i += kScoreThreads) {
-    const unsigned v = s_hist[i];
-    if (v) atomicAdd(gh + i, v);
-  }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last = (atomicAdd(done + t, 1u) == gridDim.x - 1);
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-
-  // Last CTA of this token: find the bin holding the B-th largest score.
-  const unsigned B = (unsigned)a.n_sel_blocks;
-  if ((unsigned)nb <= B) {
-    if (tid == 0) state[t] = make_int4(-1, 0, 0, nb);
-    return;
-  }
-  constexpr int kPer = kHistBins / kScoreThreads;   // 16 bins per thread
-  unsigned h[kPer];
-  unsigned sum = 0;
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    h[i] = __ldcg(gh + tid * kPer + i);
-    sum += h[i];
-  }
-  unsigned cum = block_suffix_exclusive(sum, s_warp);
-#pragma unroll
-  for (int i = kPer - 1; i >= 0; --i) {
-    const unsigned nxt = cum + h[i];
-    if (cum < B && nxt >= B) state[t] = make_int4(tid * kPer + i, (int)(B - cum), (int)h[i], nb);
-    cum = nxt;
+  if (kTopk) {
+    QSA_TS(index, 3);
+    __syncthreads();
+    const unsigned nt = s_ntouched;
+    for (unsigned i = tid; i < nt; i += kScoreThreads) {
+      const unsigned b = s_touched[i];
+      atomicAdd(ghist + b, s_hist[b]);
+    }
   }
 }
 
-// ---------------------------------------------------------------- k_filter
-__global__ void __launch_bounds__(kFilterThreads)
-k_filter(const float* __restrict__ scores, int64_t pitch, const int4* __restrict__ state,
-         unsigned* __restrict__ bitmap, int64_t wpitch, unsigned* __restrict__ cand_cnt,
-         unsigned long long* __restrict__ cand) {
+// ---------------------------------------------------------------- k_select
+struct SelSmem {
+  unsigned bitmap[kSelMaxWords];
+  unsigned long long cand[kSelLocalCand];
+  unsigned long long allc[kRankMax];     // every CTA's threshold-bin keys (rank path)
+  unsigned hist[2][256];
+  unsigned tot[256];
+  unsigned warp_tmp[32];
+  unsigned selc[kSelCluster];            // chosen threshold-bin keys per CTA (rank path)
+  unsigned ncand;
+  unsigned ncent;                        // keys gathered in CTA 0 (central path)
+  unsigned cbase;
+  unsigned sel;
+  int digit;
+  unsigned above, eq;
+  int thr, need, ncand_all;
+  int tail_cells[8];
+};
+
+__global__ void __launch_bounds__(kSelThreads, 1)
+k_select(const IndexArgs a, void* ws, const float* __restrict__ scores,
+         int32_t* __restrict__ cells, int32_t* __restrict__ count, unsigned* err) {
+  __shared__ SelSmem sm;
+  extern __shared__ int32_t s_dyn[];
+  int32_t* s_slots = s_dyn;                // slot ids of this CTA's range (prefetched)
+  int* s_list = s_dyn + kSelSlots;         // chosen blocks of this CTA, ascending
   const int t = blockIdx.y;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int4 st = state[t];
-  const int thr = st.x, ncand = st.z, nb = st.w;
-  const bool keep_cand = thr >= 0 && ncand <= kCandCap;
-  const int64_t W = ceil_div(nb, 32);
-  const int64_t w0 = (int64_t)blockIdx.x * kFilterWordsPerCta;
-  const int64_t w1 = min(W, w0 + kFilterWordsPerCta);
-  const float* srow = scores + (int64_t)t * pitch;
-  for (int64_t w = w0 + warp; w < w1; w += kFilterThreads / 32) {
-    const int64_t j = w * 32 + lane;
-    const bool in = j < nb;
-    const uint32_t key = score_key(in ? __ldcg(srow + j) : 0.f);
-    const int bin = (int)(key >> (32 - kHistBits));
-    const bool above = in && bin > thr;
-    const bool isc = in && bin == thr;
-    const unsigned am = __ballot_sync(kFull, above);
-    if (lane == 0) bitmap[(int64_t)t * wpitch + w] = am;
-    if (keep_cand) {
-      const unsigned cm = __ballot_sync(kFull, isc);
-      if (cm) {
-        const int leader = __ffs(cm) - 1;
-        unsigned basei = 0;
-        if (lane == leader) basei = atomicAdd(cand_cnt + t, (unsigned)__popc(cm));
-        basei = __shfl_sync(kFull, basei, leader);
-        if (isc)
-          cand[(int64_t)t * kCandCap + basei + __popc(cm & ((1u << lane) - 1u))] = cand_key(key, j);
-      }
-    }
-  }
-}
-
-// ----------------------------------------------------------------- k_final
-__global__ void __launch_bounds__(kFinalThreads)
-k_final(const IndexArgs a, const float* __restrict__ scores, const int4* __restrict__ state,
-        unsigned* __restrict__ bitmap, int64_t wpitch,
-        const unsigned long long* __restrict__ cand,
-        int32_t* __restrict__ cells, int32_t* __restrict__ count, unsigned* err) {
-  __shared__ unsigned s_hist[256];
-  __shared__ unsigned s_warp[32];
-  __shared__ int s_digit;
-  __shared__ unsigned s_above, s_eq;
-
-  const int t = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int4 st = state[t];
-  const int thr = st.x, ncand = st.z, nb = st.w;
-  unsigned* bm = bitmap + (int64_t)t * wpitch;
-  const float* srow = scores + (int64_t)t * a.max_blocks;
+  const uint32_t rank = cluster_rank(), NC = cluster_size();
+  const int r = a.r;
+  const int B = a.n_sel_blocks;
 
-  if (thr >= 0) {
-    // Select the `need` largest unique keys among the threshold-bin blocks,
-    // one radix digit (8 bits, most significant first) at a time.
-    const bool fast = ncand <= kCandCap;
-    constexpr int kPer = kCandCap / kFinalThreads;
-    unsigned long long c[kPer];
+  // ---- before the wait: geometry, this CTA's slot ids and the tail cells
+  // (block lists and the block table are not written by the score kernel)
+  QSA_TS(index, 10);
+  const Tok tk = token_geometry(a, t, err, false);
+  const int nb = tk.nb;
+  const int64_t per = round_up(ceil_div(nb > 0 ? nb : 1, (int64_t)NC), 32);
+  const int64_t j0 = (int64_t)rank * per;
+  const int64_t j1 = min((int64_t)nb, j0 + per);
+  const int nwords = j1 > j0 ? (int)ceil_div(j1 - j0, 32) : 0;
+  const bool slots_cached = per <= kSelSlots;
+  const bool all_cached = rank == 0 && nb <= kSelSlots;   // CTA 0 holds every slot id
+  const int32_t* slots = a.seq_blk_slots + tk.off;
+  if (all_cached) {
+    for (int64_t j = tid; j < nb; j += kSelThreads) s_slots[j] = slots[j];
+  } else if (slots_cached) {
+    for (int64_t j = j0 + tid; j < j1; j += kSelThreads) s_slots[j - j0] = slots[j];
+  }
+  int tail = 0;
+  if (tk.ok && tk.nb == tk.nb_full) tail = tk.p + 1 - (int)(tk.nb_full * r);
+  const bool tail_missing = tail > 0 && tk.nb_full >= tk.len;
+  if (tail_missing) tail = 0;
+  if (rank == 0 && tid < tail) {
+    const int slot = slots[tk.nb_full];
+    const bool sok = slot >= 0 && slot < a.n_slots;
+    if (!sok) atomicOr(err, kErrSlot);
+    const int cidx = sok ? a.blk_cells[(int64_t)slot * r + tid] : -1;
+    if (cidx < 0 || cidx >= a.n_cells) atomicOr(err, kErrCell);
+    sm.tail_cells[tid] = cidx;
+  }
+  if (tid == 0) {
+    sm.ncand = 0u;
+    sm.ncent = 0u;
+  }
+  // first half of a cluster barrier: the counters above are set before any
+  // peer writes into this CTA (the matching wait follows the classification)
+  cluster_arrive();
+
+  QSA_TS(index, 11);
+  grid_dep_wait();
+  grid_dep_launch();
+  QSA_TS(index, 12);
+  // First batch of this warp's scores in flight while the threshold bin is
+  // found from the token's histogram (every CTA of the cluster).
+  unsigned* gh = hist_of(ws, t);
+  const float* srow = scores + (int64_t)t * a.max_blocks;
+  // words are dealt round-robin to the warps: word warp + kSelWarps * b
+  float v0[kSelBatch];
+#pragma unroll
+  for (int b = 0; b < kSelBatch; ++b) {
+    const int w = warp + kSelWarps * b;
+    const int64_t j = j0 + (int64_t)w * 32 + lane;
+    v0[b] = (w < nwords && j < j1) ? __ldcg(srow + j) : -INFINITY;
+  }
+  {
+    constexpr int kPer = kHistBins / kSelThreads;   // 8 bins per thread
+    unsigned h[kPer];
+    unsigned sum = 0;
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
-      const int idx = tid + i * kFinalThreads;
-      c[i] = (fast && idx < ncand) ? __ldcg(cand + (int64_t)t * kCandCap + idx) : 0ull;
+      h[i] = __ldcg(gh + tid * kPer + i);
+      sum += h[i];
     }
-    unsigned long long prefix = 0;
-    int shift = 48;
-    unsigned need = (unsigned)st.y;
-    for (;;) {
-      for (int i = tid; i < 256; i += kFinalThreads) s_hist[i] = 0u;
-      __syncthreads();
-      if (fast) {
+    if (tid == 0) {
+      sm.thr = -1;
+      sm.need = 0;
+      sm.ncand_all = 0;
+    }
+    unsigned cum = block_suffix_exclusive(sum, sm.warp_tmp);
+    const unsigned Bu = (unsigned)B;
+    if ((unsigned)nb > Bu) {
 #pragma unroll
-        for (int i = 0; i < kPer; ++i) {
-          const int idx = tid + i * kFinalThreads;
-          if (idx < ncand && (c[i] >> (shift + 8)) == prefix)
-            atomicAdd(&s_hist[(unsigned)(c[i] >> shift) & 255u], 1u);
+      for (int i = kPer - 1; i >= 0; --i) {
+        const unsigned nxt = cum + h[i];
+        if (cum < Bu && nxt >= Bu) {
+          sm.thr = tid * kPer + i;
+          sm.need = (int)(Bu - cum);
+          sm.ncand_all = (int)h[i];
         }
-      } else {
-        for (int64_t j = tid; j < nb; j += kFinalThreads) {
-          const uint32_t key = score_key(__ldcg(srow + j));
-          if ((int)(key >> (32 - kHistBits)) != thr) continue;
-          const unsigned long long ck = cand_key(key, j);
-          if ((ck >> (shift + 8)) == prefix) atomicAdd(&s_hist[(unsigned)(ck >> shift) & 255u], 1u);
+        cum = nxt;
+      }
+    }
+    __syncthreads();
+  }
+  const int thr = sm.thr, ncand_all = sm.ncand_all;
+  const bool fast = thr < 0 || ncand_all <= kSelLocalCand;
+
+  // ---- phase A: classify this CTA's blocks
+  for (int wb = 0; wb * kSelWarps * kSelBatch < nwords; ++wb) {
+    const int wbase = wb * kSelWarps * kSelBatch + warp;
+    float v[kSelBatch];
+#pragma unroll
+    for (int b = 0; b < kSelBatch; ++b) {
+      const int w = wbase + kSelWarps * b;
+      const int64_t j = j0 + (int64_t)w * 32 + lane;
+      v[b] = (wb == 0) ? v0[b] : ((w < nwords && j < j1) ? __ldcg(srow + j) : -INFINITY);
+    }
+#pragma unroll
+    for (int b = 0; b < kSelBatch; ++b) {
+      const int w = wbase + kSelWarps * b;
+      if (w >= nwords) break;
+      const int64_t j = j0 + (int64_t)w * 32 + lane;
+      const bool in = j < j1;
+      const uint32_t key = score_key(v[b]);
+      const int bin = (int)(key >> (32 - kHistBits));
+      const unsigned am = __ballot_sync(kFull, in && bin > thr);
+      if (lane == 0) sm.bitmap[w] = am;
+      if (fast && thr >= 0) {
+        const bool isc = in && bin == thr;
+        const unsigned cm = __ballot_sync(kFull, isc);
+        if (cm) {
+          const int leader = __ffs(cm) - 1;
+          unsigned basei = 0;
+          if (lane == leader) basei = atomicAdd(&sm.ncand, (unsigned)__popc(cm));
+          basei = __shfl_sync(kFull, basei, leader);
+          const unsigned idx = basei + __popc(cm & ((1u << lane) - 1u));
+          if (isc && idx < (unsigned)kSelLocalCand) sm.cand[idx] = cand_key(key, j);
         }
       }
+    }
+  }
+  __syncthreads();
+  QSA_TS(index, 13);
+  cluster_wait();
+
+  if (nb <= kCentralBlocks && (thr < 0 || ncand_all <= kRankMax)) {
+    // ---- central path: every CTA sends its bitmap words and threshold-bin
+    // keys into CTA 0's shared memory; CTA 0 ranks the keys, orders and
+    // expands the chosen blocks alone.
+    if (rank != 0)
+      for (int w = tid; w < nwords; w += kSelThreads)
+        st_dsmem_u32(dsmem_addr(&sm.bitmap[(int)(j0 >> 5) + w], 0), sm.bitmap[w]);
+    const unsigned ncl = min(sm.ncand, (unsigned)kSelLocalCand);
+    if (tid == 0) sm.cbase = ncl ? atom_add_dsmem(dsmem_addr(&sm.ncent, 0), ncl) : 0u;
+    __syncthreads();
+    for (unsigned i = tid; i < ncl; i += kSelThreads) {
+      const unsigned at = sm.cbase + i;
+      if (at < (unsigned)kRankMax) st_dsmem_u64(dsmem_addr(&sm.allc[at], 0), sm.cand[i]);
+    }
+    cluster_sync();   // everything has landed in CTA 0
+    if (rank != 0) return;
+    QSA_TS(index, 14);
+    for (int i = tid; i < kHistBins; i += kSelThreads) gh[i] = 0u;   // zero for the next call
+    const unsigned nall = min(sm.ncent, (unsigned)kRankMax);
+    if (thr >= 0) {
+      // One 8-bit digit below the bin (key bits 19..12) splits the keys; keys
+      // in higher sub-bins are chosen, the cut-off sub-bin (usually one or
+      // two keys) is ranked exactly by full key.
+      unsigned need = (unsigned)sm.need;
+      unsigned* hh = sm.hist[0];
+      if (tid < 256) hh[tid] = 0u;
+      __syncthreads();
+      for (unsigned i = tid; i < nall; i += kSelThreads) atomicAdd(&hh[(unsigned)(sm.allc[i] >> 48) & 255u], 1u);
       __syncthreads();
       if (warp == 0) {
         unsigned hv[8], sum = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          hv[i] = s_hist[lane * 8 + i];
+          hv[i] = hh[lane * 8 + i];
           sum += hv[i];
         }
         unsigned x = sum;
@@ -397,101 +481,323 @@ k_final(const IndexArgs a, const float* __restrict__ scores, const int4* __restr
           const unsigned y = __shfl_down_sync(kFull, x, o);
           if (lane + o < 32) x += y;
         }
-        unsigned cum = x - sum;   // digits above this lane's 8
+        unsigned cum = x - sum;
 #pragma unroll
         for (int i = 7; i >= 0; --i) {
           const unsigned nxt = cum + hv[i];
           if (cum < need && nxt >= need) {
-            s_digit = lane * 8 + i;
-            s_above = cum;
-            s_eq = hv[i];
+            sm.digit = lane * 8 + i;
+            sm.above = cum;
           }
           cum = nxt;
         }
       }
       __syncthreads();
-      const int d = s_digit;
-      need -= s_above;
-      const unsigned eq = s_eq;
-      prefix = (prefix << 8) | (unsigned long long)d;
-      __syncthreads();
-      if (eq == need || shift == 0) break;
-      shift -= 8;
-    }
-    // Every key whose top bits (down to `shift`) are >= prefix is chosen.
-    if (fast) {
-#pragma unroll
-      for (int i = 0; i < kPer; ++i) {
-        const int idx = tid + i * kFinalThreads;
-        if (idx < ncand && (c[i] >> shift) >= prefix) {
-          const uint32_t j = ~(uint32_t)(c[i] >> 4);
-          atomicOr(bm + (j >> 5), 1u << (j & 31));
+      const unsigned dstar = (unsigned)sm.digit;
+      need -= sm.above;
+      for (unsigned i = tid; i < nall; i += kSelThreads) {
+        const unsigned long long c = sm.allc[i];
+        const unsigned d = (unsigned)(c >> 48) & 255u;
+        bool take = d > dstar;
+        if (d == dstar) {
+          unsigned above_c = 0;
+          for (unsigned m = 0; m < nall; ++m) {
+            const unsigned long long o = sm.allc[m];
+            above_c += (((unsigned)(o >> 48) & 255u) == dstar && o > c) ? 1u : 0u;
+          }
+          take = above_c < need;
         }
-      }
-    } else {
-      for (int64_t j = tid; j < nb; j += kFinalThreads) {
-        const uint32_t key = score_key(__ldcg(srow + j));
-        if ((int)(key >> (32 - kHistBits)) != thr) continue;
-        if ((cand_key(key, j) >> shift) >= prefix) atomicOr(bm + (j >> 5), 1u << (j & 31));
+        if (take) {
+          const int64_t j = (int64_t)(~(uint32_t)(c >> 4));
+          atomicOr(&sm.bitmap[j >> 5], 1u << (j & 31));
+        }
       }
     }
     __syncthreads();
+    // ordered list of the chosen blocks (block prefix over the bitmap words)
+    const int W = (int)ceil_div(nb, 32);
+    const int wq = (int)ceil_div(W, kSelThreads);
+    const int q0 = tid * wq, q1 = min(W, q0 + wq);
+    unsigned mine = 0;
+    for (int w = q0; w < q1; ++w) mine += __popc(sm.bitmap[w]);
+    unsigned total_sel = 0;
+    unsigned k = block_prefix_exclusive(mine, sm.warp_tmp, &total_sel);
+    if (tid == 0) sm.sel = total_sel;
+    for (int w = q0; w < q1; ++w) {
+      unsigned bits = sm.bitmap[w];
+      while (bits) {
+        if (k < (unsigned)kSelList) s_list[k] = w * 32 + (__ffs(bits) - 1);
+        ++k;
+        bits &= bits - 1u;
+      }
+    }
+    __syncthreads();
+    QSA_TS(index, 15);
+    const unsigned total = sm.sel;
+    const int nsel = (int)min(total, (unsigned)B);
+    int32_t* crow = cells + (int64_t)t * a.cells_pitch;
+    for (int i = tid; i < nsel; i += kSelThreads) {
+      const int j = s_list[i];
+      const int sl = all_cached ? s_slots[j] : slots[j];
+      const bool sok = sl >= 0 && sl < a.n_slots;
+      if (!sok) atomicOr(err, kErrSlot);
+      int cv[8];
+#pragma unroll
+      for (int m = 0; m < 8; ++m) cv[m] = (sok && m < r) ? a.blk_cells[(int64_t)sl * r + m] : -1;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        if (m >= r) break;
+        if (cv[m] < 0 || cv[m] >= a.n_cells) atomicOr(err, kErrCell);
+        crow[(int64_t)i * r + m] = cv[m];
+      }
+    }
+    if (tid < tail) crow[nsel * r + tid] = sm.tail_cells[tid];
+    if (tid == 0) {
+      if (tail_missing) atomicOr(err, kErrBlockList);
+      count[t] = nsel * r + tail;
+    }
+    for (int i = nsel * r + tail + tid; i < a.cells_pitch; i += kSelThreads) crow[i] = -1;
+    QSA_TS(index, 16);
+    return;
   }
 
-  // Ordered compaction of the bitmap + expansion to member cells.
-  const Tok tk = token_geometry(a, t, err, false);
-  const int64_t W = ceil_div(nb, 32);
-  const int64_t wpt = ceil_div(W, kFinalThreads);
-  const int64_t w0 = (int64_t)tid * wpt, w1 = min(W, w0 + wpt);
-  unsigned mine = 0;
-  for (int64_t w = w0; w < w1; ++w) mine += __popc(__ldcg(bm + w));
-  unsigned total = 0;
-  unsigned k = block_prefix_exclusive(mine, s_warp, &total);
-  const int r = a.r;
-  const int B = a.n_sel_blocks;
-  int32_t* crow = cells + (int64_t)t * a.cells_pitch;
-  const int32_t* slots = a.seq_blk_slots + tk.off;
-  for (int64_t w = w0; w < w1; ++w) {
-    unsigned bits = __ldcg(bm + w);
-    while (bits) {
-      const int b = __ffs(bits) - 1;
-      bits &= bits - 1u;
-      const int64_t j = w * 32 + b;
-      if (k < (unsigned)B) {
-        const int slot = slots[j];
-        const bool sok = slot >= 0 && slot < a.n_slots;
-        if (!sok) atomicOr(err, kErrSlot);
-        for (int i = 0; i < r; ++i) {
-          const int cidx = sok ? a.blk_cells[(int64_t)slot * r + i] : -1;
-          if (cidx < 0 || cidx >= a.n_cells) atomicOr(err, kErrCell);
-          crow[(int64_t)k * r + i] = cidx;
+  const int wpt = (int)ceil_div(nwords, kSelThreads);
+  const int w0 = tid * wpt, w1 = min(nwords, w0 + wpt);
+  unsigned base = 0, total = 0;
+  if (fast && ncand_all <= kRankMax) {
+    // ---- phase B (rank path): every CTA pulls all threshold-bin keys and
+    // ranks them directly; one cluster barrier gives the exact cut-off and
+    // every CTA's output offset.
+    unsigned mine = 0;
+    for (int w = w0; w < w1; ++w) mine += __popc(sm.bitmap[w]);
+    unsigned na = 0;
+    block_prefix_exclusive(mine, sm.warp_tmp, &na);
+    if (tid == 0) sm.sel = na;
+    if (tid < kSelCluster) sm.selc[tid] = 0u;
+    cluster_sync();   // keys and counts published; every CTA has read the histogram
+    if (rank == 0)
+      for (int i = tid; i < kHistBins; i += kSelThreads) gh[i] = 0u;   // zero for the next call
+    unsigned nap[kSelCluster], ncp[kSelCluster];
+#pragma unroll
+    for (int p = 0; p < kSelCluster; ++p) {
+      nap[p] = p < (int)NC ? ld_dsmem_u32(dsmem_addr(&sm.sel, p)) : 0u;
+      ncp[p] = p < (int)NC ? min(ld_dsmem_u32(dsmem_addr(&sm.ncand, p)), (unsigned)kSelLocalCand) : 0u;
+    }
+    unsigned cpre[kSelCluster + 1];
+    cpre[0] = 0;
+#pragma unroll
+    for (int p = 0; p < kSelCluster; ++p) cpre[p + 1] = cpre[p] + ncp[p];
+    const unsigned nall = cpre[kSelCluster];
+    for (unsigned i = tid; i < nall; i += kSelThreads) {
+      int p = 0;
+#pragma unroll
+      for (int q = 1; q < kSelCluster; ++q) p += (i >= cpre[q]) ? 1 : 0;
+      unsigned long long c;
+      const uint32_t ad = dsmem_addr(&sm.cand[i - cpre[p]], p);
+      asm("ld.shared::cluster.u64 %0, [%1];\n" : "=l"(c) : "r"(ad));
+      sm.allc[i] = c;
+    }
+    __syncthreads();
+    const unsigned need = (unsigned)sm.need;
+    for (unsigned i = tid; i < nall; i += kSelThreads) {
+      const unsigned long long c = sm.allc[i];
+      unsigned above_c = 0;
+      for (unsigned m = 0; m < nall; ++m) above_c += (sm.allc[m] > c) ? 1u : 0u;
+      if (above_c < need) {
+        int p = 0;
+#pragma unroll
+        for (int q = 1; q < kSelCluster; ++q) p += (i >= cpre[q]) ? 1 : 0;
+        atomicAdd(&sm.selc[p], 1u);
+        if (p == (int)rank) {
+          const int64_t j = (int64_t)(~(uint32_t)(c >> 4));
+          atomicOr(&sm.bitmap[(j - j0) >> 5], 1u << ((j - j0) & 31));
         }
       }
-      ++k;
     }
-  }
-  const int nsel = (int)min(total, (unsigned)B);
-  int tail = 0;
-  if (tk.ok && tk.nb == tk.nb_full) tail = tk.p + 1 - (int)(tk.nb_full * r);
-  if (tid == 0) {
-    if (tail > 0) {
-      if (tk.nb_full < tk.len) {
-        const int slot = slots[tk.nb_full];
-        const bool sok = slot >= 0 && slot < a.n_slots;
-        if (!sok) atomicOr(err, kErrSlot);
-        for (int i = 0; i < tail; ++i) {
-          const int cidx = sok ? a.blk_cells[(int64_t)slot * r + i] : -1;
-          if (cidx < 0 || cidx >= a.n_cells) atomicOr(err, kErrCell);
-          crow[nsel * r + i] = cidx;
+    __syncthreads();
+#pragma unroll
+    for (int p = 0; p < kSelCluster; ++p) {
+      const unsigned c = nap[p] + sm.selc[p];
+      if (p < (int)rank) base += c;
+      total += c;
+    }
+  } else {
+    // ---- phase B (radix path): the `need` largest keys in the threshold bin,
+    // one 8-bit digit per round, digit histograms summed over the cluster.
+    if (thr >= 0) {
+      const unsigned ncl = min(sm.ncand, (unsigned)kSelLocalCand);
+      unsigned long long prefix = 0;
+      int shift = 48;
+      unsigned need = (unsigned)sm.need;
+      int buf = 0;
+      for (;;) {
+        unsigned* hh = sm.hist[buf];
+        if (tid < 256) hh[tid] = 0u;
+        __syncthreads();
+        if (fast) {
+          for (unsigned i = tid; i < ncl; i += kSelThreads) {
+            const unsigned long long c = sm.cand[i];
+            if ((c >> (shift + 8)) == prefix) atomicAdd(&hh[(unsigned)(c >> shift) & 255u], 1u);
+          }
+        } else {
+          for (int64_t j = j0 + tid; j < j1; j += kSelThreads) {
+            const uint32_t key = score_key(__ldcg(srow + j));
+            if ((int)(key >> (32 - kHistBits)) != thr) continue;
+            const unsigned long long c = cand_key(key, j);
+            if ((c >> (shift + 8)) == prefix) atomicAdd(&hh[(unsigned)(c >> shift) & 255u], 1u);
+          }
+        }
+        cluster_sync();
+        if (tid < 256) {
+          unsigned v[kSelCluster];
+#pragma unroll
+          for (int p = 0; p < kSelCluster; ++p) v[p] = p < (int)NC ? ld_dsmem_u32(dsmem_addr(&hh[tid], p)) : 0u;
+          unsigned sum = 0;
+#pragma unroll
+          for (int p = 0; p < kSelCluster; ++p) sum += v[p];
+          sm.tot[tid] = sum;
+        }
+        __syncthreads();
+        if (warp == 0) {
+          unsigned hv[8], sum = 0;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            hv[i] = sm.tot[lane * 8 + i];
+            sum += hv[i];
+          }
+          unsigned x = sum;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const unsigned y = __shfl_down_sync(kFull, x, o);
+            if (lane + o < 32) x += y;
+          }
+          unsigned cum = x - sum;   // digits above this lane's 8
+#pragma unroll
+          for (int i = 7; i >= 0; --i) {
+            const unsigned nxt = cum + hv[i];
+            if (cum < need && nxt >= need) {
+              sm.digit = lane * 8 + i;
+              sm.above = cum;
+              sm.eq = hv[i];
+            }
+            cum = nxt;
+          }
+        }
+        __syncthreads();
+        need -= sm.above;
+        const unsigned eq = sm.eq;
+        prefix = (prefix << 8) | (unsigned long long)sm.digit;
+        buf ^= 1;
+        QSA_TS(index, 20 + (shift == 48 ? 0 : (shift == 40 ? 1 : 2)));
+        if (eq == need || shift == 0) break;
+        shift -= 8;
+      }
+      // every key whose bits down to `shift` are >= prefix is chosen
+      if (fast) {
+        for (unsigned i = tid; i < ncl; i += kSelThreads) {
+          const unsigned long long c = sm.cand[i];
+          if ((c >> shift) >= prefix) {
+            const int64_t j = (int64_t)(~(uint32_t)(c >> 4));
+            atomicOr(&sm.bitmap[(j - j0) >> 5], 1u << ((j - j0) & 31));
+          }
         }
       } else {
-        atomicOr(err, kErrBlockList);
-        tail = 0;
+        for (int64_t j = j0 + tid; j < j1; j += kSelThreads) {
+          const uint32_t key = score_key(__ldcg(srow + j));
+          if ((int)(key >> (32 - kHistBits)) != thr) continue;
+          if ((cand_key(key, j) >> shift) >= prefix) atomicOr(&sm.bitmap[(j - j0) >> 5], 1u << ((j - j0) & 31));
+        }
+      }
+      __syncthreads();
+    }
+    unsigned mine = 0;
+    for (int w = w0; w < w1; ++w) mine += __popc(sm.bitmap[w]);
+    unsigned local_total = 0;
+    block_prefix_exclusive(mine, sm.warp_tmp, &local_total);
+    if (tid == 0) sm.sel = local_total;
+    cluster_sync();   // every CTA has read the histogram and published its count
+    if (rank == 0)
+      for (int i = tid; i < kHistBins; i += kSelThreads) gh[i] = 0u;   // zero for the next call
+    unsigned c[kSelCluster];
+#pragma unroll
+    for (int p = 0; p < kSelCluster; ++p) c[p] = p < (int)NC ? ld_dsmem_u32(dsmem_addr(&sm.sel, p)) : 0u;
+#pragma unroll
+    for (int p = 0; p < kSelCluster; ++p) {
+      if (p < (int)rank) base += c[p];
+      total += c[p];
+    }
+  }
+  QSA_TS(index, 14);
+
+  // ---- phase C: ordered expansion of this CTA's chosen blocks at `base`
+  unsigned mine = 0;
+  for (int w = w0; w < w1; ++w) mine += __popc(sm.bitmap[w]);
+  unsigned local_total = 0;
+  unsigned k = block_prefix_exclusive(mine, sm.warp_tmp, &local_total);
+  QSA_TS(index, 15);
+  int32_t* crow = cells + (int64_t)t * a.cells_pitch;
+  if (local_total <= (unsigned)kSelList) {
+    // list the chosen blocks in order, then expand one block per thread
+    for (int w = w0; w < w1; ++w) {
+      unsigned bits = sm.bitmap[w];
+      while (bits) {
+        s_list[k++] = (int)(w * 32 + (__ffs(bits) - 1));
+        bits &= bits - 1u;
       }
     }
-    count[t] = nsel * r + tail;
+    __syncthreads();
+    for (unsigned i = tid; i < local_total; i += kSelThreads) {
+      const unsigned kk = base + i;
+      if (kk >= (unsigned)B) continue;
+      const int64_t j = j0 + s_list[i];
+      const int sl = slots_cached ? s_slots[j - j0] : slots[j];
+      const bool sok = sl >= 0 && sl < a.n_slots;
+      if (!sok) atomicOr(err, kErrSlot);
+      int cv[8];
+#pragma unroll
+      for (int m = 0; m < 8; ++m) cv[m] = (sok && m < r) ? a.blk_cells[(int64_t)sl * r + m] : -1;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        if (m >= r) break;
+        if (cv[m] < 0 || cv[m] >= a.n_cells) atomicOr(err, kErrCell);
+        crow[(int64_t)kk * r + m] = cv[m];
+      }
+    }
+  } else {
+    k += base;
+    for (int w = w0; w < w1; ++w) {
+      unsigned bits = sm.bitmap[w];
+      while (bits) {
+        const int64_t j = j0 + (int64_t)w * 32 + (__ffs(bits) - 1);
+        bits &= bits - 1u;
+        if (k < (unsigned)B) {
+          const int sl = slots_cached ? s_slots[j - j0] : slots[j];
+          const bool sok = sl >= 0 && sl < a.n_slots;
+          if (!sok) atomicOr(err, kErrSlot);
+          for (int m = 0; m < r; ++m) {
+            const int cidx = sok ? a.blk_cells[(int64_t)sl * r + m] : -1;
+            if (cidx < 0 || cidx >= a.n_cells) atomicOr(err, kErrCell);
+            crow[(int64_t)k * r + m] = cidx;
+          }
+        }
+        ++k;
+      }
+    }
   }
-  for (int i = nsel * r + tail + tid; i < a.cells_pitch; i += kFinalThreads) crow[i] = -1;
+  QSA_TS(index, 16);
+  const int nsel = (int)min(total, (unsigned)B);
+  if (rank == 0) {
+    if (tid < tail) crow[nsel * r + tid] = sm.tail_cells[tid];
+    if (tid == 0) {
+      if (tail_missing) atomicOr(err, kErrBlockList);
+      count[t] = nsel * r + tail;
+    }
+  }
+  for (int i = nsel * r + tail + (int)rank * kSelThreads + tid; i < a.cells_pitch; i += (int)NC * kSelThreads)
+    crow[i] = -1;
+  QSA_TS(index, 17);
+  cluster_sync();   // peers read sm.sel and the digit histograms until here
+  QSA_TS(index, 18);
 }
 
 int score_chunk(int T, int64_t max_blocks) {
@@ -505,46 +811,53 @@ int score_chunk(int T, int64_t max_blocks) {
 
 }  // namespace
 
-size_t index_workspace_bytes(int n_tokens, int64_t max_blocks) {
-  return carve(nullptr, n_tokens, max_blocks).total;
+int64_t index_max_blocks_limit() { return (int64_t)kSelCluster * kSelMaxWords * 32; }
+
+size_t index_workspace_bytes(int max_tokens, int64_t max_blocks) {
+  return (size_t)round_up((int64_t)max_tokens * kCtrlBytes, 256) +
+         (size_t)round_up((int64_t)max_tokens * max_blocks * (int64_t)sizeof(float), 256);
 }
 
-void index_workspace_zero_range(int n_tokens, int64_t max_blocks, size_t* offset, size_t* bytes) {
-  const Ws w = carve(reinterpret_cast<void*>(static_cast<uintptr_t>(256)), n_tokens, max_blocks);
-  *offset = static_cast<size_t>(static_cast<char*>(w.zero_base) - reinterpret_cast<char*>(static_cast<uintptr_t>(256)));
-  *bytes = w.zero_bytes;
+void index_workspace_zero_range(int n_tokens, int64_t, size_t* offset, size_t* bytes) {
+  *offset = 0;
+  *bytes = (size_t)n_tokens * kCtrlBytes;
 }
 
 cudaError_t launch_index_scores(const IndexArgs& a, float* scores, unsigned* err, cudaStream_t stream) {
   if (a.n_tokens <= 0 || a.max_blocks <= 0) return cudaSuccess;
   const int chunk = score_chunk(a.n_tokens, a.max_blocks);
   const dim3 grid((unsigned)ceil_div(a.max_blocks, chunk), (unsigned)a.n_tokens);
-  k_score<false><<<grid, kScoreThreads, 0, stream>>>(a, scores, nullptr, nullptr, nullptr, chunk, err);
-  return cudaGetLastError();
+  return launch_pdl(k_score<false>, grid, dim3(kScoreThreads), 0, stream, 1, a, (void*)nullptr, scores, chunk,
+                    err);
 }
 
 cudaError_t launch_index_topk(const IndexArgs& a, int32_t* cells, int32_t* count,
-                              void* wsp, unsigned* err, cudaStream_t stream) {
+                              void* ws, unsigned* err, cudaStream_t stream) {
   if (a.n_tokens <= 0) return cudaSuccess;
-  const int64_t mb = a.max_blocks > 0 ? a.max_blocks : 1;
-  Ws w = carve(wsp, a.n_tokens, mb);
-  cudaError_t e = cudaMemsetAsync(w.zero_base, 0, w.zero_bytes, stream);
+  static bool configured[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  const size_t slot_bytes = sizeof(int32_t) * (kSelSlots + kSelList);
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
+    e = cudaFuncSetAttribute(k_select, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)slot_bytes);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
   IndexArgs b = a;
-  b.max_blocks = mb;
-  const int chunk = score_chunk(a.n_tokens, mb);
-  const dim3 g1((unsigned)ceil_div(mb, chunk), (unsigned)a.n_tokens);
+  b.max_blocks = a.max_blocks > 0 ? a.max_blocks : 1;
+  float* sc = scores_of(ws, a.max_tokens);
+  const int chunk = score_chunk(a.n_tokens, b.max_blocks);
+  const dim3 g1((unsigned)ceil_div(b.max_blocks, chunk), (unsigned)a.n_tokens);
   prof_before(kKScore, stream);
-  k_score<true><<<g1, kScoreThreads, 0, stream>>>(b, w.scores, w.hist, w.done, w.state, chunk, err);
+  e = launch_pdl(k_score<true>, g1, dim3(kScoreThreads), 0, stream, 1, b, ws, sc, chunk, err);
   prof_after(kKScore, stream);
-  const dim3 g2((unsigned)ceil_div(ceil_div(mb, 32), kFilterWordsPerCta), (unsigned)a.n_tokens);
-  prof_before(kKFilter, stream);
-  k_filter<<<g2, kFilterThreads, 0, stream>>>(w.scores, mb, w.state, w.bitmap, w.wpitch, w.cand_cnt, w.cand);
-  prof_after(kKFilter, stream);
+  if (e != cudaSuccess) return e;
   prof_before(kKFinal, stream);
-  k_final<<<(unsigned)a.n_tokens, kFinalThreads, 0, stream>>>(b, w.scores, w.state, w.bitmap, w.wpitch,
-                                                               w.cand, cells, count, err);
+  e = launch_pdl(k_select, dim3(kSelCluster, (unsigned)a.n_tokens), dim3(kSelThreads), slot_bytes, stream,
+                 (unsigned)kSelCluster, b, ws, (const float*)sc, cells, count, err);
   prof_after(kKFinal, stream);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

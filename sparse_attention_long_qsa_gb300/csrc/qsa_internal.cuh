@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -42,6 +43,127 @@ __device__ __forceinline__ uint32_t score_key(float f) {
 __host__ __device__ __forceinline__ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 __host__ __device__ __forceinline__ int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 
+// ------------------------------------------------ launch chaining, clusters
+// Programmatic dependent launch: every kernel of the library is launched with
+// programmatic stream serialisation, so it may start while its predecessor in
+// the stream finishes.  A kernel reads or writes nothing its predecessor
+// produces or consumes before grid_dep_wait() (which returns once the
+// predecessor grid has completed and its memory is visible), and lets its own
+// successor launch (grid_dep_launch) only after that wait, so a successor's
+// early part never overlaps anything but this kernel.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;\n" : "=r"(r));
+  return r;
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t dsmem_addr(const void* local, uint32_t rank) {
+  uint32_t remote;
+  asm("mapa.shared::cluster.u32 %0, %1, %2;\n"
+      : "=r"(remote)
+      : "r"((uint32_t)__cvta_generic_to_shared(local)), "r"(rank));
+  return remote;
+}
+// Reads of peers' shared memory after a cluster_sync (not volatile, so the
+// compiler may issue several before using any).
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
+  float v;
+  asm("ld.shared::cluster.f32 %0, [%1];\n" : "=f"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ unsigned ld_dsmem_u32(uint32_t addr) {
+  unsigned v;
+  asm("ld.shared::cluster.u32 %0, [%1];\n" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ void st_dsmem_u32(uint32_t addr, unsigned v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;\n" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_dsmem_u64(uint32_t addr, unsigned long long v) {
+  asm volatile("st.shared::cluster.u64 [%0], %1;\n" ::"r"(addr), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned atom_add_dsmem(uint32_t addr, unsigned v) {
+  unsigned old;
+  asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;\n" : "=r"(old) : "r"(addr), "r"(v) : "memory");
+  return old;
+}
+// Split cluster barrier: arrive early, wait when the peers' earlier writes are needed.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory"); }
+__device__ __forceinline__ void st_dsmem_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;\n" ::"r"(addr), "f"(v) : "memory");
+}
+
+// cudaLaunchKernelEx with programmatic stream serialisation and an optional
+// 1-D cluster.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, unsigned cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// ------------------------------------------------------ phase timestamps
+// Built only with -DQSA_PHASE_TIMING (a profiling build, never the product
+// library): CTA 0 of a kernel records clock64() at numbered points into a
+// per-file device array that an extern "C" reader copies out.
+#ifdef QSA_PHASE_TIMING
+#define QSA_TS_DECLARE(tu)                                                              \
+  __device__ long long g_qsa_ts_##tu[64];                                               \
+  extern "C" int qsa_probe_read_##tu(long long* host) {                                 \
+    return (int)cudaMemcpyFromSymbol(host, g_qsa_ts_##tu, sizeof(long long) * 64);      \
+  }
+#define QSA_TS_IF(tu, i, cond)                                                          \
+  do {                                                                                  \
+    if (cond) {                                                                         \
+      long long g_;                                                                     \
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(g_));                            \
+      g_qsa_ts_##tu[i] = clock64();                                                     \
+      g_qsa_ts_##tu[32 + (i)] = g_;                                                     \
+    }                                                                                   \
+  } while (0)
+#define QSA_TS(tu, i) \
+  QSA_TS_IF(tu, i, blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0)
+#else
+#define QSA_TS_DECLARE(tu)
+#define QSA_TS_IF(tu, i, cond) \
+  do {                         \
+  } while (0)
+#define QSA_TS(tu, i) \
+  do {                \
+  } while (0)
+#endif
+
 // ------------------------------------------------------ measurement hook
 // Kernel ids of qsa_profile_kernel (include/qsa.h).
 enum KernelId : int { kKPool = 0, kKScore = 1, kKFilter = 2, kKFinal = 3, kKAttn = 4, kKCombine = 5,
@@ -71,6 +193,7 @@ cudaError_t launch_pool_update(const qsa_config& cfg, const __half* idx_k, int64
 
 struct IndexArgs {
   int n_tokens;
+  int max_tokens;     // token capacity the workspace layout is sized for
   const float* q_idx;
   const float* w_idx;
   const int32_t* tok_seq;
@@ -88,7 +211,9 @@ struct IndexArgs {
   int cells_pitch;    // top_k + r - 1
 };
 
-size_t index_workspace_bytes(int n_tokens, int64_t max_blocks);
+size_t index_workspace_bytes(int max_tokens, int64_t max_blocks);
+// Largest max_blocks the selection kernel supports (per-CTA bitmap capacity).
+int64_t index_max_blocks_limit();
 // Byte range of the workspace that must be zero when a call starts.
 void index_workspace_zero_range(int n_tokens, int64_t max_blocks, size_t* offset, size_t* bytes);
 cudaError_t launch_index_scores(const IndexArgs& a, float* scores, unsigned* err, cudaStream_t stream);

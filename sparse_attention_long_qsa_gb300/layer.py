@@ -51,7 +51,8 @@ class QSALayer:
         self.cells = torch.full((T, self.pitch), -1, dtype=torch.int32, device=device)
         self.count = torch.zeros(T, dtype=torch.int32, device=device)
         self.out = torch.zeros((T, cfg["n_q_heads"], cfg["head_dim"]), dtype=torch.float32, device=device)
-        self.ws_index = torch.empty(qsa.index_topk_workspace_size(self.cfg, T, self.max_blocks),
+        # zero-filled once; the library leaves its control words zero after every call
+        self.ws_index = torch.zeros(qsa.index_topk_workspace_size(self.cfg, T, self.max_blocks),
                                     dtype=torch.uint8, device=device)
         self.ws_attn = torch.empty(qsa.sparse_attn_workspace_size(self.cfg, T),
                                    dtype=torch.uint8, device=device)
@@ -75,7 +76,7 @@ class QSALayer:
         T = int(tok_pos.numel())
         qsa.index_topk(self.cfg, q_idx, w_idx, tok_seq, tok_pos, self.pooled, self.blk_cells,
                        self.seq_blk_off, self.seq_blk_slots, self.max_blocks, self.n_cells,
-                       self.cells[:T], self.count[:T], self.ws_index, stream)
+                       self.cells[:T], self.count[:T], self.ws_index, self.max_tokens, stream)
 
     def sparse_attn(self, q, n_tokens: int, stream=None):
         T = int(n_tokens)

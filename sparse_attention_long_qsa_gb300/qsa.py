@@ -30,7 +30,7 @@ EXPORTS = ("qsa_config_init", "qsa_cells_per_token", "qsa_pool_update", "qsa_ind
            "qsa_status_string")
 
 # Kernel ids of qsa_profile_kernel.
-KERNELS = {"pool": 0, "score": 1, "filter": 2, "final": 3, "attn": 4, "combine": 5}
+KERNELS = {"pool": 0, "score": 1, "select": 3, "attn": 4}
 
 
 class QSAError(RuntimeError):
@@ -75,7 +75,7 @@ def lib():
     L.qsa_index_scores.restype = _I32
     L.qsa_index_topk_workspace_size.argtypes = [CP, _I32, _I64]
     L.qsa_index_topk_workspace_size.restype = _SZ
-    L.qsa_index_topk.argtypes = [CP, _I32, _P, _P, _P, _P, _P, _P, _I64, _P, _P, _I32, _I64, _I64,
+    L.qsa_index_topk.argtypes = [CP, _I32, _I32, _P, _P, _P, _P, _P, _P, _I64, _P, _P, _I32, _I64, _I64,
                                  _P, _P, _P, _SZ, _P]
     L.qsa_index_topk.restype = _I32
     L.qsa_index_topk_noalloc.argtypes = [CP, _I32, _P, _P, _P, _P, _P, _P, _I64, _P, _P, _I32, _I64,
@@ -179,16 +179,19 @@ def index_scores(cfg, q_idx, w_idx, tok_seq, tok_pos, pooled, seq_blk_off, seq_b
     _check(st, "qsa_index_scores")
 
 
-def index_topk_workspace_size(cfg, n_tokens: int, max_blocks: int) -> int:
-    return int(lib().qsa_index_topk_workspace_size(ctypes.byref(cfg), int(n_tokens), int(max_blocks)))
+def index_topk_workspace_size(cfg, max_tokens: int, max_blocks: int) -> int:
+    return int(lib().qsa_index_topk_workspace_size(ctypes.byref(cfg), int(max_tokens), int(max_blocks)))
 
 
 def index_topk(cfg, q_idx, w_idx, tok_seq, tok_pos, pooled, blk_cells, seq_blk_off, seq_blk_slots,
-               max_blocks: int, n_cells: int, cells, count, workspace, stream=None):
+               max_blocks: int, n_cells: int, cells, count, workspace, max_tokens: int, stream=None):
+    """workspace: a uint8 CUDA tensor of index_topk_workspace_size(cfg,
+    max_tokens, max_blocks) bytes, zero-filled once when allocated."""
     import torch
     T = int(tok_pos.numel())
     st = lib().qsa_index_topk(
-        ctypes.byref(cfg), T, _ptr(q_idx, torch.float32, "q_idx"), _ptr(w_idx, torch.float32, "w_idx"),
+        ctypes.byref(cfg), T, int(max_tokens), _ptr(q_idx, torch.float32, "q_idx"),
+        _ptr(w_idx, torch.float32, "w_idx"),
         _ptr(tok_seq, torch.int32, "tok_seq"), _ptr(tok_pos, torch.int32, "tok_pos"),
         _ptr(pooled, torch.float32, "pooled"), _ptr(blk_cells, torch.int32, "blk_cells"),
         int(pooled.shape[0]), _ptr(seq_blk_off, torch.int64, "seq_blk_off"),
@@ -203,14 +206,16 @@ def sparse_attn_workspace_size(cfg, n_tokens: int) -> int:
     return int(lib().qsa_sparse_attn_workspace_size(ctypes.byref(cfg), int(n_tokens)))
 
 
-def sparse_attn(cfg, q, k_cache, v_cache, n_cells: int, cells, count, out, workspace, stream=None):
+def sparse_attn(cfg, q, k_cache, v_cache, n_cells: int, cells, count, out, workspace=None, stream=None):
     import torch
     T = int(count.numel())
+    ws_ptr = _ptr(workspace, torch.uint8, "workspace") if workspace is not None and workspace.numel() else None
+    ws_len = int(workspace.numel()) if workspace is not None else 0
     st = lib().qsa_sparse_attn(
         ctypes.byref(cfg), T, _ptr(q, torch.float16, "q"), _ptr(k_cache, None, "k_cache"),
         _ptr(v_cache, None, "v_cache"), int(n_cells), _ptr(cells, torch.int32, "cells"),
         _ptr(count, torch.int32, "count"), _ptr(out, torch.float32, "out"),
-        _ptr(workspace, torch.uint8, "workspace"), int(workspace.numel()), _stream(stream))
+        ws_ptr, ws_len, _stream(stream))
     _check(st, "qsa_sparse_attn")
 
 

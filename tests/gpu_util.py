@@ -2,9 +2,9 @@
 compare with the CPU oracle under the stated tolerances.
 
 Tolerances (stated once, used everywhere):
-  pooled keys   GPU: fp64 mean/RMS and angle reduction, fp32 sincos of the
-                reduced angle, one fp32 rounding; oracle: float64 throughout:
-                |gpu - oracle| <= 4e-7 * max|row|
+  pooled keys   GPU: fp32 mean/RMS, fp64 angle reduction, fp32 sincos of the
+                reduced angle; oracle: float64 throughout:
+                |gpu - oracle| <= 1e-6 * max|row|
   scores        fp32 GPU vs float64 oracle over the same pooled keys:
                 |gpu - oracle| <= 1e-5 * |oracle| + 1e-6 * max|row|
   selection     exact on the GPU's own scores (integers, bit-exact); against
@@ -39,7 +39,7 @@ def check_pooled(gpu, ora):
     gpu = np.asarray(gpu, dtype=np.float64)
     ora = np.asarray(ora, dtype=np.float64)
     rowmax = np.abs(ora).max(axis=-1, keepdims=True)
-    bound = 4e-7 * rowmax
+    bound = 1e-6 * rowmax
     bad = np.abs(gpu - ora) > bound
     assert not bad.any(), f"pooled mismatch at {np.argwhere(bad)[:5]}: gpu {gpu[bad][:5]} oracle {ora[bad][:5]}"
 

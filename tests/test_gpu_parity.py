@@ -205,3 +205,16 @@ def test_out_of_range_indices_are_masked_and_flagged():
     assert st == -6 and (flags & 1) and (flags & 2)
     L.blk_cells.copy_(tbl)
     assert qsa.debug_check()[0] == 0
+
+
+@pytest.mark.parametrize("top_k,n", [(16, 403), (256, 9_001), (512, 600), (4096, 30_003)])
+def test_other_budgets_cover_every_tile_layout(top_k, n):
+    """Budgets other than 2048 exercise the other attention layouts: one tile
+    (top_k 16), a 2-CTA cluster plus overflow cells (256), exactly NC tiles
+    (512 with a full budget), and several tiles per CTA (4096)."""
+    wl = make_workload(n_seq=1, prompt_len=n - 1, n_steps=3, seed=200 + top_k, cfg={"top_k": top_k})
+    run = Runner(wl)
+    for i in range(3):
+        res, _ = check_step(run, i)
+        nb = (n + i) // 4
+        assert int(res["count"][0]) == min(nb, top_k // 4) * 4 + (n + i) % 4
