@@ -153,7 +153,15 @@ qsa_status qsa_index_scores(const qsa_config* cfg, int32_t n_tokens,
  * number of calls with n_tokens <= max_tokens and any max_blocks it has room
  * for, as long as max_tokens stays the same.  max_blocks <= 1,048,576;
  * max_tokens <= 65535 (QSA_ERR_UNSUPPORTED beyond, QSA_ERR_SHAPE if
- * n_tokens > max_tokens). */
+ * n_tokens > max_tokens).
+ * recomputed / n_recomputed: optional scheduling hint, NULL / 0 for none.
+ * When this call directly follows a qsa_pool_update on the same stream, pass
+ * that update's dirty list (entries < 0 ignored): work on blocks whose slots
+ * are not in the list then starts without waiting for the update to finish
+ * (lists longer than 32 entries are not used).  The hint must name every slot
+ * the preceding update writes, or stale pooled keys may be scored.  Results do
+ * not depend on the hint otherwise.  QSA_ERR_INVALID_ARG if n_recomputed < 0,
+ * or > 0 with a NULL list. */
 size_t qsa_index_topk_workspace_size(const qsa_config* cfg, int32_t max_tokens,
                                      int64_t max_blocks);
 qsa_status qsa_index_topk(const qsa_config* cfg, int32_t n_tokens, int32_t max_tokens,
@@ -163,6 +171,7 @@ qsa_status qsa_index_topk(const qsa_config* cfg, int32_t n_tokens, int32_t max_t
                           const int64_t* seq_blk_off, const int32_t* seq_blk_slots,
                           int32_t n_seq, int64_t max_blocks, int64_t n_cells,
                           int32_t* cells, int32_t* count,
+                          const int32_t* recomputed, int32_t n_recomputed,
                           void* workspace, size_t ws_bytes, qsa_stream_t stream);
 
 /* qsa_index_topk_noalloc - the pages have no counterpart; this is a

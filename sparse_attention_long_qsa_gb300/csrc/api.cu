@@ -152,7 +152,8 @@ qsa_status qsa_index_topk(const qsa_config* cfg, int32_t n_tokens, int32_t max_t
                           const float* pooled, const int32_t* blk_cells, int64_t n_slots,
                           const int64_t* seq_blk_off, const int32_t* seq_blk_slots,
                           int32_t n_seq, int64_t max_blocks, int64_t n_cells, int32_t* cells,
-                          int32_t* count, void* workspace, size_t ws_bytes, qsa_stream_t stream) {
+                          int32_t* count, const int32_t* recomputed, int32_t n_recomputed,
+                          void* workspace, size_t ws_bytes, qsa_stream_t stream) {
   IndexArgs a{};
   qsa_status st = fill_index_args(cfg, n_tokens, max_tokens, q_idx, w_idx, tok_seq, tok_pos, pooled, n_slots,
                                   seq_blk_off, seq_blk_slots, n_seq, max_blocks, &a);
@@ -164,8 +165,11 @@ qsa_status qsa_index_topk(const qsa_config* cfg, int32_t n_tokens, int32_t max_t
   if (workspace == nullptr || !aligned(workspace, 256) ||
       ws_bytes < qsa_index_topk_workspace_size(cfg, max_tokens, max_blocks))
     return QSA_ERR_WORKSPACE;
+  if (n_recomputed < 0 || (n_recomputed > 0 && recomputed == nullptr)) return QSA_ERR_INVALID_ARG;
   a.blk_cells = blk_cells;
   a.n_cells = n_cells;
+  a.recomputed = recomputed;
+  a.n_recomputed = n_recomputed;
   unsigned* err = error_word();
   if (err == nullptr) return QSA_ERR_CUDA;
   return from_cuda(launch_index_topk(a, cells, count, workspace, err, reinterpret_cast<cudaStream_t>(stream)));

@@ -45,6 +45,7 @@ constexpr int kScoreUnroll = 2;
 // rows (blocks) one CTA covers per iteration: 8 warps x 4 rows x unroll
 constexpr int kRowsPerIter = kScoreWarps * 4 * kScoreUnroll;
 constexpr int kErrToken = 16;
+constexpr int kMaxHint = 32;              // recomputed-slot hints checked per CTA
 
 constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
@@ -207,9 +208,24 @@ k_score(const IndexArgs a, void* ws, float* __restrict__ scores, int chunk, unsi
     }
   }
 
-  // ---- pooled rows are written by the pool update
+  // ---- pooled rows are written by the pool update.  With the list of slots
+  // that update recomputed, a CTA none of whose rows is in it reads nothing
+  // the update writes and skips the wait; CTA 0 always waits, so this
+  // kernel still completes after the update.
+  bool must_wait = true;
+  if (kTopk && a.recomputed != nullptr && a.n_recomputed <= kMaxHint && blockIdx.x != 0) {
+    __shared__ int s_rec[kMaxHint];
+    for (int i = tid; i < a.n_recomputed; i += kScoreThreads) s_rec[i] = a.recomputed[i];
+    __syncthreads();
+    int hit = 0;
+    for (int64_t j = j0 + tid; j < j1; j += kScoreThreads) {
+      const int sl = __ldg(slots + j);
+      for (int i = 0; i < a.n_recomputed; ++i) hit |= (s_rec[i] == sl);
+    }
+    must_wait = __syncthreads_or(hit) != 0;
+  }
   if (kTopk) QSA_TS(index, 1);
-  grid_dep_wait();
+  if (must_wait) grid_dep_wait();
   grid_dep_launch();
   if (kTopk) QSA_TS(index, 2);
   if (!kTopk) {
@@ -456,7 +472,6 @@ k_select(const IndexArgs a, void* ws, const float* __restrict__ scores,
     cluster_sync();   // everything has landed in CTA 0
     if (rank != 0) return;
     QSA_TS(index, 14);
-    for (int i = tid; i < kHistBins; i += kSelThreads) gh[i] = 0u;   // zero for the next call
     const unsigned nall = min(sm.ncent, (unsigned)kRankMax);
     if (thr >= 0) {
       // One 8-bit digit below the bin (key bits 19..12) splits the keys; keys
@@ -557,6 +572,7 @@ k_select(const IndexArgs a, void* ws, const float* __restrict__ scores,
       count[t] = nsel * r + tail;
     }
     for (int i = nsel * r + tail + tid; i < a.cells_pitch; i += kSelThreads) crow[i] = -1;
+    for (int i = tid; i < kHistBins; i += kSelThreads) gh[i] = 0u;   // zero for the next call
     QSA_TS(index, 16);
     return;
   }

@@ -209,6 +209,9 @@ struct IndexArgs {
   int r;
   int n_sel_blocks;   // top_k / r
   int cells_pitch;    // top_k + r - 1
+  // slots the preceding pool update recomputed (scheduling hint, may be null)
+  const int32_t* recomputed;
+  int n_recomputed;
 };
 
 size_t index_workspace_bytes(int max_tokens, int64_t max_blocks);

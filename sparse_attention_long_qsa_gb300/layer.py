@@ -72,11 +72,12 @@ class QSALayer:
         qsa.pool_update(self.cfg, self.idx_k, self.blk_cells, self.slot_block_idx, d, self.norm_w,
                         self.pooled, stream)
 
-    def index_topk(self, tok_seq, tok_pos, q_idx, w_idx, stream=None):
+    def index_topk(self, tok_seq, tok_pos, q_idx, w_idx, recomputed=None, stream=None):
         T = int(tok_pos.numel())
         qsa.index_topk(self.cfg, q_idx, w_idx, tok_seq, tok_pos, self.pooled, self.blk_cells,
                        self.seq_blk_off, self.seq_blk_slots, self.max_blocks, self.n_cells,
-                       self.cells[:T], self.count[:T], self.ws_index, self.max_tokens, stream)
+                       self.cells[:T], self.count[:T], self.ws_index, self.max_tokens,
+                       recomputed, stream)
 
     def sparse_attn(self, q, n_tokens: int, stream=None):
         T = int(n_tokens)
@@ -85,8 +86,9 @@ class QSALayer:
 
     def step(self, tok_seq, tok_pos, q, q_idx, w_idx, dirty, stream=None):
         """One QSA step for T tokens; returns the out[:T] view (fp32)."""
-        self.pool_update(dirty, stream)
-        self.index_topk(tok_seq, tok_pos, q_idx, w_idx, stream)
+        d = dirty if isinstance(dirty, torch.Tensor) else _dev(np.asarray(dirty, dtype=np.int32), device=self.device)
+        self.pool_update(d, stream)
+        self.index_topk(tok_seq, tok_pos, q_idx, w_idx, recomputed=d, stream=stream)
         self.sparse_attn(q, int(tok_pos.numel()), stream)
         return self.out[:int(tok_pos.numel())]
 

@@ -76,7 +76,7 @@ def lib():
     L.qsa_index_topk_workspace_size.argtypes = [CP, _I32, _I64]
     L.qsa_index_topk_workspace_size.restype = _SZ
     L.qsa_index_topk.argtypes = [CP, _I32, _I32, _P, _P, _P, _P, _P, _P, _I64, _P, _P, _I32, _I64, _I64,
-                                 _P, _P, _P, _SZ, _P]
+                                 _P, _P, _P, _I32, _P, _SZ, _P]
     L.qsa_index_topk.restype = _I32
     L.qsa_index_topk_noalloc.argtypes = [CP, _I32, _P, _P, _P, _P, _P, _P, _I64, _P, _P, _I32, _I64,
                                          _I64, _P, _P, _P]
@@ -184,11 +184,16 @@ def index_topk_workspace_size(cfg, max_tokens: int, max_blocks: int) -> int:
 
 
 def index_topk(cfg, q_idx, w_idx, tok_seq, tok_pos, pooled, blk_cells, seq_blk_off, seq_blk_slots,
-               max_blocks: int, n_cells: int, cells, count, workspace, max_tokens: int, stream=None):
+               max_blocks: int, n_cells: int, cells, count, workspace, max_tokens: int,
+               recomputed=None, stream=None):
     """workspace: a uint8 CUDA tensor of index_topk_workspace_size(cfg,
-    max_tokens, max_blocks) bytes, zero-filled once when allocated."""
+    max_tokens, max_blocks) bytes, zero-filled once when allocated.
+    recomputed: optional int32 CUDA tensor, the dirty list of the pool update
+    issued just before on the same stream (a scheduling hint)."""
     import torch
     T = int(tok_pos.numel())
+    rec_ptr = _ptr(recomputed, torch.int32, "recomputed") if recomputed is not None else None
+    rec_n = int(recomputed.numel()) if recomputed is not None else 0
     st = lib().qsa_index_topk(
         ctypes.byref(cfg), T, int(max_tokens), _ptr(q_idx, torch.float32, "q_idx"),
         _ptr(w_idx, torch.float32, "w_idx"),
@@ -197,7 +202,7 @@ def index_topk(cfg, q_idx, w_idx, tok_seq, tok_pos, pooled, blk_cells, seq_blk_o
         int(pooled.shape[0]), _ptr(seq_blk_off, torch.int64, "seq_blk_off"),
         _ptr(seq_blk_slots, torch.int32, "seq_blk_slots"), int(seq_blk_off.numel()) - 1,
         int(max_blocks), int(n_cells), _ptr(cells, torch.int32, "cells"),
-        _ptr(count, torch.int32, "count"), _ptr(workspace, torch.uint8, "workspace"),
+        _ptr(count, torch.int32, "count"), rec_ptr, rec_n, _ptr(workspace, torch.uint8, "workspace"),
         int(workspace.numel()), _stream(stream))
     _check(st, "qsa_index_topk")
 

@@ -70,7 +70,7 @@ def test_null_and_workspace_checks(L):
     assert L.qsa_pool_update(ctypes.byref(c), fake, -1, fake, fake, 10, fake, 4, fake, fake, None) == -1
     need = L.qsa_index_topk_workspace_size(ctypes.byref(c), 5, 62_532)
     assert need > 5 * 62_532 * 4
-    args = [ctypes.byref(c), 5, 5] + [fake] * 6 + [100, fake, fake, 1, 62_532, 1000, fake, fake]
+    args = [ctypes.byref(c), 5, 5] + [fake] * 6 + [100, fake, fake, 1, 62_532, 1000, fake, fake, None, 0]
     assert L.qsa_index_topk(*args, fake, need - 1, None) == -4
     assert L.qsa_index_topk(*args, ctypes.c_void_p(0x10010), need, None) == -4   # misaligned
     assert L.qsa_index_topk(*args, None, need, None) == -4
@@ -81,13 +81,15 @@ def test_null_and_workspace_checks(L):
     assert L.qsa_sparse_attn(*bad, None, 0, None) == -1
     assert L.qsa_sparse_attn(ctypes.byref(c), 5, None, fake, fake, 1000, fake, fake, fake, None, 0, None) == -1
     assert L.qsa_index_topk(ctypes.byref(c), 70_000, 70_000, *([fake] * 6), 100, fake, fake, 1, 10, 10,
-                            fake, fake, fake, need, None) == -3
+                            fake, fake, None, 0, fake, need, None) == -3
+    # a hint length without a list
+    assert L.qsa_index_topk(*args[:-2], None, 3, fake, need, None) == -1
     # more tokens than the workspace was sized for
     assert L.qsa_index_topk(ctypes.byref(c), 6, 5, *([fake] * 6), 100, fake, fake, 1, 10, 10,
-                            fake, fake, fake, need, None) == -2
+                            fake, fake, None, 0, fake, need, None) == -2
     # beyond the selection kernel's per-token block limit
     assert L.qsa_index_topk(ctypes.byref(c), 1, 1, *([fake] * 6), 100, fake, fake, 1, (1 << 20) + 1, 10,
-                            fake, fake, fake, need, None) == -3
+                            fake, fake, None, 0, fake, need, None) == -3
     assert L.qsa_status_string(-4) == b"workspace null, misaligned or too small"
 
 
