@@ -16,6 +16,7 @@ Workloads (seeded, synthetic; shapes of the qwen4exp QSA layer):
   5x250k_q8  5 seqs x 250,000 cells in one q8_0 cache, 5 tokens per step
   tiny       1 seq, 4,096 cells
   prefill    512-token ubatch on a 250,000-cell fp16 prompt
+  verify5_250k_q8  1 seq, 250,000-cell q8_0 prompt, 5 consecutive query tokens per step
 
 --impl reference times the CPU oracle (NumPy float64) on the host cores on
 the same workload, as the slow baseline arm.
@@ -45,6 +46,8 @@ DESCR = {
     "5x250k_q8": "decode, 5 seqs x 250,000 cells in one 1.25M-cell q8_0 cache, 5 tokens/step, top_k=2048 per seq",
     "tiny": "decode, 1 seq, 4,096 cells fp16, top_k=2048",
     "prefill": "prefill ubatch, 512 tokens appended to a 250,000-cell fp16 prompt, 128 dirty blocks",
+    "verify5_250k_q8": "verify batch, 1 seq, 250,000-cell q8_0 K/V prompt + 5 consecutive query tokens/step, "
+                       "same heads, top_k=2048",
 }
 
 

@@ -21,7 +21,7 @@ from typing import List, Optional
 
 import numpy as np
 
-CONFIG_NAMES = ("tiny", "50k", "250k_q8", "5x250k_q8", "prefill")
+CONFIG_NAMES = ("tiny", "50k", "250k_q8", "5x250k_q8", "prefill", "verify5_250k_q8")
 
 
 def default_cfg(**over) -> dict:
@@ -175,6 +175,8 @@ PRESETS = {
     "250k_q8": (1, 250_000, 128, 1, "q8_0"),
     "5x250k_q8": (5, 250_000, 128, 1, "q8_0"),
     "prefill": (1, 250_000, 1, 512, "f16"),
+    # speculative verify batch: 5 consecutive query tokens of one sequence per step
+    "verify5_250k_q8": (1, 250_000, 128, 5, "q8_0"),
 }
 
 
@@ -183,7 +185,7 @@ def make_workload(name: str = "custom", *, n_seq: Optional[int] = None,
                   tokens_per_step: Optional[int] = None,
                   kv_type: Optional[str] = None, seed: int = 0,
                   shuffled: bool = False, cfg: Optional[dict] = None) -> Workload:
-    """Build a workload.  Named presets: tiny, 50k, 250k_q8, 5x250k_q8, prefill.
+    """Build a workload.  Named presets: tiny, 50k, 250k_q8, 5x250k_q8, prefill, verify5_250k_q8.
 
     Decode (tokens_per_step == 1): every step appends one position to each
     sequence and queries it; n_seq tokens per step.  Prefill

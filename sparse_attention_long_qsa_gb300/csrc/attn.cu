@@ -44,7 +44,6 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr int kThreads = 256;
 constexpr int kTile = 128;          // cells per MMA tile (M of the QK product)
 constexpr int kMaxCluster = 16;
-constexpr unsigned kErrTimeout = 32u;
 constexpr uint32_t kTmemCols = 64;  // S: cols [0,16); O half 0: [16,32); O half 1: [32,48)
 
 // ---- shared-memory layout (offsets from a 1024-byte aligned base)

@@ -56,6 +56,7 @@ constexpr int kSelBatch = 16;             // score words a warp loads before usi
 constexpr int kSelSlots = 16384;          // slot ids a CTA prefetches (rank 0: all, when they fit)
 constexpr int kCentralBlocks = kSelMaxWords * 32 / 2;   // tokens up to 65536 blocks finish in CTA 0
 constexpr int kRankMax = 1024;            // threshold-bin keys resolved by direct ranking
+static_assert(kRankMax <= kSelLocalCand, "the cut-off digit's keys reuse the candidate list");
 constexpr int kSelList = 2048;            // chosen blocks a CTA lists before expanding
 
 // Per-token histogram at the front of the workspace.  Zero on first use;
@@ -310,6 +311,7 @@ struct SelSmem {
   unsigned selc[kSelCluster];            // chosen threshold-bin keys per CTA (rank path)
   unsigned ncand;
   unsigned ncent;                        // keys gathered in CTA 0 (central path)
+  unsigned ncut;                         // keys in the cut-off digit (central path)
   unsigned cbase;
   unsigned sel;
   int digit;
@@ -507,22 +509,30 @@ k_select(const IndexArgs a, void* ws, const float* __restrict__ scores,
           cum = nxt;
         }
       }
+      if (tid == 0) sm.ncut = 0u;
       __syncthreads();
       const unsigned dstar = (unsigned)sm.digit;
       need -= sm.above;
+      // keys above the cut-off digit are chosen; the digit's own keys (a few)
+      // are gathered into this CTA's now unused candidate list and ranked
+      // among themselves
       for (unsigned i = tid; i < nall; i += kSelThreads) {
         const unsigned long long c = sm.allc[i];
         const unsigned d = (unsigned)(c >> 48) & 255u;
-        bool take = d > dstar;
-        if (d == dstar) {
-          unsigned above_c = 0;
-          for (unsigned m = 0; m < nall; ++m) {
-            const unsigned long long o = sm.allc[m];
-            above_c += (((unsigned)(o >> 48) & 255u) == dstar && o > c) ? 1u : 0u;
-          }
-          take = above_c < need;
+        if (d > dstar) {
+          const int64_t j = (int64_t)(~(uint32_t)(c >> 4));
+          atomicOr(&sm.bitmap[j >> 5], 1u << (j & 31));
+        } else if (d == dstar) {
+          sm.cand[atomicAdd(&sm.ncut, 1u)] = c;     // ncut <= nall <= kRankMax < kSelLocalCand
         }
-        if (take) {
+      }
+      __syncthreads();
+      const unsigned ncut = sm.ncut;
+      for (unsigned i = tid; i < ncut; i += kSelThreads) {
+        const unsigned long long c = sm.cand[i];
+        unsigned above_c = 0;
+        for (unsigned m = 0; m < ncut; ++m) above_c += sm.cand[m] > c ? 1u : 0u;
+        if (above_c < need) {
           const int64_t j = (int64_t)(~(uint32_t)(c >> 4));
           atomicOr(&sm.bitmap[j >> 5], 1u << (j & 31));
         }

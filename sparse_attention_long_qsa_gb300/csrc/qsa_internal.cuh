@@ -17,6 +17,7 @@ enum : unsigned {
   kErrCell = 2u,       // a cell index outside [0, n_cells) where a cell is required
   kErrBlockList = 4u,  // a sequence's block list shorter than its tokens need
   kErrMaxBlocks = 8u,  // floor((p+1)/r) above the caller's max_blocks
+  kErrTimeout = 32u,   // a bounded wait on a CTA's own copies or MMAs gave up
 };
 
 constexpr int kHeadDim = 256;     // DKQ = DV
