@@ -250,6 +250,76 @@ def sparse_attn(cfg: dict, q: np.ndarray, k_cache, v_cache, n_cells: int,
 
 
 # --------------------------------------------------------------------------
+# Append of new cells (the cache write of the step's own K/V and indexer key)
+# --------------------------------------------------------------------------
+def q8_0_block(x32: np.ndarray):
+    """q8_0 encoding of one block of 32 values ([ISSUE] q8-compact follow-up
+    and [README] section 1 run "q8_0" K/V; the pages name the format, not its
+    rounding).  Reading: scale d = max|x| / 127 and codes q = x * (1/d)
+    rounded half away from zero, clamped to +-127, with every operation in
+    float32 (the precision in which the kernel takes the same integer
+    decision); d is stored as fp16.  A block of zeros gives d = 0, q = 0.
+    Returns (q int8 [32], d float16)."""
+    x = np.asarray(x32, dtype=np.float32).reshape(32)
+    amax = np.float32(0.0)
+    for v in x:
+        a = np.float32(abs(v))
+        if a > amax:
+            amax = a
+    d = np.float32(amax / np.float32(127.0))
+    inv = np.float32(np.float32(1.0) / d) if d != 0 else np.float32(0.0)
+    q = np.zeros(32, dtype=np.int8)
+    for i, v in enumerate(x):
+        t = np.float32(v * inv)
+        m = int(np.floor(np.float32(abs(t)) + np.float32(0.5)))   # half away from zero
+        m = min(m, 127)
+        q[i] = -m if t < 0 else m
+    return q, np.float16(d)
+
+
+def kv_append(cfg: dict, tok_seq, tok_pos, cells, k_new, v_new, idx_new, k_cache, v_cache, idx_k,
+              n_cells: int, blk_cells, seq_blk_off, seq_blk_slots, n_dirty: int):
+    """Write the step's new cells into the caches and the block table, and
+    list the blocks that changed ([ISSUE] lever2b: block members live in a
+    device table; lever2: only dirtied blocks are re-pooled, their count padded
+    to a power of two by the caller).  For token t at position p of sequence
+    s occupying cell c: K/V rows of c <- k_new[t], v_new[t] (fp16 copied, or
+    q8_0-encoded per 32-value block by q8_0_block), idx_k[c] <- idx_new[t],
+    blk_cells[slot(s, p // r)][p % r] <- c.  dirty = the distinct slots of the
+    touched blocks, ascending, padded with -1 to n_dirty entries.
+    Returns updated copies (k_cache, v_cache, idx_k, blk_cells) and dirty."""
+    r, G, D = cfg["compress_ratio"], cfg["n_kv_heads"], cfg["head_dim"]
+    kc, vc = np.array(k_cache, copy=True), np.array(v_cache, copy=True)
+    ik, tbl = np.array(idx_k, copy=True), np.array(blk_cells, copy=True)
+    touched = set()
+    for t in range(len(tok_pos)):
+        s, p, c = int(tok_seq[t]), int(tok_pos[t]), int(cells[t])
+        slot = int(seq_blk_slots[int(seq_blk_off[s]) + p // r])
+        tbl[slot, p % r] = c
+        ik[c] = idx_new[t]
+        touched.add(slot)
+        for cache, rows in ((kc, k_new[t]), (vc, v_new[t])):
+            if cfg["kv_type"] == "f16":
+                cache.reshape(n_cells, G, D)[c] = rows
+                continue
+            raw = cache.view(np.uint8)
+            nq = n_cells * G * D
+            qs = raw[:nq].view(np.int8).reshape(n_cells, G, D)
+            dd = raw[nq:nq + n_cells * G * (D // 32) * 2].view(np.float16).reshape(n_cells, G, D // 32)
+            for g in range(G):
+                for b in range(D // 32):
+                    q, d = q8_0_block(np.asarray(rows[g, 32 * b:32 * b + 32], dtype=np.float32))
+                    qs[c, g, 32 * b:32 * b + 32] = q
+                    dd[c, g, b] = d
+    dirty = np.full(n_dirty, -1, dtype=np.int32)
+    srt = sorted(touched)
+    if len(srt) > n_dirty:
+        raise ValueError("more dirty blocks than the list holds")
+    dirty[:len(srt)] = srt
+    return kc, vc, ik, tbl, dirty
+
+
+# --------------------------------------------------------------------------
 # One whole step
 # --------------------------------------------------------------------------
 def run_step(cfg: dict, idx_k, k_cache, v_cache, n_cells, blk_cells,

@@ -68,6 +68,10 @@ class Step:
     w_idx: np.ndarray        # fp32 [T][HI]
     dirty: np.ndarray        # int32 [pow2 >= 4] slots whose blocks gained cells, -1 = no-op
     new_pos: List[np.ndarray]  # per seq: positions appended by this step
+    cells: np.ndarray = None   # int32 [T] the cell each token's own (new) position occupies
+    k_new: np.ndarray = None   # fp16 [T][G][D] K row of that cell before any cache encoding
+    v_new: np.ndarray = None   # fp16 [T][G][D]
+    idx_new: np.ndarray = None  # fp16 [T][DI] its indexer key
 
 
 @dataclasses.dataclass
@@ -158,14 +162,21 @@ def _normal_f16(rng, shape, chunk_rows=65536):
     return out
 
 
-def _normal_q8_0(rng, n_cells, G, D, chunk_rows=65536):
+def _normal_q8_0(rng, n_cells, G, D, keep=None, chunk_rows=65536):
+    """q8_0 cache bytes of N(0,1) rows rounded to fp16 (the K/V precision a
+    model writes), and the fp16 rows of the sorted cells `keep` (the cells
+    appended by the steps, so that an append can be fed the same rows)."""
     qs = np.empty((n_cells, G, D), dtype=np.int8)
     d = np.empty((n_cells, G, D // 32), dtype=np.float16)
+    kept = np.empty((0 if keep is None else len(keep), G, D), dtype=np.float16)
     for a in range(0, n_cells, chunk_rows):
         b = min(n_cells, a + chunk_rows)
-        x = rng.standard_normal((b - a, G, D), dtype=np.float32)
-        qs[a:b], d[a:b] = quantize_q8_0(x)
-    return np.concatenate([qs.reshape(-1).view(np.uint8), d.reshape(-1).view(np.uint8)])
+        x = rng.standard_normal((b - a, G, D), dtype=np.float32).astype(np.float16)
+        qs[a:b], d[a:b] = quantize_q8_0(x.astype(np.float32))
+        if keep is not None:
+            lo, hi = np.searchsorted(keep, [a, b])
+            kept[lo:hi] = x[keep[lo:hi] - a]
+    return np.concatenate([qs.reshape(-1).view(np.uint8), d.reshape(-1).view(np.uint8)]), kept
 
 
 PRESETS = {
@@ -285,13 +296,17 @@ def make_workload(name: str = "custom", *, n_seq: Optional[int] = None,
     seq_blk_slots = np.concatenate(seq_slots).astype(np.int32)
 
     # ---- per-cell data
+    step_cells = [np.concatenate([seq_cells[s][step_pos[i][s]] for s in range(n_seq)]).astype(np.int64)
+                  for i in range(n_steps)]
+    new_cells = np.unique(np.concatenate(step_cells)) if n_steps else np.zeros(0, np.int64)
     idx_k = _normal_f16(np.random.default_rng(s_idx), (n_cells, DI))
     if kv_type == "f16":
         k_cache = _normal_f16(np.random.default_rng(s_k), (n_cells, G, D))
         v_cache = _normal_f16(np.random.default_rng(s_v), (n_cells, G, D))
+        k_src, v_src = k_cache[new_cells], v_cache[new_cells]
     elif kv_type == "q8_0":
-        k_cache = _normal_q8_0(np.random.default_rng(s_k), n_cells, G, D)
-        v_cache = _normal_q8_0(np.random.default_rng(s_v), n_cells, G, D)
+        k_cache, k_src = _normal_q8_0(np.random.default_rng(s_k), n_cells, G, D, keep=new_cells)
+        v_cache, v_src = _normal_q8_0(np.random.default_rng(s_v), n_cells, G, D, keep=new_cells)
     else:
         raise ValueError(kv_type)
 
@@ -307,8 +322,11 @@ def make_workload(name: str = "custom", *, n_seq: Optional[int] = None,
         w_idx = rng.random((T, HI), dtype=np.float32)
         dslots = sorted({int(seq_slots[s][int(p) // r]) for s in range(n_seq) for p in step_pos[i][s]})
         dirty = _pad_pow2(np.array(dslots, dtype=np.int32), 4)
+        at = np.searchsorted(new_cells, step_cells[i])
         steps.append(Step(tok_seq, tok_pos, q, q_idx, w_idx, dirty,
-                          [x.astype(np.int32) for x in step_pos[i]]))
+                          [x.astype(np.int32) for x in step_pos[i]],
+                          cells=step_cells[i].astype(np.int32), k_new=k_src[at], v_new=v_src[at],
+                          idx_new=idx_k[step_cells[i]]))
 
     return Workload(
         name=name, cfg=c, n_seq=n_seq, n_cells=n_cells, idx_k=idx_k,

@@ -376,3 +376,88 @@ def test_step_past_budget_is_sparse():
     mask[cells[0]] = True
     ref = _sdpa(st.q[0, :8], wl.k_cache[:n, 0], wl.v_cache[:n, 0], 1 / 16, mask)
     np.testing.assert_allclose(out[0, :8], ref, rtol=1e-10, atol=1e-12)
+
+
+# ------------------------------------------------------------------ append
+def _q8_cases():
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "q8_0_blocks.json")))
+    return [(k, v) for k, v in g.items() if not k.startswith("_")]
+
+
+@pytest.mark.parametrize("name,case", _q8_cases())
+def test_q8_0_block_closed_forms(name, case):
+    x = np.zeros(32, np.float32)
+    x[:len(case["x"])] = case["x"]
+    q, d = O.q8_0_block(x)
+    want = np.zeros(32, np.int8)
+    want[:len(case["q"])] = case["q"]
+    np.testing.assert_array_equal(q, want)
+    assert float(d) == case["d"]
+
+
+def test_q8_0_block_error_bound_and_extremes():
+    rng = np.random.default_rng(5)
+    for _ in range(200):
+        x = (rng.standard_normal(32) * rng.uniform(1e-3, 1e3)).astype(np.float32)
+        q, d = O.q8_0_block(x)
+        d32 = np.abs(x).max() / 127.0
+        # codes are within half a step of x/d; the largest magnitude maps to +-127
+        assert np.all(np.abs(x - d32 * q.astype(np.float64)) <= 0.5 * d32 * (1 + 1e-5))
+        k = int(np.argmax(np.abs(x)))
+        assert abs(int(q[k])) == 127 and np.sign(q[k]) == np.sign(x[k])
+        assert abs(float(d) - d32) <= d32 * 2.0 ** -11
+
+
+def test_q8_0_block_agrees_with_the_input_encoder():
+    """The workload generator encodes its q8_0 caches with its own code; the
+    two independent implementations of the same reading agree bit for bit."""
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal((64, 256)).astype(np.float16).astype(np.float32)
+    qs, d = quantize_q8_0(x)
+    for i in range(64):
+        for b in range(8):
+            q1, d1 = O.q8_0_block(x[i, 32 * b:32 * b + 32])
+            np.testing.assert_array_equal(q1, qs[i, 32 * b:32 * b + 32])
+            assert d1 == d[i, b]
+
+
+@pytest.mark.parametrize("kv_type,shuffled,tps", [("f16", False, 1), ("q8_0", True, 1), ("q8_0", False, 5)])
+def test_kv_append_reproduces_the_workload_state(kv_type, shuffled, tps):
+    """Appending a step's new cells to the state before it gives the state
+    after it: the generator wrote every cell's encoded row up front, so the
+    caches must come out byte-identical, the table equal to the next state,
+    and the dirty list equal to the step's."""
+    n_seq = 1 if tps > 1 else 3
+    wl = make_workload(n_seq=n_seq, prompt_len=[103, 58, 9][:n_seq], n_steps=3, tokens_per_step=tps,
+                       seed=31, shuffled=shuffled, kv_type=kv_type)
+    for i in range(3):
+        st = wl.steps[i]
+        kc, vc, ik, tbl, dirty = O.kv_append(wl.cfg, st.tok_seq, st.tok_pos, st.cells, st.k_new, st.v_new,
+                                             st.idx_new, wl.k_cache, wl.v_cache, wl.idx_k, wl.n_cells,
+                                             wl.blk_cells_state(i), wl.seq_blk_off, wl.seq_blk_slots,
+                                             len(st.dirty))
+        np.testing.assert_array_equal(kc.view(np.uint8), np.asarray(wl.k_cache).view(np.uint8))
+        np.testing.assert_array_equal(vc.view(np.uint8), np.asarray(wl.v_cache).view(np.uint8))
+        np.testing.assert_array_equal(ik, wl.idx_k)
+        np.testing.assert_array_equal(tbl, wl.blk_cells_state(i + 1))
+        np.testing.assert_array_equal(dirty, st.dirty)
+
+
+def test_kv_append_writes_only_the_new_cells():
+    wl = make_workload(n_seq=2, prompt_len=[40, 21], n_steps=1, seed=32, kv_type="q8_0")
+    st = wl.steps[0]
+    zk = np.zeros_like(wl.k_cache)
+    kc, vc, ik, tbl, dirty = O.kv_append(wl.cfg, st.tok_seq, st.tok_pos, st.cells, st.k_new, st.v_new,
+                                         st.idx_new, zk, zk, np.zeros_like(wl.idx_k), wl.n_cells,
+                                         wl.blk_cells_state(0), wl.seq_blk_off, wl.seq_blk_slots, 8)
+    others = np.setdiff1d(np.arange(wl.n_cells), st.cells)
+    assert not O.kv_rows(wl.cfg, kc, wl.n_cells, others, 0).any()
+    assert not ik[others].any()
+    # the new rows dequantise to within half a step of their fp16 source
+    for t, c in enumerate(st.cells):
+        for g in range(2):
+            got = O.kv_rows(wl.cfg, kc, wl.n_cells, [c], g)[0]
+            src = st.k_new[t, g].astype(np.float64)
+            step = np.repeat(np.abs(src.reshape(8, 32)).max(1) / 127.0, 32)
+            assert np.all(np.abs(got - src) <= 0.5 * step + 127 * step * 2.0 ** -11 + 1e-12)
+    assert list(dirty[:2]) == sorted(dirty[:2]) and np.all(dirty[2:] == -1)
