@@ -66,6 +66,8 @@ def _peaks():
 def algorithmic_bytes(wl, step_idx: int):
     """Algorithmic bytes of each kernel for one step (what the method must
     move at least once), by stage:
+      append: per new cell its fp16 K/V rows read and written in the cache's
+              encoding, its indexer key read and written, table entry, dirty list
       pool:   per dirty slot r fp16 idx-key rows (256 B) + table row + 512 B write
       score:  per visible block a 512 B pooled row + 4 B slot id + 4 B score write,
               plus the token's 2 KiB query and 16 B weights
@@ -80,8 +82,12 @@ def algorithmic_bytes(wl, step_idx: int):
     G = cfg["n_kv_heads"]
     st = wl.steps[step_idx]
     row_b = 2 * 256 if cfg["kv_type"] == "f16" else 256 + 16
-    out = dict(pool=0.0, score=0.0, select=0.0, attn=0.0)
+    out = dict(append=0.0, pool=0.0, score=0.0, select=0.0, attn=0.0)
     nd = int((st.dirty >= 0).sum())
+    T = len(st.tok_pos)
+    # per new cell: its K and V rows read (fp16) and written (cache encoding),
+    # its indexer key read and written, token ids, the table entry, the dirty list
+    out["append"] = T * (2 * G * 512 + 2 * G * row_b + 2 * 256 + 3 * 4 + 4) + 4 * max(4, T)
     out["pool"] = nd * (r * 256 + 4 * r + 4 + 512)
     for p in st.tok_pos.tolist():
         nb = (p + 1) // r
@@ -150,8 +156,9 @@ class Clocks:
 # ---------------------------------------------------------------------------
 class OracleRunner:
     """The CPU oracle as it stands, stepping through a workload: each step
-    appends the step's cells, then runs the full oracle step (pool the dirty
-    blocks, score every visible block, select, expand, attend).  For steps
+    appends the step's cells (caches, keys, table), then runs the full oracle
+    step (pool the dirty blocks, score every visible block, select, expand,
+    attend).  For steps
     with many tokens (prefill) a bounded sample of the tokens is attended."""
 
     def __init__(self, wl, max_tokens_per_step: int = 8):
@@ -174,9 +181,14 @@ class OracleRunner:
         i %= len(wl.steps)
         if i == 0:
             self.table = self.table0.copy()
-        s, rows = self.append_rows(wl, i)
-        self.table[s] = rows
         st = wl.steps[i]
+        a = time.perf_counter()
+        # the step's own cells: K/V rows (encoded as the cache stores them),
+        # indexer keys and table entries, written in place
+        self.O.kv_append(wl.cfg, st.tok_seq, st.tok_pos, st.cells, st.k_new, st.v_new, st.idx_new,
+                         wl.k_cache, wl.v_cache, wl.idx_k, wl.n_cells, self.table, wl.seq_blk_off,
+                         wl.seq_blk_slots, len(st.dirty), inplace=True)
+        t_append = time.perf_counter() - a
         if len(st.tok_pos) > self.cap:
             import dataclasses
             sel = np.linspace(0, len(st.tok_pos) - 1, self.cap).astype(int)
@@ -186,7 +198,7 @@ class OracleRunner:
         self.pooled, _, _ = O.run_step(wl.cfg, wl.idx_k, wl.k_cache, wl.v_cache, wl.n_cells, self.table,
                                        wl.slot_block_idx, wl.seq_blk_off, wl.seq_blk_slots, wl.norm_w,
                                        self.pooled, st)
-        self.last_s = time.perf_counter() - a
+        self.last_s = time.perf_counter() - a + t_append
         return len(st.tok_pos)
 
 
@@ -272,11 +284,14 @@ class _ExternalEvents:
             raise RuntimeError(f"cudaEventRecordWithFlags failed: {st}")
 
 
-def measure_config(name, K, W, dev, *, e2e=True, clocks=None):
+def measure_config(name, K, W, dev, *, path="full", e2e=True, clocks=None):
     """Time K decode steps of workload `name` on the device.  The K timed
-    steps are captured as ONE CUDA graph: per step, the block-table append and
-    an L2 flush (outside the step's events), a start event node, the three
-    C-ABI calls (pool_update, index_topk, sparse_attn) and an end event node.
+    steps are captured as ONE CUDA graph: per step an L2 flush (outside the
+    step's events), a start event node, the step, an end event node.  Path
+    "full" (the layer's whole step): qsa_kv_append (the step's new cells and
+    the device dirty list), qsa_pool_update, qsa_index_topk, qsa_sparse_attn.
+    Path "calls": the last three only, the block table appended by a torch
+    index write outside the step's events and the dirty list from the host.
     The graph is replayed once; the step time is end - start of each step."""
     import torch
     from qsa_workload import make_workload
@@ -290,7 +305,8 @@ def measure_config(name, K, W, dev, *, e2e=True, clocks=None):
     L = QSALayer.from_workload(wl, 0, device=dev)
     tbl0 = L.blk_cells.clone()
     L.warm(torch.from_numpy(wl.prompt_dirty()).to(dev))
-    inputs = [step_inputs(st, device=dev) for st in wl.steps]
+    full = path == "full"
+    inputs = [step_inputs(st, device=dev, new_cells=full) for st in wl.steps]
     appends = []
     for i in range(n_steps):
         s_, rows = append_rows(wl, i)
@@ -298,36 +314,47 @@ def measure_config(name, K, W, dev, *, e2e=True, clocks=None):
     flush = torch.empty(FLUSH_BYTES[0] // 4, dtype=torch.float32, device=dev)
     toks = [len(st.tok_pos) for st in wl.steps]
     alg = [algorithmic_bytes(wl, i) for i in range(n_steps)]
-    kernels = list(qsa.KERNELS)
+    kernels = ["append", "pool", "score", "select", "attn"] if full else ["pool", "score", "select", "attn"]
+    if not full:
+        for a in alg:
+            a.pop("append")
+    step_fn = L.full_step if full else L.step
     xev = _ExternalEvents()
 
     def do_append(i):
+        # outside the step's events: the table back to the prompt state when
+        # the workload wraps around, and (path "calls") the step's own entries
         if i == 0:
             L.blk_cells.copy_(tbl0)
-        s_, rows = appends[i]
-        L.blk_cells[s_] = rows
+        if not full:
+            s_, rows = appends[i]
+            L.blk_cells[s_] = rows
 
     def order(start, n):
         return [(start + k) % n_steps for k in range(n)]
 
     def set_state(start):
+        # the table as it stands before step `start` (every earlier step's
+        # entries present), set up outside any timed region
         L.blk_cells.copy_(tbl0)
         for i in range(start % n_steps):
-            do_append(i)
+            s_, rows = appends[i]
+            L.blk_cells[s_] = rows
 
     # eager warm-up: W steps (also loads the module, sets kernel attributes)
     set_state(0)
     for i in order(0, max(W, 1)):
         do_append(i)
-        L.step(**inputs[i])
+        step_fn(**inputs[i])
     torch.cuda.synchronize()
 
+    io_keys = ("tok_seq", "tok_pos", "q", "q_idx", "w_idx") + (
+        ("cells", "k_new", "v_new", "idx_new") if full else ("dirty",))
     host = None
     if e2e:
         host = []
         for i, st in enumerate(wl.steps):
-            h = {k: torch.from_numpy(np.ascontiguousarray(getattr(st, k))).pin_memory()
-                 for k in ("tok_seq", "tok_pos", "q", "q_idx", "w_idx", "dirty")}
+            h = {k: torch.from_numpy(np.ascontiguousarray(getattr(st, k))).pin_memory() for k in io_keys}
             h["out"] = torch.empty((toks[i], wl.cfg["n_q_heads"], wl.cfg["head_dim"]),
                                    dtype=torch.float32).pin_memory()
             host.append(h)
@@ -349,9 +376,9 @@ def measure_config(name, K, W, dev, *, e2e=True, clocks=None):
                 xev.record(ev[n][0])
                 d = inputs[i]
                 if with_io:
-                    for key in ("tok_seq", "tok_pos", "q", "q_idx", "w_idx", "dirty"):
+                    for key in io_keys:
                         d[key].copy_(host[i][key], non_blocking=True)
-                L.step(**d)
+                step_fn(**d)
                 if with_io:
                     host[i]["out"].copy_(L.out[:toks[i]], non_blocking=True)
                 xev.record(ev[n][1])
@@ -389,7 +416,8 @@ def measure_config(name, K, W, dev, *, e2e=True, clocks=None):
     dom_bytes = float(np.mean([alg[i][dominant] for i in idx]))
     dev_ms = float(np.sum(ms))
     tokens = sum(toks[i] for i in idx)
-    res = dict(value=tokens / (dev_ms / 1e3), ms_per_step=dev_ms / K, tokens=tokens, wall_s=wall,
+    res = dict(value=tokens / (dev_ms / 1e3), ms_per_step=dev_ms / K, tokens=tokens, wall_s=wall, path=path,
+               launches_per_step=len(kernels),
                dominant=dominant, longest=longest, dom_ms=dom_ms, dom_bytes=dom_bytes, kern_us=kern_us,
                kern_gbs={k: kbytes[k] / (kern_us[k] * 1e-6) / 1e9 for k in kernels if kern_us[k] > 0},
                gen_s=t_gen, wl=wl, step_bytes=float(np.mean([sum(alg[i].values()) for i in idx])),
@@ -399,8 +427,7 @@ def measure_config(name, K, W, dev, *, e2e=True, clocks=None):
         # the same steps from pinned host buffers: inputs H2D and the output
         # D2H inside each step's events
         ms2, _ = run_graph(idx, with_io=True)
-        keys = ("tok_seq", "tok_pos", "q", "q_idx", "w_idx", "dirty")
-        h2d = float(np.mean([sum(host[i][k].numel() * host[i][k].element_size() for k in keys) for i in idx]))
+        h2d = float(np.mean([sum(host[i][k].numel() * host[i][k].element_size() for k in io_keys) for i in idx]))
         d2h = float(np.mean([host[i]["out"].numel() * 4 for i in idx]))
         res["e2e"] = {"value": tokens / (float(np.sum(ms2)) / 1e3), "unit": "tokens/s",
                       "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
@@ -432,7 +459,7 @@ def run_native(args, rank, world, local):
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    res = measure_config(args.config, args.steps, args.warmup, dev, clocks=clocks)
+    res = measure_config(args.config, args.steps, args.warmup, dev, path=args.path, clocks=clocks)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
@@ -443,12 +470,21 @@ def run_native(args, rank, world, local):
         max_ms = res["ms_per_step"] * args.steps
     value = world * res["tokens"] / (max_ms / 1e3)
 
+    other = "calls" if args.path == "full" else "full"
+    paths = {args.path: {"value": res["value"], "ms_per_step": res["ms_per_step"],
+                         "launches_per_step": res["launches_per_step"]}}
+    if rank == 0 and args.compare:
+        ro = measure_config(args.config, args.steps, args.warmup, dev, path=other, e2e=False)
+        paths[other] = {"value": ro["value"], "ms_per_step": ro["ms_per_step"],
+                        "launches_per_step": ro["launches_per_step"],
+                        "kernels_us": {k: round(v, 3) for k, v in ro["kern_us"].items()}}
+
     secondary = {}
     if args.secondary and rank == 0:
         for name in args.secondary.split(","):
             if name == args.config or name in ("", "none"):
                 continue
-            r2 = measure_config(name, min(args.steps, 128), args.warmup, dev, e2e=False)
+            r2 = measure_config(name, min(args.steps, 128), args.warmup, dev, path=args.path, e2e=False)
             secondary[name] = {
                 "workload": DESCR[name], "value": r2["value"], "unit": "tokens/s",
                 "ms_per_step": r2["ms_per_step"],
@@ -479,7 +515,13 @@ def run_native(args, rank, world, local):
         "data": "synthetic (seeded N(0,1) K/V/keys, U(0,1) weights)",
         "config": {"workload": DESCR[args.config], "name": args.config,
                    "tokens_per_step": len(wl.steps[0].tok_pos),
-                   "launch": "the K timed steps captured as one CUDA graph (per step: table append, L2 flush, start event, 3 C-ABI calls = 4 kernels chained by programmatic dependent launch, end event), replayed once",
+                   "path": args.path,
+                   "launch": ("the K timed steps captured as one CUDA graph (per step: L2 flush, start event, "
+                              + ("qsa_kv_append + qsa_pool_update + qsa_index_topk + qsa_sparse_attn = 5 kernels"
+                                 if args.path == "full" else
+                                 "table append outside the events, qsa_pool_update + qsa_index_topk + "
+                                 "qsa_sparse_attn = 4 kernels")
+                              + " chained by programmatic dependent launch, end event), replayed once"),
                    "l2": f"flushed before every step ({FLUSH_BYTES[0] >> 20} MiB write), outside the step's events",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"kernel": res["dominant"], "choice": "kernel moving the most algorithmic bytes per step",
@@ -495,7 +537,8 @@ def run_native(args, rank, world, local):
         "step_gbs": res["step_bytes"] / (res["ms_per_step"] * 1e-3) / 1e9,
         "cpu_baseline": cpu,
         "e2e": res.get("e2e"),
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": res["launches_per_step"] * args.steps,
+        "paths": paths,
         "clocks": res["clocks"],
         "secondary": secondary or None,
     }
@@ -513,6 +556,11 @@ def main():
     ap.add_argument("--config", default="50k", choices=list(DESCR))
     ap.add_argument("--secondary", default="250k_q8,5x250k_q8",
                     help="comma list of further workloads timed on rank 0 ('none': no others)")
+    ap.add_argument("--path", default="full", choices=["full", "calls"],
+                    help="full: append + pool + index + attention (the layer's whole step); "
+                         "calls: the last three, the table appended outside the timed region")
+    ap.add_argument("--no-compare", dest="compare", action="store_false",
+                    help="do not also time the other path")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--flush-mb", type=int, default=1024,

@@ -5,6 +5,8 @@
  * qwen4exp (Qwen3.8-Flash-Next) CUDA: decode slows linearly with context"),
  * in the fix summary's sections lever1, lever2, lever2b, lever3 and sparse256:
  *
+ *   qsa_kv_append     the step's new K/V cells, indexer keys and block-table
+ *                     entries, and the list of blocks they dirty (lever2b)
  *   qsa_pool_update   persistent pooled block-key cache (lever2, lever2b)
  *   qsa_index_topk    indexer block scores, block-granular top-k, block -> cell
  *                     expansion with the tail cells carried along (lever3)
@@ -95,6 +97,35 @@ qsa_status qsa_config_init(qsa_config* cfg);
  * min(n_kv, indexer_top_k + r - 1) = 2051).  Row pitch of `cells`. */
 int32_t qsa_cells_per_token(const qsa_config* cfg);
 
+/* ---------------------------------------------------------------------------
+ * S0  qsa_kv_append  (issue #28734, fix summary, lever2b: block members live in
+ * a device table; lever2: only dirtied blocks are re-pooled, padded to a power
+ * of two; q8_0 cache: the author's q8-compact follow-up)
+ * Writes the step's new cells and lists the blocks they change, so that the
+ * pool update that follows needs no host round trip.  Token t (sequence
+ * tok_seq[t], position tok_pos[t]) occupies cell cells[t]:
+ *   K/V rows of the cell <- k_new[t], v_new[t]  (fp16 [T][n_kv_heads][head_dim];
+ *       kv_type f16: copied; q8_0: each 32-value block encoded with scale
+ *       d = max|x| / 127 stored as fp16 and codes x * (1/d) rounded half away
+ *       from zero, clamped to +-127, all in fp32)
+ *   idx_k[cell] <- idx_new[t]  (fp16 [T][idx_dim])
+ *   blk_cells[slot(seq, p / r)][p % r] <- cell
+ *   dirty <- the distinct slots of the touched blocks, ascending, padded with
+ *            -1 to n_dirty entries (a qsa_pool_update dirty list).
+ * The block list of each sequence must already hold the slot of every block
+ * a new position falls in.  Tokens must occupy distinct cells and positions.
+ * Limits: n_new <= 1024 (QSA_ERR_UNSUPPORTED beyond); n_dirty >= n_new
+ * (QSA_ERR_SHAPE otherwise: room for every token in a block of its own).
+ * All buffers 16-byte aligned except the int32 arrays.  A token with an
+ * out-of-range sequence, position, block, slot or cell is skipped and flagged
+ * in the device error word. */
+qsa_status qsa_kv_append(const qsa_config* cfg, int32_t n_new,
+                         const int32_t* tok_seq, const int32_t* tok_pos, const int32_t* cells,
+                         const void* k_new, const void* v_new, const void* idx_new,
+                         void* k_cache, void* v_cache, void* idx_k, int64_t n_cells,
+                         int32_t* blk_cells, int64_t n_slots,
+                         const int64_t* seq_blk_off, const int32_t* seq_blk_slots, int32_t n_seq,
+                         int32_t* dirty, int32_t n_dirty, qsa_stream_t stream);
 /* ---------------------------------------------------------------------------
  * S1  qsa_pool_update  (issue #28734, fix summary, lever2 and lever2b)
  * For each dirty slot s (entries < 0 are skipped; the caller pads the list to
@@ -236,7 +267,8 @@ qsa_status qsa_blocks_dirty(const int32_t* old_tbl, const int32_t* new_tbl,
  * current device.  QSA_ERR_DEVICE_BOUNDS if a kernel met an out-of-range
  * index since the last check; *flags (if non-null) receives the bit set:
  * 1 slot, 2 cell, 4 block list too short, 8 token position beyond max_blocks,
- * 16 token with a sequence id outside [0, n_seq) or a negative position. */
+ * 16 token with a sequence id outside [0, n_seq) or a negative position,
+ * 32 a kernel's bounded wait on its own tensor-core work gave up. */
 qsa_status qsa_debug_check(qsa_stream_t stream, uint32_t* flags);
 
 /* Measurement hook (host state, process-wide, not for concurrent use from
@@ -247,7 +279,7 @@ qsa_status qsa_debug_check(qsa_stream_t stream, uint32_t* flags);
  * launch's device time.
  * Kernel ids: 0 pool update (qsa_pool_update), 1 block scores + threshold
  * bin, 3 cluster select + expansion (qsa_index_topk), 4 attention
- * (qsa_sparse_attn); 2 and 5 are reserved.  `before`/`after` are cudaEvent_t
+ * (qsa_sparse_attn), 5 append (qsa_kv_append); 2 is reserved.  `before`/`after` are cudaEvent_t
  * handles; NULL clears.  QSA_ERR_INVALID_ARG for an unknown id. */
 qsa_status qsa_profile_kernel(int32_t kernel, void* before, void* after);
 

@@ -278,7 +278,7 @@ def q8_0_block(x32: np.ndarray):
 
 
 def kv_append(cfg: dict, tok_seq, tok_pos, cells, k_new, v_new, idx_new, k_cache, v_cache, idx_k,
-              n_cells: int, blk_cells, seq_blk_off, seq_blk_slots, n_dirty: int):
+              n_cells: int, blk_cells, seq_blk_off, seq_blk_slots, n_dirty: int, inplace: bool = False):
     """Write the step's new cells into the caches and the block table, and
     list the blocks that changed ([ISSUE] lever2b: block members live in a
     device table; lever2: only dirtied blocks are re-pooled, their count padded
@@ -287,10 +287,14 @@ def kv_append(cfg: dict, tok_seq, tok_pos, cells, k_new, v_new, idx_new, k_cache
     q8_0-encoded per 32-value block by q8_0_block), idx_k[c] <- idx_new[t],
     blk_cells[slot(s, p // r)][p % r] <- c.  dirty = the distinct slots of the
     touched blocks, ascending, padded with -1 to n_dirty entries.
-    Returns updated copies (k_cache, v_cache, idx_k, blk_cells) and dirty."""
+    Returns updated copies (k_cache, v_cache, idx_k, blk_cells) and dirty
+    (with inplace=True the given arrays are updated and returned)."""
     r, G, D = cfg["compress_ratio"], cfg["n_kv_heads"], cfg["head_dim"]
-    kc, vc = np.array(k_cache, copy=True), np.array(v_cache, copy=True)
-    ik, tbl = np.array(idx_k, copy=True), np.array(blk_cells, copy=True)
+    if inplace:
+        kc, vc, ik, tbl = k_cache, v_cache, idx_k, blk_cells
+    else:
+        kc, vc = np.array(k_cache, copy=True), np.array(v_cache, copy=True)
+        ik, tbl = np.array(idx_k, copy=True), np.array(blk_cells, copy=True)
     touched = set()
     for t in range(len(tok_pos)):
         s, p, c = int(tok_seq[t]), int(tok_pos[t]), int(cells[t])

@@ -214,6 +214,31 @@ qsa_status qsa_sparse_attn(const qsa_config* cfg, int32_t n_tokens, const void* 
   return from_cuda(launch_sparse_attn(a, workspace, err, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+qsa_status qsa_kv_append(const qsa_config* cfg, int32_t n_new, const int32_t* tok_seq, const int32_t* tok_pos,
+                         const int32_t* cells, const void* k_new, const void* v_new, const void* idx_new,
+                         void* k_cache, void* v_cache, void* idx_k, int64_t n_cells, int32_t* blk_cells,
+                         int64_t n_slots, const int64_t* seq_blk_off, const int32_t* seq_blk_slots,
+                         int32_t n_seq, int32_t* dirty, int32_t n_dirty, qsa_stream_t stream) {
+  qsa_status st = check_cfg(cfg);
+  if (st != QSA_OK) return st;
+  if (n_new < 0 || n_cells < 0 || n_slots < 0 || n_seq < 0 || n_dirty < 0) return QSA_ERR_INVALID_ARG;
+  if (n_cells > kMaxI32 || n_slots > kMaxI32 || n_new > kAppendMaxTokens) return QSA_ERR_UNSUPPORTED;
+  if (n_new == 0) return QSA_OK;
+  if (n_dirty < n_new) return QSA_ERR_SHAPE;
+  if (!tok_seq || !tok_pos || !cells || !k_new || !v_new || !idx_new || !k_cache || !v_cache || !idx_k ||
+      !blk_cells || !seq_blk_off || !seq_blk_slots || !dirty || n_seq == 0)
+    return QSA_ERR_INVALID_ARG;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(idx_new, 16) || !aligned(k_cache, 16) ||
+      !aligned(v_cache, 16) || !aligned(idx_k, 16) || !aligned(seq_blk_off, 8))
+    return QSA_ERR_INVALID_ARG;
+  unsigned* err = error_word();
+  if (err == nullptr) return QSA_ERR_CUDA;
+  return from_cuda(launch_append(*cfg, n_new, tok_seq, tok_pos, cells, static_cast<const __half*>(k_new),
+                                 static_cast<const __half*>(v_new), static_cast<const __half*>(idx_new), k_cache,
+                                 v_cache, static_cast<__half*>(idx_k), n_cells, blk_cells, n_slots, seq_blk_off,
+                                 seq_blk_slots, n_seq, dirty, n_dirty, err, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 qsa_status qsa_blocks_dirty(const int32_t* old_tbl, const int32_t* new_tbl, int64_t n_slots,
                             int32_t r, int32_t* out_dirty, int32_t cap, int32_t* n_dirty,
                             int32_t pad_pow2_min) {

@@ -1,0 +1,240 @@
+// Append of the step's new cells: K/V rows (fp16 copy or q8_0 encoding),
+// indexer keys, block-table entries, and the list of blocks this dirties.
+//
+// llama.cpp issue #28734 ("decode slows linearly with context"), fix summary:
+// lever2b keeps each block's member cells on the device; lever2 re-pools only
+// the blocks an ubatch dirtied, their count bucketed to a power of two so a
+// captured graph keeps its shape.  Here the dirtied blocks are found on the
+// device from the appended positions, so a step needs no host round trip
+// between writing its cells and re-pooling their blocks.  q8_0 (the author's
+// q8-compact follow-up; README section 1 runs a q8_0 K/V cache): blocks of 32
+// values, scale d = max|x| / 127 stored as fp16, codes x * (1/d) rounded half
+// away from zero, all in fp32.
+//
+// One warp per (token, row): rows 0..G-1 are the K heads, G..2G-1 the V
+// heads, 2G the indexer key together with the table entry.  An extra last CTA
+// builds the dirty list: the distinct slots, ascending, padded with -1.
+// Everything is read and encoded before the grid-dependency wait (the new
+// rows are inputs, not outputs of the preceding kernel); only the stores wait.
+#include "qsa_internal.cuh"
+
+namespace qsa {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kAppThreads = 256;
+constexpr int kAppWarps = kAppThreads / 32;
+
+struct AppendArgs {
+  int n_new;
+  int G;
+  int r;
+  int kv_q8;
+  const int32_t* tok_seq;
+  const int32_t* tok_pos;
+  const int32_t* cell;
+  const __half* k_new;
+  const __half* v_new;
+  const __half* idx_new;
+  unsigned char* k_cache;
+  unsigned char* v_cache;
+  __half* idx_k;
+  int64_t n_cells;
+  int32_t* blk_cells;
+  int64_t n_slots;
+  const int64_t* seq_blk_off;
+  const int32_t* seq_blk_slots;
+  int n_seq;
+  int32_t* dirty;
+  int n_dirty;
+};
+
+// Slot of the block holding token t's position, or -1 when any index is out
+// of range (flagged when `report`).
+__device__ __forceinline__ int token_slot(const AppendArgs& a, int t, int* in_block, unsigned* err, bool report) {
+  const int s = a.tok_seq[t], p = a.tok_pos[t], c = a.cell[t];
+  if (s < 0 || s >= a.n_seq || p < 0) {
+    if (report) atomicOr(err, kErrToken);
+    return -1;
+  }
+  if (c < 0 || c >= a.n_cells) {
+    if (report) atomicOr(err, kErrCell);
+    return -1;
+  }
+  const int64_t off = a.seq_blk_off[s], len = a.seq_blk_off[s + 1] - off;
+  const int64_t j = p / a.r;
+  if (j >= len) {
+    if (report) atomicOr(err, kErrBlockList);
+    return -1;
+  }
+  const int slot = a.seq_blk_slots[off + j];
+  if (slot < 0 || slot >= a.n_slots) {
+    if (report) atomicOr(err, kErrSlot);
+    return -1;
+  }
+  *in_block = p - (int)j * a.r;
+  return slot;
+}
+
+__global__ void __launch_bounds__(kAppThreads)
+k_append(const AppendArgs a, unsigned* err) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (blockIdx.x == gridDim.x - 1) {
+    // ---- the dirty list (n_new <= kAppendMaxTokens, 4 tokens per thread)
+    __shared__ int s_slot[kAppendMaxTokens];
+    __shared__ unsigned s_warp[kAppWarps];
+    for (int t = tid; t < a.n_new; t += kAppThreads) {
+      int ib = 0;
+      s_slot[t] = token_slot(a, t, &ib, err, false);
+    }
+    __syncthreads();
+    // token t leads its slot if no earlier token has it; leaders are ranked
+    // by slot (ascending order of the list)
+    constexpr int kPer = kAppendMaxTokens / kAppThreads;
+    __shared__ unsigned char s_lead[kAppendMaxTokens];
+    int lead_slot[kPer];
+    unsigned nlead = 0;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int t = tid + k * kAppThreads;
+      int sl = t < a.n_new ? s_slot[t] : -1;
+      for (int u = 0; u < t && sl >= 0; ++u)
+        if (s_slot[u] == sl) sl = -1;
+      lead_slot[k] = sl;
+      if (t < a.n_new) s_lead[t] = sl >= 0 ? 1 : 0;
+      nlead += sl >= 0 ? 1u : 0u;
+    }
+    unsigned tot = nlead;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) tot += __shfl_xor_sync(kFull, tot, o);
+    if (lane == 0) s_warp[warp] = tot;
+    __syncthreads();
+    unsigned n_lead = 0;
+    for (int w = 0; w < kAppWarps; ++w) n_lead += s_warp[w];
+    int rank[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      rank[k] = -1;
+      const int sl = lead_slot[k];
+      if (sl < 0) continue;
+      int below = 0;
+      for (int u = 0; u < a.n_new; ++u) below += (s_lead[u] && s_slot[u] < sl) ? 1 : 0;
+      rank[k] = below;
+    }
+    grid_dep_wait();
+    grid_dep_launch();
+#pragma unroll
+    for (int k = 0; k < kAppendMaxTokens / kAppThreads; ++k)
+      if (rank[k] >= 0 && rank[k] < a.n_dirty) a.dirty[rank[k]] = lead_slot[k];
+    for (int i = (int)n_lead + tid; i < a.n_dirty; i += kAppThreads) a.dirty[i] = -1;
+    return;
+  }
+
+  // ---- one warp per (token, row)
+  const int rows = 2 * a.G + 1;
+  const int64_t w = (int64_t)blockIdx.x * kAppWarps + warp;
+  const bool active = w < (int64_t)a.n_new * rows;
+  const int t = active ? (int)(w / rows) : 0;
+  const int kind = active ? (int)(w - (int64_t)t * rows) : 0;
+  int ib = 0;
+  const int slot = active ? token_slot(a, t, &ib, err, kind == 2 * a.G && lane == 0) : -1;
+  const int64_t c = active ? a.cell[t] : 0;
+  const bool ok = active && slot >= 0;
+
+  if (kind < 2 * a.G) {
+    const int g = kind < a.G ? kind : kind - a.G;
+    const __half* src = (kind < a.G ? a.k_new : a.v_new) + ((int64_t)t * a.G + g) * kHeadDim;
+    unsigned char* cache = kind < a.G ? a.k_cache : a.v_cache;
+    const uint4 raw = ok ? __ldg(reinterpret_cast<const uint4*>(src) + lane) : make_uint4(0, 0, 0, 0);
+    if (!a.kv_q8) {
+      grid_dep_wait();
+      grid_dep_launch();
+      if (ok) reinterpret_cast<uint4*>(cache + (c * a.G + g) * kHeadDim * 2)[lane] = raw;
+      return;
+    }
+    // q8_0: lanes 4b..4b+3 hold the 32 values of block b
+    const __half2* h = reinterpret_cast<const __half2*>(&raw);
+    float x[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __half22float2(h[i]);
+      x[2 * i] = f.x;
+      x[2 * i + 1] = f.y;
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+    const float d = amax / 127.0f;
+    const float inv = d != 0.f ? 1.0f / d : 0.f;
+    uint2 qs;
+    signed char* qb = reinterpret_cast<signed char*>(&qs);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float v = x[i] * inv;
+      float m = floorf(fabsf(v) + 0.5f);             // half away from zero
+      m = fminf(m, 127.f);
+      qb[i] = (signed char)(v < 0.f ? -(int)m : (int)m);
+    }
+    grid_dep_wait();
+    grid_dep_launch();
+    if (ok) {
+      reinterpret_cast<uint2*>(cache + (c * a.G + g) * kHeadDim)[lane] = qs;
+      if ((lane & 3) == 0) {
+        __half* sc = reinterpret_cast<__half*>(cache + a.n_cells * (int64_t)a.G * kHeadDim);
+        sc[(c * a.G + g) * (kHeadDim / 32) + (lane >> 2)] = __float2half_rn(d);
+      }
+    }
+    return;
+  }
+  // indexer key row (256 bytes: lanes 0..15) and the table entry
+  uint4 raw = make_uint4(0, 0, 0, 0);
+  if (ok && lane < 16) raw = __ldg(reinterpret_cast<const uint4*>(a.idx_new + (int64_t)t * kIdxDim) + lane);
+  grid_dep_wait();
+  grid_dep_launch();
+  if (!ok) return;
+  if (lane < 16) reinterpret_cast<uint4*>(a.idx_k + c * kIdxDim)[lane] = raw;
+  if (lane == 0) a.blk_cells[(int64_t)slot * a.r + ib] = (int32_t)c;
+}
+
+}  // namespace
+
+cudaError_t launch_append(const qsa_config& cfg, int n_new, const int32_t* tok_seq, const int32_t* tok_pos,
+                          const int32_t* cell, const __half* k_new, const __half* v_new, const __half* idx_new,
+                          void* k_cache, void* v_cache, __half* idx_k, int64_t n_cells, int32_t* blk_cells,
+                          int64_t n_slots, const int64_t* seq_blk_off, const int32_t* seq_blk_slots, int n_seq,
+                          int32_t* dirty, int n_dirty, unsigned* err, cudaStream_t stream) {
+  if (n_new <= 0) return cudaSuccess;
+  AppendArgs a{};
+  a.n_new = n_new;
+  a.G = cfg.n_kv_heads;
+  a.r = cfg.compress_ratio;
+  a.kv_q8 = cfg.kv_type == QSA_KV_Q8_0;
+  a.tok_seq = tok_seq;
+  a.tok_pos = tok_pos;
+  a.cell = cell;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.idx_new = idx_new;
+  a.k_cache = static_cast<unsigned char*>(k_cache);
+  a.v_cache = static_cast<unsigned char*>(v_cache);
+  a.idx_k = idx_k;
+  a.n_cells = n_cells;
+  a.blk_cells = blk_cells;
+  a.n_slots = n_slots;
+  a.seq_blk_off = seq_blk_off;
+  a.seq_blk_slots = seq_blk_slots;
+  a.n_seq = n_seq;
+  a.dirty = dirty;
+  a.n_dirty = n_dirty;
+  const int64_t warps = (int64_t)n_new * (2 * cfg.n_kv_heads + 1);
+  const unsigned blocks = (unsigned)ceil_div(warps, kAppWarps) + 1;   // + the dirty-list CTA
+  prof_before(kKAppend, stream);
+  cudaError_t e = launch_pdl(k_append, dim3(blocks), dim3(kAppThreads), 0, stream, 1, a, err);
+  prof_after(kKAppend, stream);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace qsa

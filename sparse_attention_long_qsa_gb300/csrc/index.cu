@@ -44,7 +44,6 @@ constexpr int kScoreWarps = kScoreThreads / 32;
 constexpr int kScoreUnroll = 2;
 // rows (blocks) one CTA covers per iteration: 8 warps x 4 rows x unroll
 constexpr int kRowsPerIter = kScoreWarps * 4 * kScoreUnroll;
-constexpr int kErrToken = 16;
 constexpr int kMaxHint = 32;              // recomputed-slot hints checked per CTA
 
 constexpr int kSelThreads = 512;
@@ -86,7 +85,7 @@ __device__ __forceinline__ Tok token_geometry(const IndexArgs& a, int t, unsigne
   const int seq = a.tok_seq[t];
   const int p = a.tok_pos[t];
   if (seq < 0 || seq >= a.n_seq || p < 0) {
-    if (report) atomicOr(err, (unsigned)kErrToken);
+    if (report) atomicOr(err, kErrToken);
     return k;
   }
   k.off = a.seq_blk_off[seq];

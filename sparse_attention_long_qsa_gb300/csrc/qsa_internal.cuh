@@ -17,7 +17,8 @@ enum : unsigned {
   kErrCell = 2u,       // a cell index outside [0, n_cells) where a cell is required
   kErrBlockList = 4u,  // a sequence's block list shorter than its tokens need
   kErrMaxBlocks = 8u,  // floor((p+1)/r) above the caller's max_blocks
-  kErrTimeout = 32u,   // a bounded wait on a CTA's own copies or MMAs gave up
+  kErrToken = 16u,     // a token with a sequence id outside [0, n_seq) or a negative position
+  kErrTimeout = 32u,   // a bounded wait on a CTA's own tensor-core work gave up
 };
 
 constexpr int kHeadDim = 256;     // DKQ = DV
@@ -167,7 +168,7 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 
 // ------------------------------------------------------ measurement hook
 // Kernel ids of qsa_profile_kernel (include/qsa.h).
-enum KernelId : int { kKPool = 0, kKScore = 1, kKFilter = 2, kKFinal = 3, kKAttn = 4, kKCombine = 5,
+enum KernelId : int { kKPool = 0, kKScore = 1, kKReserved = 2, kKFinal = 3, kKAttn = 4, kKAppend = 5,
                       kNumKernels = 6 };
 struct ProfileHook {
   cudaEvent_t before[kNumKernels];
@@ -241,5 +242,14 @@ struct AttnArgs {
 
 size_t attn_workspace_bytes(int n_tokens, int n_q_heads, int cells_pitch);
 cudaError_t launch_sparse_attn(const AttnArgs& a, void* ws, unsigned* err, cudaStream_t stream);
+
+// Append of new cells (append.cu).  The dirty list is built by one CTA:
+// at most kAppendMaxTokens tokens per call.
+constexpr int kAppendMaxTokens = 1024;
+cudaError_t launch_append(const qsa_config& cfg, int n_new, const int32_t* tok_seq, const int32_t* tok_pos,
+                          const int32_t* cell, const __half* k_new, const __half* v_new, const __half* idx_new,
+                          void* k_cache, void* v_cache, __half* idx_k, int64_t n_cells, int32_t* blk_cells,
+                          int64_t n_slots, const int64_t* seq_blk_off, const int32_t* seq_blk_slots, int n_seq,
+                          int32_t* dirty, int n_dirty, unsigned* err, cudaStream_t stream);
 
 }  // namespace qsa

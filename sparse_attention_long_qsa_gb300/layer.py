@@ -2,9 +2,10 @@
 
 QSALayer owns the caller-side buffers of include/qsa.h (caches, block tables,
 the pooled block-key cache, workspaces, outputs) as torch CUDA tensors and
-runs a step as the three C-ABI calls on one stream:
+runs a step as the C-ABI calls on one stream:
 
-    pool_update(dirty) -> index_topk(tokens) -> sparse_attn(tokens)
+    step:       pool_update(dirty) -> index_topk(tokens) -> sparse_attn(tokens)
+    full_step:  kv_append(new cells) -> the same three, fed the device dirty list
 
 It holds no arithmetic of its own.
 """
@@ -56,6 +57,7 @@ class QSALayer:
                                     dtype=torch.uint8, device=device)
         self.ws_attn = torch.empty(qsa.sparse_attn_workspace_size(self.cfg, T),
                                    dtype=torch.uint8, device=device)
+        self._dirty = None
 
     @classmethod
     def from_workload(cls, wl, step: int = 0, max_tokens: Optional[int] = None, device="cuda"):
@@ -92,6 +94,30 @@ class QSALayer:
         self.sparse_attn(q, int(tok_pos.numel()), stream)
         return self.out[:int(tok_pos.numel())]
 
+    def kv_append(self, tok_seq, tok_pos, cells, k_new, v_new, idx_new, stream=None):
+        """Write the step's new cells and build the dirty list on the device;
+        returns the dirty-list view (padded to a power of two >= max(4, T))."""
+        T = int(tok_pos.numel())
+        nd = 4
+        while nd < T:
+            nd *= 2
+        if self._dirty is None or self._dirty.numel() < nd:
+            self._dirty = torch.full((max(nd, 4),), -1, dtype=torch.int32, device=self.device)
+        d = self._dirty[:nd]
+        qsa.kv_append(self.cfg, tok_seq, tok_pos, cells, k_new, v_new, idx_new, self.k_cache, self.v_cache,
+                      self.idx_k, self.blk_cells, self.seq_blk_off, self.seq_blk_slots, d, stream)
+        return d
+
+    def full_step(self, tok_seq, tok_pos, q, q_idx, w_idx, cells, k_new, v_new, idx_new, stream=None, **_):
+        """The whole layer step from the new tokens on: append of their cells
+        (K/V, indexer keys, table, device dirty list), pool update, index
+        top-k, sparse attention.  Returns the out[:T] view (fp32)."""
+        d = self.kv_append(tok_seq, tok_pos, cells, k_new, v_new, idx_new, stream)
+        self.pool_update(d, stream)
+        self.index_topk(tok_seq, tok_pos, q_idx, w_idx, recomputed=d, stream=stream)
+        self.sparse_attn(q, int(tok_pos.numel()), stream)
+        return self.out[:int(tok_pos.numel())]
+
     def set_cells(self, slots, rows):
         """Write block-table rows (the append of new cells), device side."""
         s = _dev(np.asarray(slots, dtype=np.int64), device=self.device)
@@ -102,11 +128,16 @@ class QSALayer:
         self.pool_update(dirty_all)
 
 
-def step_inputs(st, device="cuda"):
-    """Device tensors of a qsa_workload.Step."""
-    return dict(tok_seq=_dev(st.tok_seq, device=device), tok_pos=_dev(st.tok_pos, device=device),
-                q=_dev(st.q, device=device), q_idx=_dev(st.q_idx, device=device),
-                w_idx=_dev(st.w_idx, device=device), dirty=_dev(st.dirty, device=device))
+def step_inputs(st, device="cuda", new_cells=False):
+    """Device tensors of a qsa_workload.Step (with new_cells: also the
+    step's own cells and their rows, the inputs of full_step)."""
+    d = dict(tok_seq=_dev(st.tok_seq, device=device), tok_pos=_dev(st.tok_pos, device=device),
+             q=_dev(st.q, device=device), q_idx=_dev(st.q_idx, device=device),
+             w_idx=_dev(st.w_idx, device=device), dirty=_dev(st.dirty, device=device))
+    if new_cells:
+        d.update(cells=_dev(st.cells, device=device), k_new=_dev(st.k_new, device=device),
+                 v_new=_dev(st.v_new, device=device), idx_new=_dev(st.idx_new, device=device))
+    return d
 
 
 def append_rows(wl, step: int):

@@ -26,11 +26,11 @@ STATUS = {0: "QSA_OK", -1: "QSA_ERR_INVALID_ARG", -2: "QSA_ERR_SHAPE", -3: "QSA_
 EXPORTS = ("qsa_config_init", "qsa_cells_per_token", "qsa_pool_update", "qsa_index_scores",
            "qsa_index_topk_workspace_size", "qsa_index_topk", "qsa_index_topk_noalloc",
            "qsa_sparse_attn_workspace_size",
-           "qsa_sparse_attn", "qsa_blocks_dirty", "qsa_debug_check", "qsa_profile_kernel",
+           "qsa_sparse_attn", "qsa_kv_append", "qsa_blocks_dirty", "qsa_debug_check", "qsa_profile_kernel",
            "qsa_status_string")
 
 # Kernel ids of qsa_profile_kernel.
-KERNELS = {"pool": 0, "score": 1, "select": 3, "attn": 4}
+KERNELS = {"pool": 0, "score": 1, "select": 3, "attn": 4, "append": 5}
 
 
 class QSAError(RuntimeError):
@@ -85,6 +85,9 @@ def lib():
     L.qsa_sparse_attn_workspace_size.restype = _SZ
     L.qsa_sparse_attn.argtypes = [CP, _I32, _P, _P, _P, _I64, _P, _P, _P, _P, _SZ, _P]
     L.qsa_sparse_attn.restype = _I32
+    L.qsa_kv_append.argtypes = [CP, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _P, _I64, _P, _P, _I32,
+                                _P, _I32, _P]
+    L.qsa_kv_append.restype = _I32
     L.qsa_blocks_dirty.argtypes = [_P, _P, _I64, _I32, _P, _I32, ctypes.POINTER(_I32), _I32]
     L.qsa_blocks_dirty.restype = _I32
     L.qsa_debug_check.argtypes = [_P, ctypes.POINTER(ctypes.c_uint32)]
@@ -222,6 +225,24 @@ def sparse_attn(cfg, q, k_cache, v_cache, n_cells: int, cells, count, out, works
         _ptr(count, torch.int32, "count"), _ptr(out, torch.float32, "out"),
         ws_ptr, ws_len, _stream(stream))
     _check(st, "qsa_sparse_attn")
+
+
+def kv_append(cfg, tok_seq, tok_pos, cells, k_new, v_new, idx_new, k_cache, v_cache, idx_k, blk_cells,
+              seq_blk_off, seq_blk_slots, dirty, stream=None):
+    """Write the step's new cells (K/V rows, indexer keys, block-table
+    entries) and fill `dirty` with the slots of the blocks they change."""
+    import torch
+    n_cells = int(idx_k.shape[0])
+    st = lib().qsa_kv_append(
+        ctypes.byref(cfg), int(tok_pos.numel()), _ptr(tok_seq, torch.int32, "tok_seq"),
+        _ptr(tok_pos, torch.int32, "tok_pos"), _ptr(cells, torch.int32, "cells"),
+        _ptr(k_new, torch.float16, "k_new"), _ptr(v_new, torch.float16, "v_new"),
+        _ptr(idx_new, torch.float16, "idx_new"), _ptr(k_cache, None, "k_cache"), _ptr(v_cache, None, "v_cache"),
+        _ptr(idx_k, torch.float16, "idx_k"), n_cells, _ptr(blk_cells, torch.int32, "blk_cells"),
+        int(blk_cells.shape[0]), _ptr(seq_blk_off, torch.int64, "seq_blk_off"),
+        _ptr(seq_blk_slots, torch.int32, "seq_blk_slots"), int(seq_blk_off.numel()) - 1,
+        _ptr(dirty, torch.int32, "dirty"), int(dirty.numel()), _stream(stream))
+    _check(st, "qsa_kv_append")
 
 
 def blocks_dirty(old_tbl: np.ndarray, new_tbl: np.ndarray, pad_pow2_min: int = 4) -> np.ndarray:

@@ -120,3 +120,22 @@ def test_binding_refuses_cpu_tensors(L):
     with pytest.raises(ValueError, match="CUDA"):
         qsa.pool_update(c, torch.zeros((4, 128), dtype=torch.float16), torch.zeros((1, 4), dtype=torch.int32),
                         torch.zeros(1, dtype=torch.int32), t, torch.ones(128), torch.zeros((1, 128)))
+
+
+def test_kv_append_host_checks(L):
+    c = qsa.config()
+    f = 0x10000
+    base = [ctypes.byref(c), 4, f, f, f, f, f, f, f, f, f, 1000, f, 100, f, f, 1, f, 4, None]
+    def call(**kw):
+        args = list(base)
+        for i, v in kw.items():
+            args[int(i[1:])] = v
+        return L.qsa_kv_append(*args)
+    assert call(a1=0) == 0                      # nothing to append: no pointer is read
+    assert call(a1=1025) == -3                  # beyond the dirty-list kernel's token limit
+    assert call(a18=3) == -2                    # fewer dirty entries than tokens
+    assert call(a2=None) == -1
+    assert call(a5=f + 8) == -1                 # new K rows must be 16-byte aligned
+    assert call(a10=f + 2) == -1                # indexer keys must be 16-byte aligned
+    assert call(a16=0) == -1                    # no sequence
+    assert L.qsa_kv_append(ctypes.byref(qsa.config(kv_type=7)), *base[1:]) == -1
