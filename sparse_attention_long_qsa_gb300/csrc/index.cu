@@ -31,6 +31,8 @@
 //             the member cells of its chosen blocks at its offset in the
 //             token's list (blocks ascending), CTA 0 appends the tail cells
 //             and clears the histogram for the next call.
+#include <cstring>
+
 #include "qsa_internal.cuh"
 
 QSA_TS_DECLARE(index)
@@ -41,9 +43,15 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kScoreThreads = 256;
 constexpr int kScoreWarps = kScoreThreads / 32;
-constexpr int kScoreUnroll = 2;
-// rows (blocks) one CTA covers per iteration: 8 warps x 4 rows x unroll
-constexpr int kRowsPerIter = kScoreWarps * 4 * kScoreUnroll;
+// Each warp streams its rows through a ring of kRingStages stages of 4 rows
+// (one row per group of 8 lanes) by 16-byte cp.async copies: every lane copies
+// its 16 bytes of each row, so a row is one warp instruction and up to
+// kRingStages x 2 KiB per warp stay in flight without blocking the warp.
+constexpr int kRingStages = 4;
+constexpr int kRingFloats = kScoreWarps * kRingStages * 4 * kIdxDim;
+constexpr int kScoreChunkMax = 2048;      // rows one CTA scores (their slot ids are kept in shared memory)
+constexpr size_t kScoreSmem = sizeof(float) * kRingFloats + sizeof(int32_t) * kScoreChunkMax +
+                              sizeof(unsigned) * kHistBins + sizeof(unsigned short) * kHistBins;
 constexpr int kMaxHint = 32;              // recomputed-slot hints checked per CTA
 
 constexpr int kSelThreads = 512;
@@ -159,31 +167,61 @@ __device__ __forceinline__ unsigned long long cand_key(uint32_t key, int64_t j) 
 // heads (64 fp32 registers), so each group reads the 512-byte row as four
 // fully used 128-byte lines.  The 4 head dot products are reduced across the
 // group with a reduce-scatter (6 shuffles per row in all).
+__device__ __forceinline__ void ring_copy16(float* dst, const float* src, bool valid) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+  const int n = valid ? 16 : 0;   // 0: the 16 bytes are zero-filled
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(d), "l"(src), "r"(n) : "memory");
+}
+
+// Packed fp32 FMA on a pair of lanes of a register pair: d = a * b + c
+// element-wise, each element rounded as fmaf.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  unsigned long long ra, rb, rc, rd;
+  memcpy(&ra, &a, 8);
+  memcpy(&rb, &b, 8);
+  memcpy(&rc, &c, 8);
+  asm("fma.rn.f32x2 %0, %1, %2, %3;\n" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
+  float2 d;
+  memcpy(&d, &rd, 8);
+  return d;
+}
+
 template <bool kTopk>
 __global__ void __launch_bounds__(kScoreThreads, 2)
 k_score(const IndexArgs a, void* ws, float* __restrict__ scores, int chunk, unsigned* err) {
-  // Shared histogram of this CTA's rows plus the list of bins it touched, so
+  // Shared memory: the warps' row rings, the slot ids of this CTA's range,
+  // and a histogram of this CTA's scores plus the list of bins it touched (so
   // the flush to the token's global histogram costs one atomic per touched
-  // bin instead of a sweep of all bins.
-  __shared__ unsigned s_hist[kTopk ? kHistBins : 1];
-  __shared__ unsigned short s_touched[kTopk ? kHistBins : 1];
+  // bin instead of a sweep of all bins).
+  extern __shared__ __align__(16) unsigned char score_smem[];
+  float* ring = reinterpret_cast<float*>(score_smem);
+  int32_t* s_slot = reinterpret_cast<int32_t*>(ring + kRingFloats);
+  unsigned* s_hist = reinterpret_cast<unsigned*>(s_slot + kScoreChunkMax);
+  unsigned short* s_touched = reinterpret_cast<unsigned short*>(s_hist + kHistBins);
   __shared__ unsigned s_ntouched;
+  __shared__ int s_rec[kMaxHint];
 
   const int t = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (kTopk) QSA_TS(index, 0);
-  // ---- before the wait: token geometry, query, first slot ids (not written
-  // by the pool update that precedes this kernel)
+  // ---- before the wait: token geometry, query, slot ids (not written by
+  // the pool update that precedes this kernel)
   const Tok tk = token_geometry(a, t, err, blockIdx.x == 0 && tid == 0);
   const int nb = tk.nb;
   float* srow = scores + (int64_t)t * a.max_blocks;
   const int64_t j0 = (int64_t)blockIdx.x * chunk;
   const int64_t j1 = min((int64_t)nb, j0 + chunk);
+  const int nrows = j1 > j0 ? (int)(j1 - j0) : 0;
   if (kTopk) {
     for (int i = tid; i < kHistBins; i += kScoreThreads) s_hist[i] = 0u;
     if (tid == 0) s_ntouched = 0u;
   }
   unsigned* ghist = kTopk ? hist_of(ws, t) : nullptr;
+  const int32_t* slots = a.seq_blk_slots + tk.off;
+  for (int i = tid; i < nrows; i += kScoreThreads) s_slot[i] = __ldg(slots + j0 + i);
+  const bool use_hint = kTopk && a.recomputed != nullptr && a.n_recomputed <= kMaxHint && blockIdx.x != 0;
+  if (use_hint)
+    for (int i = tid; i < a.n_recomputed; i += kScoreThreads) s_rec[i] = a.recomputed[i];
 
   const int sub = lane & 7, grp = lane >> 3;
   float4 qv[kIdxHeads][4];
@@ -197,30 +235,18 @@ k_score(const IndexArgs a, void* ws, float* __restrict__ scores, int chunk, unsi
   }
   const int bit2 = (lane >> 2) & 1, bit1 = (lane >> 1) & 1;
   const float wh = __ldg(a.w_idx + (int64_t)t * kIdxHeads + bit2 * 2 + bit1);
-  const int32_t* slots = a.seq_blk_slots + tk.off;
-  int slot0[kScoreUnroll];
-  {
-    const int64_t base = j0 + warp * 4 * kScoreUnroll;
-#pragma unroll
-    for (int u = 0; u < kScoreUnroll; ++u) {
-      const int64_t j = base + u * 4 + grp;
-      slot0[u] = j < j1 ? __ldg(slots + j) : 0;
-    }
-  }
+  __syncthreads();
 
   // ---- pooled rows are written by the pool update.  With the list of slots
   // that update recomputed, a CTA none of whose rows is in it reads nothing
   // the update writes and skips the wait; CTA 0 always waits, so this
   // kernel still completes after the update.
   bool must_wait = true;
-  if (kTopk && a.recomputed != nullptr && a.n_recomputed <= kMaxHint && blockIdx.x != 0) {
-    __shared__ int s_rec[kMaxHint];
-    for (int i = tid; i < a.n_recomputed; i += kScoreThreads) s_rec[i] = a.recomputed[i];
-    __syncthreads();
+  if (use_hint) {
     int hit = 0;
-    for (int64_t j = j0 + tid; j < j1; j += kScoreThreads) {
-      const int sl = __ldg(slots + j);
-      for (int i = 0; i < a.n_recomputed; ++i) hit |= (s_rec[i] == sl);
+    for (int i = tid; i < nrows; i += kScoreThreads) {
+      const int sl = s_slot[i];
+      for (int e = 0; e < a.n_recomputed; ++e) hit |= (s_rec[e] == sl);
     }
     must_wait = __syncthreads_or(hit) != 0;
   }
@@ -232,62 +258,78 @@ k_score(const IndexArgs a, void* ws, float* __restrict__ scores, int chunk, unsi
     const int64_t f1 = min(a.max_blocks, j0 + chunk);
     for (int64_t j = max((int64_t)nb, j0) + tid; j < f1; j += kScoreThreads) srow[j] = -INFINITY;
   }
-  if (kTopk) __syncthreads();
 
-  bool first = true;
-  for (int64_t base = j0 + warp * 4 * kScoreUnroll; base < j1; base += kRowsPerIter) {
-    float4 kv[kScoreUnroll][4];
-    bool ok[kScoreUnroll], live[kScoreUnroll];
+  // ---- this warp's rows [r0, r1), 4 per stage
+  const int per_w = (int)round_up(ceil_div(nrows, kScoreWarps), 4);
+  const int r0 = min(nrows, warp * per_w), r1 = min(nrows, r0 + per_w);
+  const int nst = (int)ceil_div(r1 - r0, 4);
+  float* wring = ring + warp * (kRingStages * 4 * kIdxDim);
+  // lane l copies row l / 8 of a stage: chunk k * 8 + l % 8 (16 bytes) for
+  // k = 0..3, so each copy instruction moves one whole 128-byte line of each
+  // of the 4 rows and every lane computes one row address per stage
+  auto issue = [&](int st) {
+    if (st < nst) {
+      const int i = r0 + st * 4 + grp;
+      const int slot = i < r1 ? s_slot[i] : -1;
+      const bool ok = slot >= 0 && slot < a.n_slots;
+      float* dst = wring + ((st % kRingStages) * 4 + grp) * kIdxDim + sub * 4;
+      const float* src = a.pooled + (int64_t)(ok ? slot : 0) * kIdxDim + sub * 4;
 #pragma unroll
-    for (int u = 0; u < kScoreUnroll; ++u) {
-      const int64_t j = base + u * 4 + grp;
-      live[u] = j < j1;
-      int slot = first ? slot0[u] : (live[u] ? __ldg(slots + j) : 0);
-      ok[u] = live[u] && slot >= 0 && slot < a.n_slots;
-      if (live[u] && !ok[u] && sub == 0) atomicOr(err, kErrSlot);
-      const float4* row = reinterpret_cast<const float4*>(a.pooled + (int64_t)(ok[u] ? slot : 0) * kIdxDim);
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        kv[u][k] = ok[u] ? __ldg(row + k * 8 + sub) : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int k = 0; k < 4; ++k) ring_copy16(dst + k * 32, src + k * 32, ok);
     }
-    first = false;
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+  };
 #pragma unroll
-    for (int u = 0; u < kScoreUnroll; ++u) {
-      float acc[kIdxHeads];
+  for (int st = 0; st < kRingStages - 1; ++st) issue(st);
+
+  for (int it = 0; it < nst; ++it) {
+    issue(it + kRingStages - 1);
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(kRingStages - 1) : "memory");
+    __syncwarp();
+    const int i = r0 + it * 4 + grp;
+    const bool live = i < r1;
+    const int slot = live ? s_slot[i] : 0;
+    const bool ok = live && slot >= 0 && slot < a.n_slots;
+    if (live && !ok && sub == 0) atomicOr(err, kErrSlot);
+    const float4* row = reinterpret_cast<const float4*>(wring + ((it % kRingStages) * 4 + grp) * kIdxDim);
+    float4 kv[4];
 #pragma unroll
-      for (int h = 0; h < kIdxHeads; ++h) {
-        float s = 0.f;
+    for (int k = 0; k < 4; ++k) kv[k] = row[k * 8 + sub];
+    // per head: even and odd dims accumulate in the two halves of a packed
+    // fp32 FMA, then add
+    float acc[kIdxHeads];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          s = fmaf(qv[h][k].x, kv[u][k].x, s);
-          s = fmaf(qv[h][k].y, kv[u][k].y, s);
-          s = fmaf(qv[h][k].z, kv[u][k].z, s);
-          s = fmaf(qv[h][k].w, kv[u][k].w, s);
-        }
-        acc[h] = s;
+    for (int h = 0; h < kIdxHeads; ++h) {
+      float2 e = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        e = ffma2(make_float2(qv[h][k].x, qv[h][k].y), make_float2(kv[k].x, kv[k].y), e);
+        e = ffma2(make_float2(qv[h][k].z, qv[h][k].w), make_float2(kv[k].z, kv[k].w), e);
       }
-      // reduce-scatter over the 8 lanes of the group
-      float k0 = bit2 ? acc[2] : acc[0], k1 = bit2 ? acc[3] : acc[1];
-      const float s0 = bit2 ? acc[0] : acc[2], s1 = bit2 ? acc[1] : acc[3];
-      k0 += __shfl_xor_sync(kFull, s0, 4);
-      k1 += __shfl_xor_sync(kFull, s1, 4);
-      float d = bit1 ? k1 : k0;
-      d += __shfl_xor_sync(kFull, bit1 ? k0 : k1, 2);
-      d += __shfl_xor_sync(kFull, d, 1);               // head 2*bit2 + bit1, all 128 dims
-      float v = wh * fmaxf(d, 0.f);
-      v += __shfl_xor_sync(kFull, v, 2);
-      v += __shfl_xor_sync(kFull, v, 4);               // sum over the 4 heads
-      if (live[u] && sub == 0) {
-        const float sc = ok[u] ? v : -INFINITY;
-        const int64_t j = base + u * 4 + grp;
-        srow[j] = sc;
-        if (kTopk) {
-          const unsigned bin = score_key(sc) >> (32 - kHistBits);
-          if (atomicAdd(&s_hist[bin], 1u) == 0u) s_touched[atomicAdd(&s_ntouched, 1u)] = (unsigned short)bin;
-        }
+      acc[h] = e.x + e.y;
+    }
+    // reduce-scatter over the 8 lanes of the group
+    float k0 = bit2 ? acc[2] : acc[0], k1 = bit2 ? acc[3] : acc[1];
+    const float s0 = bit2 ? acc[0] : acc[2], s1 = bit2 ? acc[1] : acc[3];
+    k0 += __shfl_xor_sync(kFull, s0, 4);
+    k1 += __shfl_xor_sync(kFull, s1, 4);
+    float d = bit1 ? k1 : k0;
+    d += __shfl_xor_sync(kFull, bit1 ? k0 : k1, 2);
+    d += __shfl_xor_sync(kFull, d, 1);               // head 2*bit2 + bit1, all 128 dims
+    float v = wh * fmaxf(d, 0.f);
+    v += __shfl_xor_sync(kFull, v, 2);
+    v += __shfl_xor_sync(kFull, v, 4);               // sum over the 4 heads
+    if (live && sub == 0) {
+      const float sc = ok ? v : -INFINITY;
+      srow[j0 + i] = sc;
+      if (kTopk) {
+        const unsigned bin = score_key(sc) >> (32 - kHistBits);
+        if (atomicAdd(&s_hist[bin], 1u) == 0u) s_touched[atomicAdd(&s_ntouched, 1u)] = (unsigned short)bin;
       }
     }
+    __syncwarp();   // every lane is done with this stage before it is refilled
   }
+  asm volatile("cp.async.wait_group 0;\n" ::: "memory");
   if (kTopk) {
     QSA_TS(index, 3);
     __syncthreads();
@@ -825,13 +867,37 @@ k_select(const IndexArgs a, void* ws, const float* __restrict__ scores,
   QSA_TS(index, 18);
 }
 
-int score_chunk(int T, int64_t max_blocks) {
-  // Aim for ~4 CTAs per SM of a 152-SM part across all tokens.
-  const int64_t target = 608;
-  int64_t iters = ceil_div(max_blocks * (int64_t)T, target * kRowsPerIter);
-  if (iters < 1) iters = 1;
-  if (iters > 64) iters = 64;
-  return (int)(iters * kRowsPerIter);
+// Rows per score CTA: every token's rows in one wave of 2 CTAs per SM, in
+// whole warp stages (8 warps x 4 rows), at most kScoreChunkMax.
+int score_chunk(int T, int64_t max_blocks, int sms) {
+  const int64_t per = ceil_div(max_blocks * (int64_t)T, 2 * (int64_t)sms);
+  int64_t chunk = round_up(per < 32 ? 32 : per, 32);
+  if (chunk > kScoreChunkMax) chunk = kScoreChunkMax;
+  return (int)chunk;
+}
+
+// Per-device set-up of the index kernels: SM count, shared-memory limits.
+cudaError_t index_setup(int* sms) {
+  static int sm_count[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (sm_count[dev] == 0) {
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_score<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScoreSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_score<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScoreSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_select, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(sizeof(int32_t) * (kSelSlots + kSelList)));
+    if (e != cudaSuccess) return e;
+    sm_count[dev] = n;
+  }
+  *sms = sm_count[dev];
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -850,32 +916,29 @@ void index_workspace_zero_range(int n_tokens, int64_t, size_t* offset, size_t* b
 
 cudaError_t launch_index_scores(const IndexArgs& a, float* scores, unsigned* err, cudaStream_t stream) {
   if (a.n_tokens <= 0 || a.max_blocks <= 0) return cudaSuccess;
-  const int chunk = score_chunk(a.n_tokens, a.max_blocks);
+  int sms = 0;
+  cudaError_t e = index_setup(&sms);
+  if (e != cudaSuccess) return e;
+  const int chunk = score_chunk(a.n_tokens, a.max_blocks, sms);
   const dim3 grid((unsigned)ceil_div(a.max_blocks, chunk), (unsigned)a.n_tokens);
-  return launch_pdl(k_score<false>, grid, dim3(kScoreThreads), 0, stream, 1, a, (void*)nullptr, scores, chunk,
-                    err);
+  return launch_pdl(k_score<false>, grid, dim3(kScoreThreads), kScoreSmem, stream, 1, a, (void*)nullptr, scores,
+                    chunk, err);
 }
 
 cudaError_t launch_index_topk(const IndexArgs& a, int32_t* cells, int32_t* count,
                               void* ws, unsigned* err, cudaStream_t stream) {
   if (a.n_tokens <= 0) return cudaSuccess;
-  static bool configured[64];
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  int sms = 0;
+  cudaError_t e = index_setup(&sms);
   if (e != cudaSuccess) return e;
   const size_t slot_bytes = sizeof(int32_t) * (kSelSlots + kSelList);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
-    e = cudaFuncSetAttribute(k_select, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)slot_bytes);
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
   IndexArgs b = a;
   b.max_blocks = a.max_blocks > 0 ? a.max_blocks : 1;
   float* sc = scores_of(ws, a.max_tokens);
-  const int chunk = score_chunk(a.n_tokens, b.max_blocks);
+  const int chunk = score_chunk(a.n_tokens, b.max_blocks, sms);
   const dim3 g1((unsigned)ceil_div(b.max_blocks, chunk), (unsigned)a.n_tokens);
   prof_before(kKScore, stream);
-  e = launch_pdl(k_score<true>, g1, dim3(kScoreThreads), 0, stream, 1, b, ws, sc, chunk, err);
+  e = launch_pdl(k_score<true>, g1, dim3(kScoreThreads), kScoreSmem, stream, 1, b, ws, sc, chunk, err);
   prof_after(kKScore, stream);
   if (e != cudaSuccess) return e;
   prof_before(kKFinal, stream);
