@@ -65,7 +65,8 @@ constexpr uint32_t kOffXS = kOffXV + kOvf * 512;    // fp32 [kOvf][8] scores / p
 constexpr uint32_t kOffXO = kOffXS + kOvf * 8 * 4;  // fp32 [8][256] partial output
 constexpr uint32_t kOffXM = kOffXO + 8 * 256 * 4;   // fp32 [8] max, [8] sum
 constexpr uint32_t kOffXC = kOffXM + 64;            // int [kOvf] cells
-constexpr uint32_t kSmemBytes = kOffXC + kOvf * 4 + 1024;   // + alignment slack
+constexpr uint32_t kOffW = kOffXC + kOvf * 4;        // fp32 [16][8] combine weights, [8] denominators
+constexpr uint32_t kSmemBytes = kOffW + (kMaxCluster * 8 + 8) * 4 + 1024;   // + alignment slack
 
 // Byte offset of 16-byte chunk `c16` (0..31 along a 512-byte row) of row `row`
 // in a tile of `rows` rows stored as 128-byte swizzled atoms: atom column
@@ -174,6 +175,8 @@ k_attn_tc(const AttnArgs a, unsigned* err) {
   const int g = blockIdx.y, t = blockIdx.z;
   const uint32_t rank = cluster_rank(), NC = cluster_size();
   const int G = a.n_kv_heads, Hq = G * kGqa;
+  // scores live in the log2 domain: s * attn_scale * log2(e), exponentials by exp2f
+  const float scale2 = a.attn_scale * 1.4426950408889634f;
 
   QSA_TS(attn, 0);
   // ---- prologue (inputs not produced by the preceding index kernels)
@@ -333,7 +336,7 @@ k_attn_tc(const AttnArgs a, unsigned* err) {
       const bool valid = cell < nv && scell[cell] >= 0;
 #pragma unroll
       for (int h = 0; h < kGqa; ++h) {
-        sv[h] = valid ? sv[h] * a.attn_scale : -INFINITY;
+        sv[h] = valid ? sv[h] * scale2 : -INFINITY;
         float m = sv[h];
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
@@ -343,7 +346,7 @@ k_attn_tc(const AttnArgs a, unsigned* err) {
 #pragma unroll
       for (int h = 0; h < kGqa; ++h) {
         tmax[h] = fmaxf(fmaxf(sred[h], sred[8 + h]), fmaxf(sred[16 + h], sred[24 + h]));
-        const float p = (tmax[h] == -INFINITY) ? 0.f : expf(sv[h] - tmax[h]);
+        const float p = (tmax[h] == -INFINITY) ? 0.f : exp2f(sv[h] - tmax[h]);
         const __half ph = __float2half_rn(p);
         // the sum uses the rounded p the MMA sees
         float e = __half2float(ph);
@@ -389,8 +392,8 @@ k_attn_tc(const AttnArgs a, unsigned* err) {
 #pragma unroll
       for (int h = 0; h < kGqa; ++h) {
         const float mn = fmaxf(run_m[h], tmax[h]);
-        const float fa = (run_m[h] == -INFINITY) ? 0.f : expf(run_m[h] - mn);
-        const float fb = (tmax[h] == -INFINITY) ? 0.f : expf(tmax[h] - mn);
+        const float fa = (run_m[h] == -INFINITY) ? 0.f : exp2f(run_m[h] - mn);
+        const float fb = (tmax[h] == -INFINITY) ? 0.f : exp2f(tmax[h] - mn);
         acc[0][h] = acc[0][h] * fa + o0[h] * fb;
         acc[1][h] = acc[1][h] * fa + o1[h] * fb;
         run_l[h] = run_l[h] * fa + tsum[h] * fb;
@@ -472,8 +475,8 @@ k_attn_tc(const AttnArgs a, unsigned* err) {
           }
         }
         const bool ok = c < ovf_n && xc[c] >= 0;
-        xs[c * 8 + h0] = ok ? d0 * a.attn_scale : -INFINITY;
-        xs[c * 8 + h0 + 1] = ok ? d1 * a.attn_scale : -INFINITY;
+        xs[c * 8 + h0] = ok ? d0 * scale2 : -INFINITY;
+        xs[c * 8 + h0 + 1] = ok ? d1 * scale2 : -INFINITY;
       }
       bar_half(2);
       // softmax per head: 16 lanes per head, cells l and l+16
@@ -483,8 +486,8 @@ k_attn_tc(const AttnArgs a, unsigned* err) {
         float m = fmaxf(s0v, s1v);
 #pragma unroll
         for (int o = 8; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
-        const float p0 = (m == -INFINITY) ? 0.f : expf(s0v - m);
-        const float p1 = (m == -INFINITY) ? 0.f : expf(s1v - m);
+        const float p0 = (m == -INFINITY) ? 0.f : exp2f(s0v - m);
+        const float p1 = (m == -INFINITY) ? 0.f : exp2f(s1v - m);
         float sum = p0 + p1;
 #pragma unroll
         for (int o = 8; o >= 1; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
@@ -531,8 +534,8 @@ k_attn_tc(const AttnArgs a, unsigned* err) {
     for (int h = 0; h < kGqa; ++h) {
       const float mx = xm[h];
       const float mn = fmaxf(run_m[h], mx);
-      const float fa = (run_m[h] == -INFINITY) ? 0.f : expf(run_m[h] - mn);
-      const float fb = (mx == -INFINITY) ? 0.f : expf(mx - mn);
+      const float fa = (run_m[h] == -INFINITY) ? 0.f : exp2f(run_m[h] - mn);
+      const float fb = (mx == -INFINITY) ? 0.f : exp2f(mx - mn);
       acc[0][h] = acc[0][h] * fa + xo[h * kHeadDim + 32 * warp + lane] * fb;
       acc[1][h] = acc[1][h] * fa + xo[h * kHeadDim + 128 + 32 * warp + lane] * fb;
       run_l[h] = run_l[h] * fa + xm[8 + h] * fb;
@@ -565,21 +568,30 @@ k_attn_tc(const AttnArgs a, unsigned* err) {
   cluster_sync();   // all pushes have landed; nobody touches a peer after this
   QSA_TS(attn, 26);
   {
+    // per (partial, head) weight exp2(m_p - max_p m_p) once, then the
+    // denominators, then every output dim is a weighted sum of the partials
+    float* sw = reinterpret_cast<float*>(base + kOffW);           // [NC][8] weights, then [8] denominators
+    if (tid < (int)NC * kGqa) {
+      const int p = tid / kGqa, h = tid - p * kGqa;
+      float mx = -INFINITY;
+      for (int q = 0; q < (int)NC; ++q) mx = fmaxf(mx, sml[q * 16 + h]);
+      const float mp = sml[p * 16 + h];
+      sw[tid] = (mp == -INFINITY || mx == -INFINITY) ? 0.f : exp2f(mp - mx);
+    }
+    __syncthreads();
+    if (tid < kGqa) {
+      float den = 0.f;
+      for (int p = 0; p < (int)NC; ++p) den = fmaf(sw[p * kGqa + tid], sml[p * 16 + 8 + tid], den);
+      sw[kMaxCluster * kGqa + tid] = den;
+    }
+    __syncthreads();
     const int d0 = (int)rank * dpc;
     for (int i = tid; i < kGqa * dpc; i += kThreads) {
       const int h = i / dpc, e = i % dpc, d = d0 + e;
       if (d >= kHeadDim) continue;
-      float mx = -INFINITY;
-      for (int p = 0; p < (int)NC; ++p) mx = fmaxf(mx, sml[p * 16 + h]);
-      float num = 0.f, den = 0.f;
-      if (mx != -INFINITY) {
-        for (int p = 0; p < (int)NC; ++p) {
-          const float mp = sml[p * 16 + h];
-          const float w = (mp == -INFINITY) ? 0.f : expf(mp - mx);
-          den = fmaf(w, sml[p * 16 + 8 + h], den);
-          num = fmaf(w, so[(p * kGqa + h) * dpc + e], num);
-        }
-      }
+      float num = 0.f;
+      for (int p = 0; p < (int)NC; ++p) num = fmaf(sw[p * kGqa + h], so[(p * kGqa + h) * dpc + e], num);
+      const float den = sw[kMaxCluster * kGqa + h];
       a.out[((int64_t)t * Hq + g * kGqa + h) * kHeadDim + d] = den > 0.f ? num / den : 0.f;
     }
   }
