@@ -4,9 +4,11 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config 50k] [--impl native|reference]
 
 A step is one decode step of one QSA layer over all sequences of the
-workload: qsa_pool_update (dirty block) -> qsa_index_topk (score, select,
-expand) -> qsa_sparse_attn (split-KV attention + combine), through the C ABI
-on one stream.  Inputs are resident in HBM when the timed region starts; L2
+workload, through the C ABI on one stream: qsa_kv_append (the step's new
+cells, the device dirty list and the re-pooling of the dirtied blocks) ->
+qsa_index_topk (score, select, expand) -> qsa_sparse_attn (attention with its
+split merge).  --path calls times qsa_pool_update -> qsa_index_topk ->
+qsa_sparse_attn with the table appended outside the timed region instead.  Inputs are resident in HBM when the timed region starts; L2
 is flushed (a 1 GiB write) before every step, outside the per-step events.
 Prints one JSON line (rank 0).
 
@@ -288,10 +290,11 @@ def measure_config(name, K, W, dev, *, path="full", e2e=True, clocks=None):
     """Time K decode steps of workload `name` on the device.  The K timed
     steps are captured as ONE CUDA graph: per step an L2 flush (outside the
     step's events), a start event node, the step, an end event node.  Path
-    "full" (the layer's whole step): qsa_kv_append (the step's new cells and
-    the device dirty list), qsa_pool_update, qsa_index_topk, qsa_sparse_attn.
-    Path "calls": the last three only, the block table appended by a torch
-    index write outside the step's events and the dirty list from the host.
+    "full" (the layer's whole step): qsa_kv_append (the step's new cells, the
+    device dirty list and, in the same launch, the re-pooling of the dirtied
+    blocks), qsa_index_topk, qsa_sparse_attn.  Path "calls": qsa_pool_update,
+    qsa_index_topk, qsa_sparse_attn, the block table appended by a torch index
+    write outside the step's events and the dirty list from the host.
     The graph is replayed once; the step time is end - start of each step."""
     import torch
     from qsa_workload import make_workload
@@ -314,9 +317,12 @@ def measure_config(name, K, W, dev, *, path="full", e2e=True, clocks=None):
     flush = torch.empty(FLUSH_BYTES[0] // 4, dtype=torch.float32, device=dev)
     toks = [len(st.tok_pos) for st in wl.steps]
     alg = [algorithmic_bytes(wl, i) for i in range(n_steps)]
-    kernels = ["append", "pool", "score", "select", "attn"] if full else ["pool", "score", "select", "attn"]
-    if not full:
-        for a in alg:
+    # path "full": the append kernel also re-pools the blocks it dirties
+    kernels = ["append", "score", "select", "attn"] if full else ["pool", "score", "select", "attn"]
+    for a in alg:
+        if full:
+            a["append"] += a.pop("pool")
+        else:
             a.pop("append")
     step_fn = L.full_step if full else L.step
     xev = _ExternalEvents()
@@ -517,7 +523,8 @@ def run_native(args, rank, world, local):
                    "tokens_per_step": len(wl.steps[0].tok_pos),
                    "path": args.path,
                    "launch": ("the K timed steps captured as one CUDA graph (per step: L2 flush, start event, "
-                              + ("qsa_kv_append + qsa_pool_update + qsa_index_topk + qsa_sparse_attn = 5 kernels"
+                              + ("qsa_kv_append (re-pooling the blocks it dirties) + qsa_index_topk + "
+                                 "qsa_sparse_attn = 4 kernels"
                                  if args.path == "full" else
                                  "table append outside the events, qsa_pool_update + qsa_index_topk + "
                                  "qsa_sparse_attn = 4 kernels")
@@ -557,7 +564,7 @@ def main():
     ap.add_argument("--secondary", default="250k_q8,5x250k_q8",
                     help="comma list of further workloads timed on rank 0 ('none': no others)")
     ap.add_argument("--path", default="full", choices=["full", "calls"],
-                    help="full: append + pool + index + attention (the layer's whole step); "
+                    help="full: append (with the pool update) + index + attention (the layer's whole step); "
                          "calls: the last three, the table appended outside the timed region")
     ap.add_argument("--no-compare", dest="compare", action="store_false",
                     help="do not also time the other path")

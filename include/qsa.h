@@ -114,6 +114,11 @@ int32_t qsa_cells_per_token(const qsa_config* cfg);
  *            -1 to n_dirty entries (a qsa_pool_update dirty list).
  * The block list of each sequence must already hold the slot of every block
  * a new position falls in.  Tokens must occupy distinct cells and positions.
+ * pooled (optional, NULL to skip): when given, the dirtied blocks are also
+ * re-pooled in the same launch, exactly as a qsa_pool_update(dirty) issued
+ * after this call would (bit-identical rows); slot_block_idx and norm_w are
+ * then required (as qsa_pool_update takes them) and the dirty list can still
+ * be passed to qsa_index_topk as its scheduling hint.
  * Limits: n_new <= 1024 (QSA_ERR_UNSUPPORTED beyond); n_dirty >= n_new
  * (QSA_ERR_SHAPE otherwise: room for every token in a block of its own).
  * All buffers 16-byte aligned except the int32 arrays.  A token with an
@@ -125,7 +130,9 @@ qsa_status qsa_kv_append(const qsa_config* cfg, int32_t n_new,
                          void* k_cache, void* v_cache, void* idx_k, int64_t n_cells,
                          int32_t* blk_cells, int64_t n_slots,
                          const int64_t* seq_blk_off, const int32_t* seq_blk_slots, int32_t n_seq,
-                         int32_t* dirty, int32_t n_dirty, qsa_stream_t stream);
+                         int32_t* dirty, int32_t n_dirty,
+                         const int32_t* slot_block_idx, const float* norm_w, float* pooled,
+                         qsa_stream_t stream);
 /* ---------------------------------------------------------------------------
  * S1  qsa_pool_update  (issue #28734, fix summary, lever2 and lever2b)
  * For each dirty slot s (entries < 0 are skipped; the caller pads the list to

@@ -218,7 +218,8 @@ qsa_status qsa_kv_append(const qsa_config* cfg, int32_t n_new, const int32_t* to
                          const int32_t* cells, const void* k_new, const void* v_new, const void* idx_new,
                          void* k_cache, void* v_cache, void* idx_k, int64_t n_cells, int32_t* blk_cells,
                          int64_t n_slots, const int64_t* seq_blk_off, const int32_t* seq_blk_slots,
-                         int32_t n_seq, int32_t* dirty, int32_t n_dirty, qsa_stream_t stream) {
+                         int32_t n_seq, int32_t* dirty, int32_t n_dirty, const int32_t* slot_block_idx,
+                         const float* norm_w, float* pooled, qsa_stream_t stream) {
   qsa_status st = check_cfg(cfg);
   if (st != QSA_OK) return st;
   if (n_new < 0 || n_cells < 0 || n_slots < 0 || n_seq < 0 || n_dirty < 0) return QSA_ERR_INVALID_ARG;
@@ -231,12 +232,15 @@ qsa_status qsa_kv_append(const qsa_config* cfg, int32_t n_new, const int32_t* to
   if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(idx_new, 16) || !aligned(k_cache, 16) ||
       !aligned(v_cache, 16) || !aligned(idx_k, 16) || !aligned(seq_blk_off, 8))
     return QSA_ERR_INVALID_ARG;
+  if (pooled != nullptr && (!slot_block_idx || !norm_w || !aligned(norm_w, 8) || !aligned(pooled, 8)))
+    return QSA_ERR_INVALID_ARG;
   unsigned* err = error_word();
   if (err == nullptr) return QSA_ERR_CUDA;
   return from_cuda(launch_append(*cfg, n_new, tok_seq, tok_pos, cells, static_cast<const __half*>(k_new),
                                  static_cast<const __half*>(v_new), static_cast<const __half*>(idx_new), k_cache,
                                  v_cache, static_cast<__half*>(idx_k), n_cells, blk_cells, n_slots, seq_blk_off,
-                                 seq_blk_slots, n_seq, dirty, n_dirty, err, reinterpret_cast<cudaStream_t>(stream)));
+                                 seq_blk_slots, n_seq, dirty, n_dirty, slot_block_idx, norm_w, pooled, err,
+                                 reinterpret_cast<cudaStream_t>(stream)));
 }
 
 qsa_status qsa_blocks_dirty(const int32_t* old_tbl, const int32_t* new_tbl, int64_t n_slots,

@@ -16,7 +16,7 @@
 // builds the dirty list: the distinct slots, ascending, padded with -1.
 // Everything is read and encoded before the grid-dependency wait (the new
 // rows are inputs, not outputs of the preceding kernel); only the stores wait.
-#include "qsa_internal.cuh"
+#include "pool_row.cuh"
 
 namespace qsa {
 namespace {
@@ -47,6 +47,11 @@ struct AppendArgs {
   int n_seq;
   int32_t* dirty;
   int n_dirty;
+  // re-pooling of the dirtied blocks in the same launch (pooled == nullptr: off)
+  const int32_t* slot_block_idx;
+  const float* norm_w;
+  float* pooled;
+  float eps;
 };
 
 // Slot of the block holding token t's position, or -1 when any index is out
@@ -77,15 +82,18 @@ __device__ __forceinline__ int token_slot(const AppendArgs& a, int t, int* in_bl
 }
 
 __global__ void __launch_bounds__(kAppThreads)
-k_append(const AppendArgs a, unsigned* err) {
+k_append(const AppendArgs a, const Turns turns, unsigned* err) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (blockIdx.x == gridDim.x - 1) {
     // ---- the dirty list (n_new <= kAppendMaxTokens, 4 tokens per thread)
     __shared__ int s_slot[kAppendMaxTokens];
+    __shared__ unsigned char s_ib[kAppendMaxTokens];
+    __shared__ int s_dslot[kAppendMaxTokens];
     __shared__ unsigned s_warp[kAppWarps];
     for (int t = tid; t < a.n_new; t += kAppThreads) {
       int ib = 0;
       s_slot[t] = token_slot(a, t, &ib, err, false);
+      s_ib[t] = (unsigned char)ib;
     }
     __syncthreads();
     // token t leads its slot if no earlier token has it; leaders are ranked
@@ -125,8 +133,56 @@ k_append(const AppendArgs a, unsigned* err) {
     grid_dep_launch();
 #pragma unroll
     for (int k = 0; k < kAppendMaxTokens / kAppThreads; ++k)
-      if (rank[k] >= 0 && rank[k] < a.n_dirty) a.dirty[rank[k]] = lead_slot[k];
+      if (rank[k] >= 0 && rank[k] < a.n_dirty) {
+        a.dirty[rank[k]] = lead_slot[k];
+        s_dslot[rank[k]] = lead_slot[k];
+      }
     for (int i = (int)n_lead + tid; i < a.n_dirty; i += kAppThreads) a.dirty[i] = -1;
+    if (a.pooled == nullptr) return;
+    __syncthreads();
+    // ---- re-pool the dirtied blocks, one warp per block (as qsa_pool_update
+    // would after this launch): members from the table, except the positions
+    // this launch appends, whose cells and keys come from the inputs (other
+    // warps of this launch are writing them)
+    const int nl = min((int)n_lead, a.n_dirty);
+    for (int e = warp; e < nl; e += kAppWarps) {
+      const int slot = s_dslot[e];
+      int m = -1, tn = -1;
+      if (lane < a.r) {
+        m = a.blk_cells[(int64_t)slot * a.r + lane];
+        for (int t = 0; t < a.n_new; ++t)
+          if (s_slot[t] == slot && s_ib[t] == lane) {
+            m = a.cell[t];
+            tn = t;
+          }
+      }
+      int cell[kMaxR], tnew[kMaxR];
+#pragma unroll
+      for (int i = 0; i < kMaxR; ++i) {
+        cell[i] = __shfl_sync(kFull, m, i);
+        tnew[i] = __shfl_sync(kFull, tn, i);
+        if (i >= a.r) cell[i] = -1;
+      }
+      const int blk = a.slot_block_idx[slot];
+      float2 lo[kMaxR], hi[kMaxR];
+      bool present[kMaxR];
+#pragma unroll
+      for (int i = 0; i < kMaxR; ++i) {
+        const bool ok = cell[i] >= 0 && cell[i] < a.n_cells;
+        if (cell[i] >= a.n_cells && lane == 0) atomicOr(err, kErrCell);
+        const __half* src = tnew[i] >= 0 ? a.idx_new + (int64_t)tnew[i] * kIdxDim
+                                         : a.idx_k + (int64_t)(ok ? cell[i] : 0) * kIdxDim;
+        const __half2* row = reinterpret_cast<const __half2*>(src);
+        lo[i] = ok ? __half22float2(row[lane]) : make_float2(0.f, 0.f);
+        hi[i] = ok ? __half22float2(row[32 + lane]) : make_float2(0.f, 0.f);
+        present[i] = ok;
+      }
+      float2 olo, ohi;
+      pool_rows_warp(lo, hi, present, blk, a.r, a.norm_w, turns, a.eps, &olo, &ohi);
+      float* out = a.pooled + (int64_t)slot * kIdxDim;
+      reinterpret_cast<float2*>(out)[lane] = olo;
+      reinterpret_cast<float2*>(out)[32 + lane] = ohi;
+    }
     return;
   }
 
@@ -204,7 +260,8 @@ cudaError_t launch_append(const qsa_config& cfg, int n_new, const int32_t* tok_s
                           const int32_t* cell, const __half* k_new, const __half* v_new, const __half* idx_new,
                           void* k_cache, void* v_cache, __half* idx_k, int64_t n_cells, int32_t* blk_cells,
                           int64_t n_slots, const int64_t* seq_blk_off, const int32_t* seq_blk_slots, int n_seq,
-                          int32_t* dirty, int n_dirty, unsigned* err, cudaStream_t stream) {
+                          int32_t* dirty, int n_dirty, const int32_t* slot_block_idx, const float* norm_w,
+                          float* pooled, unsigned* err, cudaStream_t stream) {
   if (n_new <= 0) return cudaSuccess;
   AppendArgs a{};
   a.n_new = n_new;
@@ -228,10 +285,15 @@ cudaError_t launch_append(const qsa_config& cfg, int n_new, const int32_t* tok_s
   a.n_seq = n_seq;
   a.dirty = dirty;
   a.n_dirty = n_dirty;
+  a.slot_block_idx = slot_block_idx;
+  a.norm_w = norm_w;
+  a.pooled = pooled;
+  a.eps = cfg.rms_eps;
+  const Turns turns = make_turns(cfg.rope_theta);
   const int64_t warps = (int64_t)n_new * (2 * cfg.n_kv_heads + 1);
   const unsigned blocks = (unsigned)ceil_div(warps, kAppWarps) + 1;   // + the dirty-list CTA
   prof_before(kKAppend, stream);
-  cudaError_t e = launch_pdl(k_append, dim3(blocks), dim3(kAppThreads), 0, stream, 1, a, err);
+  cudaError_t e = launch_pdl(k_append, dim3(blocks), dim3(kAppThreads), 0, stream, 1, a, turns, err);
   prof_after(kKAppend, stream);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

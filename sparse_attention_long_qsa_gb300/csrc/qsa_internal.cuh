@@ -250,6 +250,7 @@ cudaError_t launch_append(const qsa_config& cfg, int n_new, const int32_t* tok_s
                           const int32_t* cell, const __half* k_new, const __half* v_new, const __half* idx_new,
                           void* k_cache, void* v_cache, __half* idx_k, int64_t n_cells, int32_t* blk_cells,
                           int64_t n_slots, const int64_t* seq_blk_off, const int32_t* seq_blk_slots, int n_seq,
-                          int32_t* dirty, int n_dirty, unsigned* err, cudaStream_t stream);
+                          int32_t* dirty, int n_dirty, const int32_t* slot_block_idx, const float* norm_w,
+                          float* pooled, unsigned* err, cudaStream_t stream);
 
 }  // namespace qsa

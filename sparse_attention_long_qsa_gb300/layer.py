@@ -5,7 +5,8 @@ the pooled block-key cache, workspaces, outputs) as torch CUDA tensors and
 runs a step as the C-ABI calls on one stream:
 
     step:       pool_update(dirty) -> index_topk(tokens) -> sparse_attn(tokens)
-    full_step:  kv_append(new cells) -> the same three, fed the device dirty list
+    full_step:  kv_append(new cells, re-pooling the blocks they dirty) ->
+                index_topk(tokens) -> sparse_attn(tokens)
 
 It holds no arithmetic of its own.
 """
@@ -94,8 +95,9 @@ class QSALayer:
         self.sparse_attn(q, int(tok_pos.numel()), stream)
         return self.out[:int(tok_pos.numel())]
 
-    def kv_append(self, tok_seq, tok_pos, cells, k_new, v_new, idx_new, stream=None):
-        """Write the step's new cells and build the dirty list on the device;
+    def kv_append(self, tok_seq, tok_pos, cells, k_new, v_new, idx_new, stream=None, pool=False):
+        """Write the step's new cells and build the dirty list on the device
+        (with pool=True also re-pool the dirtied blocks in the same launch);
         returns the dirty-list view (padded to a power of two >= max(4, T))."""
         T = int(tok_pos.numel())
         nd = 4
@@ -104,16 +106,17 @@ class QSALayer:
         if self._dirty is None or self._dirty.numel() < nd:
             self._dirty = torch.full((max(nd, 4),), -1, dtype=torch.int32, device=self.device)
         d = self._dirty[:nd]
+        extra = dict(slot_block_idx=self.slot_block_idx, norm_w=self.norm_w, pooled=self.pooled) if pool else {}
         qsa.kv_append(self.cfg, tok_seq, tok_pos, cells, k_new, v_new, idx_new, self.k_cache, self.v_cache,
-                      self.idx_k, self.blk_cells, self.seq_blk_off, self.seq_blk_slots, d, stream)
+                      self.idx_k, self.blk_cells, self.seq_blk_off, self.seq_blk_slots, d, stream=stream, **extra)
         return d
 
     def full_step(self, tok_seq, tok_pos, q, q_idx, w_idx, cells, k_new, v_new, idx_new, stream=None, **_):
         """The whole layer step from the new tokens on: append of their cells
-        (K/V, indexer keys, table, device dirty list), pool update, index
-        top-k, sparse attention.  Returns the out[:T] view (fp32)."""
-        d = self.kv_append(tok_seq, tok_pos, cells, k_new, v_new, idx_new, stream)
-        self.pool_update(d, stream)
+        (K/V, indexer keys, table, device dirty list) with the pool update of
+        the blocks they dirty in the same launch, index top-k, sparse
+        attention.  Returns the out[:T] view (fp32)."""
+        d = self.kv_append(tok_seq, tok_pos, cells, k_new, v_new, idx_new, stream, pool=True)
         self.index_topk(tok_seq, tok_pos, q_idx, w_idx, recomputed=d, stream=stream)
         self.sparse_attn(q, int(tok_pos.numel()), stream)
         return self.out[:int(tok_pos.numel())]

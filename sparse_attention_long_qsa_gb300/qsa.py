@@ -86,7 +86,7 @@ def lib():
     L.qsa_sparse_attn.argtypes = [CP, _I32, _P, _P, _P, _I64, _P, _P, _P, _P, _SZ, _P]
     L.qsa_sparse_attn.restype = _I32
     L.qsa_kv_append.argtypes = [CP, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _P, _I64, _P, _P, _I32,
-                                _P, _I32, _P]
+                                _P, _I32, _P, _P, _P, _P]
     L.qsa_kv_append.restype = _I32
     L.qsa_blocks_dirty.argtypes = [_P, _P, _I64, _I32, _P, _I32, ctypes.POINTER(_I32), _I32]
     L.qsa_blocks_dirty.restype = _I32
@@ -228,10 +228,15 @@ def sparse_attn(cfg, q, k_cache, v_cache, n_cells: int, cells, count, out, works
 
 
 def kv_append(cfg, tok_seq, tok_pos, cells, k_new, v_new, idx_new, k_cache, v_cache, idx_k, blk_cells,
-              seq_blk_off, seq_blk_slots, dirty, stream=None):
+              seq_blk_off, seq_blk_slots, dirty, slot_block_idx=None, norm_w=None, pooled=None, stream=None):
     """Write the step's new cells (K/V rows, indexer keys, block-table
-    entries) and fill `dirty` with the slots of the blocks they change."""
+    entries) and fill `dirty` with the slots of the blocks they change; with
+    `pooled` (and slot_block_idx, norm_w) also re-pool those blocks."""
     import torch
+    pool_args = (None, None, None)
+    if pooled is not None:
+        pool_args = (_ptr(slot_block_idx, torch.int32, "slot_block_idx"), _ptr(norm_w, torch.float32, "norm_w"),
+                     _ptr(pooled, torch.float32, "pooled"))
     n_cells = int(idx_k.shape[0])
     st = lib().qsa_kv_append(
         ctypes.byref(cfg), int(tok_pos.numel()), _ptr(tok_seq, torch.int32, "tok_seq"),
@@ -241,7 +246,7 @@ def kv_append(cfg, tok_seq, tok_pos, cells, k_new, v_new, idx_new, k_cache, v_ca
         _ptr(idx_k, torch.float16, "idx_k"), n_cells, _ptr(blk_cells, torch.int32, "blk_cells"),
         int(blk_cells.shape[0]), _ptr(seq_blk_off, torch.int64, "seq_blk_off"),
         _ptr(seq_blk_slots, torch.int32, "seq_blk_slots"), int(seq_blk_off.numel()) - 1,
-        _ptr(dirty, torch.int32, "dirty"), int(dirty.numel()), _stream(stream))
+        _ptr(dirty, torch.int32, "dirty"), int(dirty.numel()), *pool_args, _stream(stream))
     _check(st, "qsa_kv_append")
 
 

@@ -125,7 +125,7 @@ def test_binding_refuses_cpu_tensors(L):
 def test_kv_append_host_checks(L):
     c = qsa.config()
     f = 0x10000
-    base = [ctypes.byref(c), 4, f, f, f, f, f, f, f, f, f, 1000, f, 100, f, f, 1, f, 4, None]
+    base = [ctypes.byref(c), 4, f, f, f, f, f, f, f, f, f, 1000, f, 100, f, f, 1, f, 4, None, None, None, None]
     def call(**kw):
         args = list(base)
         for i, v in kw.items():
@@ -138,4 +138,5 @@ def test_kv_append_host_checks(L):
     assert call(a5=f + 8) == -1                 # new K rows must be 16-byte aligned
     assert call(a10=f + 2) == -1                # indexer keys must be 16-byte aligned
     assert call(a16=0) == -1                    # no sequence
+    assert call(a21=f) == -1                    # re-pooling needs slot_block_idx and norm_w
     assert L.qsa_kv_append(ctypes.byref(qsa.config(kv_type=7)), *base[1:]) == -1

@@ -48,12 +48,21 @@ def _poison_new_cells(wl, L):
 def test_append_matches_oracle_bit_for_bit(kw):
     wl = make_workload(seed=41, **kw)
     L = QSALayer.from_workload(wl, 0)
+    L2 = QSALayer.from_workload(wl, 0)
     kc, vc, ik = _poison_new_cells(wl, L)
+    _poison_new_cells(wl, L2)
+    for X in (L, L2):
+        X.warm(torch.from_numpy(wl.prompt_dirty()).cuda())
     tbl = wl.blk_cells_state(0)
     for i, st in enumerate(wl.steps):
         inp = step_inputs(st, new_cells=True)
-        d = L.kv_append(inp["tok_seq"], inp["tok_pos"], inp["cells"], inp["k_new"], inp["v_new"], inp["idx_new"])
+        args = (inp["tok_seq"], inp["tok_pos"], inp["cells"], inp["k_new"], inp["v_new"], inp["idx_new"])
+        # L re-pools the dirtied blocks inside the append; L2 runs the pool update after it
+        d = L.kv_append(*args, pool=True)
+        d2 = L2.kv_append(*args)
+        L2.pool_update(d2)
         torch.cuda.synchronize()
+        assert torch.equal(L.pooled, L2.pooled)
         kc, vc, ik, tbl, dirty = O.kv_append(wl.cfg, st.tok_seq, st.tok_pos, st.cells, st.k_new, st.v_new,
                                              st.idx_new, kc, vc, ik, wl.n_cells, tbl, wl.seq_blk_off,
                                              wl.seq_blk_slots, int(d.numel()))
