@@ -117,8 +117,9 @@ int32_t qsa_cells_per_token(const qsa_config* cfg);
  * pooled (optional, NULL to skip): when given, the dirtied blocks are also
  * re-pooled in the same launch, exactly as a qsa_pool_update(dirty) issued
  * after this call would (bit-identical rows); slot_block_idx and norm_w are
- * then required (as qsa_pool_update takes them) and the dirty list can still
- * be passed to qsa_index_topk as its scheduling hint.
+ * then required (as qsa_pool_update takes them).  (This list is written by
+ * the launch, so it cannot serve as the scheduling hint of a qsa_index_topk
+ * issued right after it.)
  * Limits: n_new <= 1024 (QSA_ERR_UNSUPPORTED beyond); n_dirty >= n_new
  * (QSA_ERR_SHAPE otherwise: room for every token in a block of its own).
  * All buffers 16-byte aligned except the int32 arrays.  A token with an
@@ -197,8 +198,11 @@ qsa_status qsa_index_scores(const qsa_config* cfg, int32_t n_tokens,
  * that update's dirty list (entries < 0 ignored): work on blocks whose slots
  * are not in the list then starts without waiting for the update to finish
  * (lists longer than 32 entries are not used).  The hint must name every slot
- * the preceding update writes, or stale pooled keys may be scored.  Results do
- * not depend on the hint otherwise.  QSA_ERR_INVALID_ARG if n_recomputed < 0,
+ * the preceding update writes, or stale pooled keys may be scored, and it is
+ * read before the preceding call has finished: it must hold its values before
+ * that call is issued (a host-written list, as qsa_pool_update takes; not the
+ * list a qsa_kv_append just wrote).  Results do not depend on the hint
+ * otherwise.  QSA_ERR_INVALID_ARG if n_recomputed < 0,
  * or > 0 with a NULL list. */
 size_t qsa_index_topk_workspace_size(const qsa_config* cfg, int32_t max_tokens,
                                      int64_t max_blocks);

@@ -116,8 +116,10 @@ class QSALayer:
         (K/V, indexer keys, table, device dirty list) with the pool update of
         the blocks they dirty in the same launch, index top-k, sparse
         attention.  Returns the out[:T] view (fp32)."""
-        d = self.kv_append(tok_seq, tok_pos, cells, k_new, v_new, idx_new, stream, pool=True)
-        self.index_topk(tok_seq, tok_pos, q_idx, w_idx, recomputed=d, stream=stream)
+        # no scheduling hint here: the dirty list is written by the append
+        # itself, and index_topk reads a hint before its predecessor finishes
+        self.kv_append(tok_seq, tok_pos, cells, k_new, v_new, idx_new, stream, pool=True)
+        self.index_topk(tok_seq, tok_pos, q_idx, w_idx, stream=stream)
         self.sparse_attn(q, int(tok_pos.numel()), stream)
         return self.out[:int(tok_pos.numel())]
 
