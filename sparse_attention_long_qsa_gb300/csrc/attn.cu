@@ -33,6 +33,8 @@
 // Waits on the MMA completion barrier are bounded: on timeout the CTA records
 // an error bit and keeps going through every barrier (its output is then
 // meaningless but nothing hangs).
+#include <cstring>
+
 #include "qsa_internal.cuh"
 
 QSA_TS_DECLARE(attn)
@@ -146,13 +148,24 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
 // Barrier among the 128 threads of warps 0-3 (id 1) or of warps 4-7 (id 2).
 __device__ __forceinline__ void bar_half(int id) { asm volatile("bar.sync %0, 128;\n" ::"r"(id) : "memory"); }
 
-// 8 int8 values * scale -> 8 fp16 packed in a uint4.
-__device__ __forceinline__ uint4 dq8(uint2 raw, float s) {
-  const int8_t* b = reinterpret_cast<const int8_t*>(&raw);
+// 8 int8 values * scale -> 8 fp16 packed in a uint4, with no int->float
+// conversion (a quarter-rate pipe): byte b + 128 is placed in the low
+// mantissa byte of 1024.0h (exactly 1024 + b + 128), 1152 is subtracted
+// (exact), and the fp16 product with the scale is rounded once, which equals
+// rounding the exact fp32 product d * q to fp16.
+__device__ __forceinline__ uint4 dq8(uint2 raw, __half2 s2) {
+  const uint32_t lo = raw.x ^ 0x80808080u, hi = raw.y ^ 0x80808080u;
+  const __half2 bias = __float2half2_rn(1152.0f);
+  uint32_t w[4] = {__byte_perm(lo, 0x64646464u, 0x5140), __byte_perm(lo, 0x64646464u, 0x5342),
+                   __byte_perm(hi, 0x64646464u, 0x5140), __byte_perm(hi, 0x64646464u, 0x5342)};
   uint4 o;
   __half2* h = reinterpret_cast<__half2*>(&o);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(s * (float)b[2 * i], s * (float)b[2 * i + 1]);
+  for (int i = 0; i < 4; ++i) {
+    __half2 v;
+    memcpy(&v, &w[i], 4);
+    h[i] = __hmul2(__hsub2(v, bias), s2);
+  }
   return o;
 }
 
@@ -299,7 +312,7 @@ k_attn_tc(const AttnArgs a, unsigned* err) {
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         // 16 int8 = dims half*128 + 16j .. +15 -> two 16-byte fp16 chunks
-        const float skf = __half2float(ksh[j >> 1]), svf = __half2float(vsh[j >> 1]);
+        const __half2 skf = __half2half2(ksh[j >> 1]), svf = __half2half2(vsh[j >> 1]);
         const int c16 = half * 16 + 2 * j;
         *reinterpret_cast<uint4*>(base + kOffK + sw128(kTile, row, c16)) = dq8(make_uint2(kr[j].x, kr[j].y), skf);
         *reinterpret_cast<uint4*>(base + kOffK + sw128(kTile, row, c16 + 1)) = dq8(make_uint2(kr[j].z, kr[j].w), skf);
@@ -438,13 +451,13 @@ k_attn_tc(const AttnArgs a, unsigned* err) {
         for (int i = tx; i < kOvf * 16; i += 128) {   // (row, 16-value group)
           const int row = i >> 4, grp = i & 15, c = xc[row];
           uint4 kr = make_uint4(0, 0, 0, 0), vr = make_uint4(0, 0, 0, 0);
-          float sk = 0.f, svv = 0.f;
+          __half2 sk = __float2half2_rn(0.f), svv = __float2half2_rn(0.f);
           if (c >= 0) {
             const int64_t cg = (int64_t)c * G + g;
             kr = __ldg(reinterpret_cast<const uint4*>(kq + cg * kHeadDim + grp * 16));
             vr = __ldg(reinterpret_cast<const uint4*>(vq + cg * kHeadDim + grp * 16));
-            sk = __half2float(kd[cg * 8 + (grp >> 1)]);
-            svv = __half2float(vd[cg * 8 + (grp >> 1)]);
+            sk = __half2half2(kd[cg * 8 + (grp >> 1)]);
+            svv = __half2half2(vd[cg * 8 + (grp >> 1)]);
           }
           uint4* kdst = reinterpret_cast<uint4*>(base + kOffXK + row * 512 + grp * 32);
           uint4* vdst = reinterpret_cast<uint4*>(base + kOffXV + row * 512 + grp * 32);
