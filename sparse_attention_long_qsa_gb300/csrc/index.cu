@@ -282,15 +282,14 @@ k_score(const IndexArgs a, void* ws, float* __restrict__ scores, int chunk, unsi
 #pragma unroll
   for (int st = 0; st < kRingStages - 1; ++st) issue(st);
 
+  // Scores are collected 32 rows at a time (8 stages): lane L keeps the score
+  // of group L % 4 of stage L / 4 of the batch, so the score stores and the
+  // histogram updates run once per 32 rows with every lane busy.
+  float hold = 0.f;
   for (int it = 0; it < nst; ++it) {
     issue(it + kRingStages - 1);
     asm volatile("cp.async.wait_group %0;\n" ::"n"(kRingStages - 1) : "memory");
     __syncwarp();
-    const int i = r0 + it * 4 + grp;
-    const bool live = i < r1;
-    const int slot = live ? s_slot[i] : 0;
-    const bool ok = live && slot >= 0 && slot < a.n_slots;
-    if (live && !ok && sub == 0) atomicOr(err, kErrSlot);
     const float4* row = reinterpret_cast<const float4*>(wring + ((it % kRingStages) * 4 + grp) * kIdxDim);
     float4 kv[4];
 #pragma unroll
@@ -318,16 +317,25 @@ k_score(const IndexArgs a, void* ws, float* __restrict__ scores, int chunk, unsi
     d += __shfl_xor_sync(kFull, d, 1);               // head 2*bit2 + bit1, all 128 dims
     float v = wh * fmaxf(d, 0.f);
     v += __shfl_xor_sync(kFull, v, 2);
-    v += __shfl_xor_sync(kFull, v, 4);               // sum over the 4 heads
-    if (live && sub == 0) {
-      const float sc = ok ? v : -INFINITY;
-      srow[j0 + i] = sc;
-      if (kTopk) {
-        const unsigned bin = score_key(sc) >> (32 - kHistBits);
-        if (atomicAdd(&s_hist[bin], 1u) == 0u) s_touched[atomicAdd(&s_ntouched, 1u)] = (unsigned short)bin;
+    v += __shfl_xor_sync(kFull, v, 4);               // sum over the 4 heads, on every lane of the group
+    const float vg = __shfl_sync(kFull, v, (lane & 3) * 8);
+    if ((it & 7) == (lane >> 2)) hold = vg;
+    __syncwarp();   // every lane is done with this stage before it is refilled
+    if ((it & 7) == 7 || it == nst - 1) {
+      const int st = it - (it & 7) + (lane >> 2);
+      const int i = r0 + st * 4 + (lane & 3);
+      if (st <= it && i < r1) {
+        const int slot = s_slot[i];
+        const bool ok = slot >= 0 && slot < a.n_slots;
+        if (!ok) atomicOr(err, kErrSlot);
+        const float sc = ok ? hold : -INFINITY;
+        srow[j0 + i] = sc;
+        if (kTopk) {
+          const unsigned bin = score_key(sc) >> (32 - kHistBits);
+          if (atomicAdd(&s_hist[bin], 1u) == 0u) s_touched[atomicAdd(&s_ntouched, 1u)] = (unsigned short)bin;
+        }
       }
     }
-    __syncwarp();   // every lane is done with this stage before it is refilled
   }
   asm volatile("cp.async.wait_group 0;\n" ::: "memory");
   if (kTopk) {
