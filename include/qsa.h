@@ -73,6 +73,8 @@ typedef enum {
 } qsa_status;
 
 typedef enum { QSA_KV_F16 = 0, QSA_KV_Q8_0 = 1 } qsa_kv_type;
+/* n_recomputed value of qsa_index_topk's scheduling hint (see there). */
+#define QSA_HINT_QUERY_BLOCKS (-1)
 
 typedef struct {
   int32_t n_q_heads;       /* 16 */
@@ -193,7 +195,11 @@ qsa_status qsa_index_scores(const qsa_config* cfg, int32_t n_tokens,
  * for, as long as max_tokens stays the same.  max_blocks <= 1,048,576;
  * max_tokens <= 65535 (QSA_ERR_UNSUPPORTED beyond, QSA_ERR_SHAPE if
  * n_tokens > max_tokens).
- * recomputed / n_recomputed: optional scheduling hint, NULL / 0 for none.
+ * recomputed / n_recomputed: optional scheduling hint, NULL / 0 for none;
+ * NULL / QSA_HINT_QUERY_BLOCKS asserts instead that the preceding call on the
+ * stream changed only the pooled keys of blocks holding the query tokens' own
+ * positions (a qsa_kv_append of exactly these tokens, which re-pools them):
+ * work on the other blocks then starts without waiting for that call.
  * When this call directly follows a qsa_pool_update on the same stream, pass
  * that update's dirty list (entries < 0 ignored): work on blocks whose slots
  * are not in the list then starts without waiting for the update to finish
@@ -202,8 +208,8 @@ qsa_status qsa_index_scores(const qsa_config* cfg, int32_t n_tokens,
  * read before the preceding call has finished: it must hold its values before
  * that call is issued (a host-written list, as qsa_pool_update takes; not the
  * list a qsa_kv_append just wrote).  Results do not depend on the hint
- * otherwise.  QSA_ERR_INVALID_ARG if n_recomputed < 0,
- * or > 0 with a NULL list. */
+ * otherwise.  QSA_ERR_INVALID_ARG if n_recomputed < 0 (other than
+ * QSA_HINT_QUERY_BLOCKS with a NULL list), or > 0 with a NULL list. */
 size_t qsa_index_topk_workspace_size(const qsa_config* cfg, int32_t max_tokens,
                                      int64_t max_blocks);
 qsa_status qsa_index_topk(const qsa_config* cfg, int32_t n_tokens, int32_t max_tokens,

@@ -165,7 +165,8 @@ qsa_status qsa_index_topk(const qsa_config* cfg, int32_t n_tokens, int32_t max_t
   if (workspace == nullptr || !aligned(workspace, 256) ||
       ws_bytes < qsa_index_topk_workspace_size(cfg, max_tokens, max_blocks))
     return QSA_ERR_WORKSPACE;
-  if (n_recomputed < 0 || (n_recomputed > 0 && recomputed == nullptr)) return QSA_ERR_INVALID_ARG;
+  const bool query_hint = n_recomputed == QSA_HINT_QUERY_BLOCKS && recomputed == nullptr;
+  if ((n_recomputed < 0 && !query_hint) || (n_recomputed > 0 && recomputed == nullptr)) return QSA_ERR_INVALID_ARG;
   a.blk_cells = blk_cells;
   a.n_cells = n_cells;
   a.recomputed = recomputed;

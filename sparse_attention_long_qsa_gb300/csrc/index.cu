@@ -220,6 +220,10 @@ k_score(const IndexArgs a, void* ws, float* __restrict__ scores, int chunk, unsi
   const int32_t* slots = a.seq_blk_slots + tk.off;
   for (int i = tid; i < nrows; i += kScoreThreads) s_slot[i] = __ldg(slots + j0 + i);
   const bool use_hint = kTopk && a.recomputed != nullptr && a.n_recomputed <= kMaxHint && blockIdx.x != 0;
+  // caller's assertion: the preceding call recomputed only blocks holding
+  // the query tokens' own positions (an append of exactly these tokens)
+  const bool query_hint = kTopk && a.recomputed == nullptr && a.n_recomputed == QSA_HINT_QUERY_BLOCKS &&
+                          blockIdx.x != 0;
   if (use_hint)
     for (int i = tid; i < a.n_recomputed; i += kScoreThreads) s_rec[i] = a.recomputed[i];
 
@@ -247,6 +251,15 @@ k_score(const IndexArgs a, void* ws, float* __restrict__ scores, int chunk, unsi
     for (int i = tid; i < nrows; i += kScoreThreads) {
       const int sl = s_slot[i];
       for (int e = 0; e < a.n_recomputed; ++e) hit |= (s_rec[e] == sl);
+    }
+    must_wait = __syncthreads_or(hit) != 0;
+  } else if (query_hint) {
+    // any token of this sequence whose own block lies in this CTA's range
+    const int seq = a.tok_seq[t];
+    int hit = 0;
+    for (int u = tid; u < a.n_tokens; u += kScoreThreads) {
+      const int64_t jb = (int64_t)a.tok_pos[u] / a.r;
+      hit |= (a.tok_seq[u] == seq && jb >= j0 && jb < j1) ? 1 : 0;
     }
     must_wait = __syncthreads_or(hit) != 0;
   }

@@ -116,10 +116,10 @@ class QSALayer:
         (K/V, indexer keys, table, device dirty list) with the pool update of
         the blocks they dirty in the same launch, index top-k, sparse
         attention.  Returns the out[:T] view (fp32)."""
-        # no scheduling hint here: the dirty list is written by the append
-        # itself, and index_topk reads a hint before its predecessor finishes
+        # the append re-pooled only the query tokens' own blocks: score work on
+        # the other blocks may start before it finishes
         self.kv_append(tok_seq, tok_pos, cells, k_new, v_new, idx_new, stream, pool=True)
-        self.index_topk(tok_seq, tok_pos, q_idx, w_idx, stream=stream)
+        self.index_topk(tok_seq, tok_pos, q_idx, w_idx, recomputed="query_blocks", stream=stream)
         self.sparse_attn(q, int(tok_pos.numel()), stream)
         return self.out[:int(tok_pos.numel())]
 

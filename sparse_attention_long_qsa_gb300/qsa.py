@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libqsa.so")
 QSA_OK = 0
 QSA_KV_F16 = 0
 QSA_KV_Q8_0 = 1
+QSA_HINT_QUERY_BLOCKS = -1
 STATUS = {0: "QSA_OK", -1: "QSA_ERR_INVALID_ARG", -2: "QSA_ERR_SHAPE", -3: "QSA_ERR_UNSUPPORTED",
           -4: "QSA_ERR_WORKSPACE", -5: "QSA_ERR_CUDA", -6: "QSA_ERR_DEVICE_BOUNDS"}
 
@@ -191,12 +192,16 @@ def index_topk(cfg, q_idx, w_idx, tok_seq, tok_pos, pooled, blk_cells, seq_blk_o
                recomputed=None, stream=None):
     """workspace: a uint8 CUDA tensor of index_topk_workspace_size(cfg,
     max_tokens, max_blocks) bytes, zero-filled once when allocated.
-    recomputed: optional int32 CUDA tensor, the dirty list of the pool update
-    issued just before on the same stream (a scheduling hint)."""
+    recomputed: optional scheduling hint: an int32 CUDA tensor, the
+    (host-written) dirty list of the pool update issued just before on the
+    same stream, or "query_blocks" after an append of exactly these tokens."""
     import torch
     T = int(tok_pos.numel())
-    rec_ptr = _ptr(recomputed, torch.int32, "recomputed") if recomputed is not None else None
-    rec_n = int(recomputed.numel()) if recomputed is not None else 0
+    if isinstance(recomputed, str) and recomputed == "query_blocks":
+        rec_ptr, rec_n = None, QSA_HINT_QUERY_BLOCKS
+    else:
+        rec_ptr = _ptr(recomputed, torch.int32, "recomputed") if recomputed is not None else None
+        rec_n = int(recomputed.numel()) if recomputed is not None else 0
     st = lib().qsa_index_topk(
         ctypes.byref(cfg), T, int(max_tokens), _ptr(q_idx, torch.float32, "q_idx"),
         _ptr(w_idx, torch.float32, "w_idx"),

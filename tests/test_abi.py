@@ -82,8 +82,10 @@ def test_null_and_workspace_checks(L):
     assert L.qsa_sparse_attn(ctypes.byref(c), 5, None, fake, fake, 1000, fake, fake, fake, None, 0, None) == -1
     assert L.qsa_index_topk(ctypes.byref(c), 70_000, 70_000, *([fake] * 6), 100, fake, fake, 1, 10, 10,
                             fake, fake, None, 0, fake, need, None) == -3
-    # a hint length without a list
+    # a hint length without a list; a negative length other than the query-blocks hint
     assert L.qsa_index_topk(*args[:-2], None, 3, fake, need, None) == -1
+    assert L.qsa_index_topk(*args[:-2], None, -2, fake, need, None) == -1
+    assert L.qsa_index_topk(*args[:-2], fake, -1, fake, need, None) == -1
     # more tokens than the workspace was sized for
     assert L.qsa_index_topk(ctypes.byref(c), 6, 5, *([fake] * 6), 100, fake, fake, 1, 10, 10,
                             fake, fake, None, 0, fake, need, None) == -2
