@@ -8,8 +8,11 @@ workload, through the C ABI on one stream: qsa_kv_append (the step's new
 cells, the device dirty list and the re-pooling of the dirtied blocks) ->
 qsa_index_topk (score, select, expand) -> qsa_sparse_attn (attention with its
 split merge).  --path calls times qsa_pool_update -> qsa_index_topk ->
-qsa_sparse_attn with the table appended outside the timed region instead.  Inputs are resident in HBM when the timed region starts; L2
-is flushed (a 1 GiB write) before every step, outside the per-step events.
+qsa_sparse_attn with the table appended outside the timed region instead.
+Inputs are resident in HBM when the timed region starts; L2 is flushed
+before every step, outside the per-step events: a 1 GiB write, then a
+256 MiB read of its head, so the step starts with no line of its own data in
+L2 and no dirty line whose write-back it would pay for.
 Prints one JSON line (rank 0).
 
 Workloads (seeded, synthetic; shapes of the qwen4exp QSA layer):
@@ -40,6 +43,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "QSA-layer decode tokens/s at 50k/250k ctx (1 and 5 seqs); HBM GB/s vs peak"
 FLUSH_BYTES = [1 << 30]   # L2 flush buffer (--flush-mb)
+FLUSH_READ_BYTES = 256 << 20   # read after the flush write (> the 129 MB L2)
 
 DESCR = {
     "50k": "decode, 1 seq, 50,000-cell fp16 K/V prompt + 1 cell/step (tails cycle 1,2,3,0), "
@@ -288,8 +292,8 @@ class _ExternalEvents:
 
 def measure_config(name, K, W, dev, *, path="full", e2e=True, clocks=None):
     """Time K decode steps of workload `name` on the device.  The K timed
-    steps are captured as ONE CUDA graph: per step an L2 flush (outside the
-    step's events), a start event node, the step, an end event node.  Path
+    steps are captured as ONE CUDA graph: per step an L2 flush (write, then
+    read; outside the step's events), a start event node, the step, an end event node.  Path
     "full" (the layer's whole step): qsa_kv_append (the step's new cells, the
     device dirty list and, in the same launch, the re-pooling of the dirtied
     blocks), qsa_index_topk, qsa_sparse_attn.  Path "calls": qsa_pool_update,
@@ -315,6 +319,7 @@ def measure_config(name, K, W, dev, *, path="full", e2e=True, clocks=None):
         s_, rows = append_rows(wl, i)
         appends.append((torch.from_numpy(s_).to(dev), torch.from_numpy(rows).to(dev)))
     flush = torch.empty(FLUSH_BYTES[0] // 4, dtype=torch.float32, device=dev)
+    rsum = torch.zeros((), dtype=torch.float32, device=dev)
     toks = [len(st.tok_pos) for st in wl.steps]
     alg = [algorithmic_bytes(wl, i) for i in range(n_steps)]
     # path "full": the append kernel also re-pools the blocks it dirties
@@ -377,6 +382,9 @@ def measure_config(name, K, W, dev, *, path="full", e2e=True, clocks=None):
             for n, i in enumerate(idx):
                 do_append(i)
                 flush.fill_(float(n))
+                # read back the buffer's head (> L2): the flush's dirty lines
+                # are written back here, not by the step's first reads
+                rsum.copy_(flush[:FLUSH_READ_BYTES // 4].sum())
                 for k, (a, b) in hk[n].items():
                     qsa.profile_kernel(k, a, b)
                 xev.record(ev[n][0])
@@ -529,7 +537,8 @@ def run_native(args, rank, world, local):
                                  "table append outside the events, qsa_pool_update + qsa_index_topk + "
                                  "qsa_sparse_attn = 4 kernels")
                               + " chained by programmatic dependent launch, end event), replayed once"),
-                   "l2": f"flushed before every step ({FLUSH_BYTES[0] >> 20} MiB write), outside the step's events",
+                   "l2": (f"flushed before every step ({FLUSH_BYTES[0] >> 20} MiB write, then a {FLUSH_READ_BYTES >> 20} MiB "
+                          "read of its head so that no dirty line is left), outside the step's events"),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"kernel": res["dominant"], "choice": "kernel moving the most algorithmic bytes per step",
                      "longest_kernel": res["longest"], "bound": "hbm", "achieved": achieved,
