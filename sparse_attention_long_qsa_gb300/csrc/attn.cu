@@ -658,18 +658,33 @@ cudaError_t pick_cluster(const AttnArgs& a, int* nc_out) {
   }
   const int tiles = (int)ceil_div(a.cells_pitch, kTile);
   const int want = tiles < kMaxCluster ? tiles : kMaxCluster;
-  const int clusters = a.n_tokens * a.n_kv_heads;
-  int nc = 0, largest = 1;
+  const int64_t clusters = (int64_t)a.n_tokens * a.n_kv_heads;
+  int nc = 0;
   for (int i = 0; i < 5; ++i) {            // sizes 16, 8, 4, 2, 1
     const int c = 16 >> i;
     if (c > want || max_active[dev][i] <= 0) continue;
-    if (largest == 1 && c > 1) largest = c;
     if (clusters <= max_active[dev][i]) {  // the largest size that runs in one wave
       nc = c;
       break;
     }
   }
-  if (nc == 0) nc = largest;               // several waves either way: fewest tiles per CTA
+  if (nc == 0) {
+    // Several waves at every size: a CTA costs about one tile's time of its
+    // own (launch, prologue, cluster combine) plus one per tile it takes, so
+    // pick the size with the fewest waves x (1 + tiles per CTA).
+    int64_t best = -1;
+    for (int i = 0; i < 5; ++i) {
+      const int c = 16 >> i;
+      if (c > want || max_active[dev][i] <= 0) continue;
+      const int64_t waves = ceil_div(clusters, (int64_t)max_active[dev][i]);
+      const int64_t cost = waves * (1 + ceil_div((int64_t)tiles, (int64_t)c));
+      if (best < 0 || cost < best) {
+        best = cost;
+        nc = c;
+      }
+    }
+    if (nc == 0) nc = 1;
+  }
   *nc_out = nc;
   return cudaSuccess;
 }
