@@ -19,7 +19,8 @@
 //             HBM traffic at long context: 512 B per block), writes fp32
 //             scores and adds each block to a per-token 4096-bin histogram of
 //             the top 12 bits of the order-preserving score key.
-//   k_select  one thread-block cluster per token.  Every CTA reads the
+//   k_select  one thread-block cluster per token (8 CTAs for a few tokens,
+//             down to 1 for many: select_cluster).  Every CTA reads the
 //             histogram and finds the bin holding the B-th largest score.
 //             Each CTA then takes a range of blocks: blocks above that bin go
 //             straight into its shared selection bitmap (warp ballots), blocks
@@ -897,6 +898,26 @@ int score_chunk(int T, int64_t max_blocks, int sms) {
   return (int)chunk;
 }
 
+// CTAs per selection cluster.  One k_select CTA fills an SM (512 threads,
+// ~118 KB of shared memory).  A CTA costs about 5 us of its own (histogram,
+// barriers, ordering, expansion) plus ~3 us per 62,500 blocks it classifies,
+// so few tokens take 8-CTA clusters (one wave either way) and many tokens
+// take small clusters (fewer waves); a CTA holds at most kSelMaxWords words.
+int select_cluster(int T, int64_t max_blocks, int sms) {
+  int best_nc = kSelCluster;
+  double best = -1.0;
+  for (int nc = kSelCluster; nc >= 1; nc >>= 1) {
+    if (ceil_div(max_blocks, (int64_t)nc) > (int64_t)kSelMaxWords * 32) break;
+    const double waves = (double)ceil_div((int64_t)T * nc, (int64_t)(sms > 0 ? sms : 1));
+    const double cost = waves * (5.0 + 3.0 * (double)max_blocks / 62500.0 / nc);
+    if (best < 0.0 || cost < best) {
+      best = cost;
+      best_nc = nc;
+    }
+  }
+  return best_nc;
+}
+
 // Per-device set-up of the index kernels: SM count, shared-memory limits.
 cudaError_t index_setup(int* sms) {
   static int sm_count[64];
@@ -963,8 +984,9 @@ cudaError_t launch_index_topk(const IndexArgs& a, int32_t* cells, int32_t* count
   prof_after(kKScore, stream);
   if (e != cudaSuccess) return e;
   prof_before(kKFinal, stream);
-  e = launch_pdl(k_select, dim3(kSelCluster, (unsigned)a.n_tokens), dim3(kSelThreads), slot_bytes, stream,
-                 (unsigned)kSelCluster, b, ws, (const float*)sc, cells, count, err);
+  const int nc = select_cluster(a.n_tokens, b.max_blocks, sms);
+  e = launch_pdl(k_select, dim3((unsigned)nc, (unsigned)a.n_tokens), dim3(kSelThreads), slot_bytes, stream,
+                 (unsigned)nc, b, ws, (const float*)sc, cells, count, err);
   prof_after(kKFinal, stream);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -85,6 +85,19 @@ def test_prefill_chunk_causal():
         assert np.all(res["cells"][t, :cnt] <= st.tok_pos[t])
 
 
+@pytest.mark.parametrize("T", [20, 40])
+def test_multi_token_select_cluster_sizes(T):
+    """Selection clusters shrink as tokens grow (8 CTAs for a few tokens, 4 at
+    20 tokens, 2 at 40, 1 at 96 on a 152-SM GPU): each size is exact."""
+    wl = make_workload(n_seq=1, prompt_len=10_001, n_steps=1, tokens_per_step=T, seed=7 + T)
+    run = Runner(wl)
+    res, _ = check_step(run, 0)
+    st = wl.steps[0]
+    for t in range(T):
+        cnt = int(res["count"][t])
+        assert np.all(res["cells"][t, :cnt] <= st.tok_pos[t])
+
+
 @pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 7, 2048, 2050, 2051, 2052, 2055])
 def test_degenerate_and_budget_edges(n):
     """n <= top_k + r - 1: dense causal attention over all n cells; past it
