@@ -75,8 +75,11 @@ def algorithmic_bytes(wl, step_idx: int):
       append: per new cell its fp16 K/V rows read and written in the cache's
               encoding, its indexer key read and written, table entry, dirty list
       pool:   per dirty slot r fp16 idx-key rows (256 B) + table row + 512 B write
-      score:  per visible block a 512 B pooled row + 4 B slot id + 4 B score write,
-              plus the token's 2 KiB query and 16 B weights
+      score:  per visible block of a sequence a 512 B pooled row + 4 B slot id
+              (once per step however many of its tokens score it), per token
+              and visible block a 4 B score write, plus the token's 2 KiB
+              query and 16 B weights
+      hist:   (token-tiled scoring only) the scores read back, 4 B each
       select: 4 B score read per visible block, per chosen block 4 B slot +
               r*4 B members, + the cell list written
       attn:   per selected cell and KV head one K and one V row (512 B each fp16,
@@ -88,18 +91,23 @@ def algorithmic_bytes(wl, step_idx: int):
     G = cfg["n_kv_heads"]
     st = wl.steps[step_idx]
     row_b = 2 * 256 if cfg["kv_type"] == "f16" else 256 + 16
-    out = dict(append=0.0, pool=0.0, score=0.0, select=0.0, attn=0.0)
+    out = dict(append=0.0, pool=0.0, score=0.0, hist=0.0, select=0.0, attn=0.0)
     nd = int((st.dirty >= 0).sum())
     T = len(st.tok_pos)
     # per new cell: its K and V rows read (fp16) and written (cache encoding),
     # its indexer key read and written, token ids, the table entry, the dirty list
     out["append"] = T * (2 * G * 512 + 2 * G * row_b + 2 * 256 + 3 * 4 + 4) + 4 * max(4, T)
     out["pool"] = nd * (r * 256 + 4 * r + 4 + 512)
+    rows = {}
+    for s_, p in zip(st.tok_seq.tolist(), st.tok_pos.tolist()):
+        rows[s_] = max(rows.get(s_, 0), (p + 1) // r)
+    out["score"] = float(sum(rows.values()) * (512 + 4))
     for p in st.tok_pos.tolist():
         nb = (p + 1) // r
         tail = p + 1 - nb * r
         nsel = min(nb, B) * r + tail
-        out["score"] += nb * (512 + 4 + 4) + 2048 + 16
+        out["score"] += nb * 4 + 2048 + 16
+        out["hist"] += nb * 4
         out["select"] += nb * 4 + min(nb, B) * (4 + 4 * r) + (cfg["top_k"] + r - 1) * 4
         out["attn"] += (nsel * G * 2 * row_b + nsel * 4 + cfg["n_q_heads"] * cfg["head_dim"] * 2
                         + cfg["n_q_heads"] * cfg["head_dim"] * 4)
@@ -323,12 +331,15 @@ def measure_config(name, K, W, dev, *, path="full", e2e=True, clocks=None):
     toks = [len(st.tok_pos) for st in wl.steps]
     alg = [algorithmic_bytes(wl, i) for i in range(n_steps)]
     # path "full": the append kernel also re-pools the blocks it dirties
-    kernels = ["append", "score", "select", "attn"] if full else ["pool", "score", "select", "attn"]
+    index_k = qsa.index_topk_kernels(toks[0], wl.n_seq)   # score (+ hist), select
+    kernels = (["append"] if full else ["pool"]) + index_k + ["attn"]
     for a in alg:
         if full:
             a["append"] += a.pop("pool")
         else:
             a.pop("append")
+        if "hist" not in index_k:
+            a.pop("hist")
     step_fn = L.full_step if full else L.step
     xev = _ExternalEvents()
 
@@ -431,7 +442,7 @@ def measure_config(name, K, W, dev, *, path="full", e2e=True, clocks=None):
     dev_ms = float(np.sum(ms))
     tokens = sum(toks[i] for i in idx)
     res = dict(value=tokens / (dev_ms / 1e3), ms_per_step=dev_ms / K, tokens=tokens, wall_s=wall, path=path,
-               launches_per_step=len(kernels),
+               launches_per_step=len(kernels), kernels=kernels,
                dominant=dominant, longest=longest, dom_ms=dom_ms, dom_bytes=dom_bytes, kern_us=kern_us,
                kern_gbs={k: kbytes[k] / (kern_us[k] * 1e-6) / 1e9 for k in kernels if kern_us[k] > 0},
                gen_s=t_gen, wl=wl, step_bytes=float(np.mean([sum(alg[i].values()) for i in idx])),
@@ -532,10 +543,11 @@ def run_native(args, rank, world, local):
                    "path": args.path,
                    "launch": ("the K timed steps captured as one CUDA graph (per step: L2 flush, start event, "
                               + ("qsa_kv_append (re-pooling the blocks it dirties) + qsa_index_topk + "
-                                 "qsa_sparse_attn = 4 kernels"
+                                 "qsa_sparse_attn"
                                  if args.path == "full" else
                                  "table append outside the events, qsa_pool_update + qsa_index_topk + "
-                                 "qsa_sparse_attn = 4 kernels")
+                                 "qsa_sparse_attn")
+                              + f" = {res['launches_per_step']} kernels ({', '.join(res['kernels'])})"
                               + " chained by programmatic dependent launch, end event), replayed once"),
                    "l2": (f"flushed before every step ({FLUSH_BYTES[0] >> 20} MiB write, then a {FLUSH_READ_BYTES >> 20} MiB "
                           "read of its head so that no dirty line is left), outside the step's events"),

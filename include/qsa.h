@@ -163,7 +163,9 @@ qsa_status qsa_pool_update(const qsa_config* cfg,
  * For token t of sequence s = tok_seq[t] at position p = tok_pos[t], and each
  * block j < floor((p+1)/r) of s:
  *   scores[t][j] = sum_h w_idx[t][h] * max(0, q_idx[t][h] . pooled[slot(s,j)])
- * fp32, fixed summation order (the same kernel qsa_index_topk runs).  Entries
+ * fp32, fixed summation order: the kernel qsa_index_topk runs for the same
+ * n_tokens and n_seq (one pass per token, or token-tiled when tokens share
+ * sequences: see qsa_index_topk_kernels), so the scores are the same bits.  Entries
  * j >= floor((p+1)/r) of the row (pitch max_blocks) are written as -inf.
  * max_blocks: host upper bound on floor((p+1)/r) over the tokens; a token
  * beyond it is clamped and flagged.  Exposed so the scores can be checked on
@@ -208,7 +210,8 @@ qsa_status qsa_index_scores(const qsa_config* cfg, int32_t n_tokens,
  * read before the preceding call has finished: it must hold its values before
  * that call is issued (a host-written list, as qsa_pool_update takes; not the
  * list a qsa_kv_append just wrote).  Results do not depend on the hint
- * otherwise.  QSA_ERR_INVALID_ARG if n_recomputed < 0 (other than
+ * otherwise, and the token-tiled scorer (qsa_index_topk_kernels) always
+ * waits.  QSA_ERR_INVALID_ARG if n_recomputed < 0 (other than
  * QSA_HINT_QUERY_BLOCKS with a NULL list), or > 0 with a NULL list. */
 size_t qsa_index_topk_workspace_size(const qsa_config* cfg, int32_t max_tokens,
                                      int64_t max_blocks);
@@ -294,11 +297,22 @@ qsa_status qsa_debug_check(qsa_stream_t stream, uint32_t* flags);
  * (cudaEventRecordExternal, so inside a stream capture they become event
  * nodes that timestamp every replay), and cudaEventElapsedTime gives that
  * launch's device time.
- * Kernel ids: 0 pool update (qsa_pool_update), 1 block scores + threshold
- * bin, 3 cluster select + expansion (qsa_index_topk), 4 attention
- * (qsa_sparse_attn), 5 append (qsa_kv_append); 2 is reserved.  `before`/`after` are cudaEvent_t
- * handles; NULL clears.  QSA_ERR_INVALID_ARG for an unknown id. */
+ * Kernel ids: 0 pool update (qsa_pool_update), 1 block scores (+ threshold
+ * histogram when one token per sequence), 2 threshold histogram of
+ * token-tiled scores, 3 cluster select + expansion (qsa_index_topk), 4
+ * attention (qsa_sparse_attn), 5 append (qsa_kv_append).  `before`/`after`
+ * are cudaEvent_t handles; NULL clears.  QSA_ERR_INVALID_ARG for an unknown
+ * id. */
 qsa_status qsa_profile_kernel(int32_t kernel, void* before, void* after);
+
+/* Which kernels (bit k = kernel id k above) one qsa_index_topk call of
+ * n_tokens tokens over n_seq sequences launches.  Scoring is token-tiled
+ * (each pooled row read once per tile of 16 tokens of one sequence and
+ * scored on the tensor cores, kernel 1, then kernel 2 builds the threshold
+ * histogram) when n_tokens > 8 and n_tokens >= 2 * n_seq; otherwise one pass
+ * per token builds the histogram as it scores.  qsa_index_scores follows the same
+ * rule, so both calls compute bit-identical scores. */
+uint32_t qsa_index_topk_kernels(int32_t n_tokens, int32_t n_seq);
 
 const char* qsa_status_string(qsa_status s);
 

@@ -199,9 +199,10 @@ def make_workload(name: str = "custom", *, n_seq: Optional[int] = None,
     """Build a workload.  Named presets: tiny, 50k, 250k_q8, 5x250k_q8, prefill, verify5_250k_q8.
 
     Decode (tokens_per_step == 1): every step appends one position to each
-    sequence and queries it; n_seq tokens per step.  Prefill
-    (tokens_per_step > 1, one sequence): one step appends tokens_per_step
-    positions and queries all of them.
+    sequence and queries it; n_seq tokens per step.  Prefill or verify
+    (tokens_per_step > 1): every step appends tokens_per_step consecutive
+    positions to each sequence and queries all of them (tokens ordered by
+    sequence, then position).
 
     Cells: prompts occupy contiguous cell ranges (sequence-major), decode cells
     are appended interleaved across sequences; shuffled=True permutes all cells
@@ -224,8 +225,6 @@ def make_workload(name: str = "custom", *, n_seq: Optional[int] = None,
         prompt_len = [int(prompt_len)] * n_seq
     prompt_len = [int(x) for x in prompt_len]
     assert len(prompt_len) == n_seq
-    if tokens_per_step > 1:
-        assert n_seq == 1, "prefill workloads hold one sequence"
 
     c = default_cfg(kv_type=kv_type, **(cfg or {}))
     r = c["compress_ratio"]

@@ -283,6 +283,12 @@ qsa_status qsa_debug_check(qsa_stream_t stream, uint32_t* flags) {
   return QSA_ERR_DEVICE_BOUNDS;
 }
 
+uint32_t qsa_index_topk_kernels(int32_t n_tokens, int32_t n_seq) {
+  if (n_tokens <= 0) return 0u;
+  if (qsa::index_tiled(n_tokens, n_seq)) return (1u << qsa::kKScore) | (1u << qsa::kKHist) | (1u << qsa::kKFinal);
+  return (1u << qsa::kKScore) | (1u << qsa::kKFinal);
+}
+
 qsa_status qsa_profile_kernel(int32_t kernel, void* before, void* after) {
   if (kernel < 0 || kernel >= kNumKernels) return QSA_ERR_INVALID_ARG;
   g_profile.before[kernel] = static_cast<cudaEvent_t>(before);

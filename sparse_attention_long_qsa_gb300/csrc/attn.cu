@@ -36,6 +36,7 @@
 #include <cstring>
 
 #include "qsa_internal.cuh"
+#include "tc_util.cuh"
 
 QSA_TS_DECLARE(attn)
 
@@ -70,80 +71,10 @@ constexpr uint32_t kOffXC = kOffXM + 64;            // int [kOvf] cells
 constexpr uint32_t kOffW = kOffXC + kOvf * 4;        // fp32 [16][8] combine weights, [8] denominators
 constexpr uint32_t kSmemBytes = kOffW + (kMaxCluster * 8 + 8) * 4 + 1024;   // + alignment slack
 
-// Byte offset of 16-byte chunk `c16` (0..31 along a 512-byte row) of row `row`
-// in a tile of `rows` rows stored as 128-byte swizzled atoms: atom column
-// c16 / 8 (64 fp16 values), row-major 128-byte rows inside it, the chunk index
-// XOR-ed with row % 8 (the 128B swizzle of the canonical UMMA layouts).
-__device__ __forceinline__ uint32_t sw128(uint32_t rows, uint32_t row, uint32_t c16) {
-  return (c16 >> 3) * rows * 128u + row * 128u + (((c16 & 7u) ^ (row & 7u)) << 4);
-}
-
-// Shared-memory matrix descriptor (tcgen05): start address, leading and stride
-// byte offsets (>> 4), descriptor version 1, 128-byte swizzle.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
-  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
-  return d;
-}
-
 // Instruction descriptor, kind::f16: fp32 accumulate, fp16 A and B,
 // M = 128, N = 16; A K-major (QK) or MN-major (PV), B K-major.
 constexpr uint32_t kIdescQK = (1u << 4) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
 constexpr uint32_t kIdescPV = kIdescQK | (1u << 15);
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t saddr, const void* gmem, bool pred) {
-  const int sz = pred ? 16 : 0;
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(saddr), "l"(gmem), "r"(sz) : "memory");
-}
-
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc)
-      : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
-               : "memory");
-}
-
-// Bounded wait on an mbarrier phase; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (int i = 0; i < (1 << 22); ++i) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    if (ok) return true;
-  }
-  return false;
-}
-
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float* v) {
-  uint32_t r[8];
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-               : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
 
 // Barrier among the 128 threads of warps 0-3 (id 1) or of warps 4-7 (id 2).
 __device__ __forceinline__ void bar_half(int id) { asm volatile("bar.sync %0, 128;\n" ::"r"(id) : "memory"); }

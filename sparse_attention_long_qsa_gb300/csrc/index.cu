@@ -19,6 +19,11 @@
 //             HBM traffic at long context: 512 B per block), writes fp32
 //             scores and adds each block to a per-token 4096-bin histogram of
 //             the top 12 bits of the order-preserving score key.
+//   k_score_tc / k_hist  replace k_score when the call's tokens share
+//             sequences (a verify batch, a prefill ubatch): each pooled row
+//             is read once per tile of 16 tokens and scored on the
+//             tensor cores (split-TF32, fp32-accurate), then k_hist builds the
+//             histogram from the written scores.
 //   k_select  one thread-block cluster per token (8 CTAs for a few tokens,
 //             down to 1 for many: select_cluster).  Every CTA reads the
 //             histogram and finds the bin holding the B-th largest score.
@@ -32,9 +37,11 @@
 //             the member cells of its chosen blocks at its offset in the
 //             token's list (blocks ascending), CTA 0 appends the tail cells
 //             and clears the histogram for the next call.
+#include <algorithm>
 #include <cstring>
 
 #include "qsa_internal.cuh"
+#include "tc_util.cuh"
 
 QSA_TS_DECLARE(index)
 
@@ -360,6 +367,270 @@ k_score(const IndexArgs a, void* ws, float* __restrict__ scores, int chunk, unsi
       const unsigned b = s_touched[i];
       atomicAdd(ghist + b, s_hist[b]);
     }
+  }
+}
+
+// ------------------------------------------------------------- k_score_tc
+// Token-tiled scores on the tensor cores: D[row][4u + h] = pooled[row] .
+// q_idx[t0 + u][h] for M = 128 rows x N = 4 NT (NT tokens x 4 heads) x K =
+// 128 dims, tcgen05 kind::tf32 with each fp32 operand split in two, x = t(x)
+// + l(x), t(x) = x with its low 13 mantissa bits cleared (a TF32 value) and
+// l(x) = x - t(x) rounded to TF32:  D = t(A) t(B) + t(A) l(B) + l(A) t(B),
+// every product exact in fp32, accumulated in fp32 in tensor memory.  The
+// omitted l(A) l(B) and the rounding of l(.) are below 2^-21 of each product,
+// under the rounding of an fp32 FMA chain over 128 terms.  A is gathered by
+// slot with cp.async into a 128B-swizzled K-major tile, KC dims at a time,
+// and split in place; B (the query tile) is split once per CTA.  The
+// epilogue turns the 4 head dots of a (row, token) into its score as k_score
+// does, warps 0-3 for the first half of the tokens, warps 4-7 for the second.
+template <int NT, int KC>
+struct TcShape {
+  static constexpr int N = NT * 4;
+  static constexpr uint32_t kBBytes = (uint32_t)N * 512u;        // t(B) or l(B): N rows x 128 fp32
+  static constexpr uint32_t kABytes = 128u * KC * 4u;            // t(A) or l(A): 128 rows x KC fp32
+  static constexpr uint32_t kOffBt = 0, kOffBl = kBBytes;
+  static constexpr uint32_t kOffAt = 2 * kBBytes, kOffAl = 2 * kBBytes + kABytes;
+  static constexpr uint32_t kOffBar = 2 * kBBytes + 2 * kABytes;
+  static constexpr uint32_t kOffTmem = kOffBar + 8;
+  static constexpr uint32_t kOffSlot = kOffBar + 16;             // int32 [128]
+  static constexpr size_t kSmem = kOffSlot + 128 * 4 + 1024;     // + alignment slack
+  static constexpr uint32_t kTmemCols = N < 32 ? 32u : (uint32_t)N;
+  // kind::tf32: fp32 accumulate, A and B TF32, both K-major, N, M = 128
+  static constexpr uint32_t kIdesc = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) |
+                                     ((128u >> 4) << 24);
+  static_assert(NT % 8 == 0 && N <= 256 && N % 16 == 0, "token tile");
+  static_assert(KC % 32 == 0 && 128 % KC == 0, "dim chunk");
+};
+
+__device__ __forceinline__ float tf32_trunc(float x) { return __uint_as_float(__float_as_uint(x) & 0xffffe000u); }
+// x rounded to the nearest TF32 value (ties away from zero)
+__device__ __forceinline__ float tf32_round(float x) {
+  return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u);
+}
+
+template <int NT, int KC, bool kTopk>
+__global__ void __launch_bounds__(256, 1)
+k_score_tc(const IndexArgs a, float* __restrict__ scores, unsigned* err) {
+  using S = TcShape<NT, KC>;
+  extern __shared__ unsigned char tc_smem_raw[];
+  const uint32_t raw_s = smem_u32(tc_smem_raw);
+  const uint32_t base_s = (raw_s + 1023u) & ~1023u;
+  unsigned char* base = tc_smem_raw + (base_s - raw_s);
+  int32_t* s_slot = reinterpret_cast<int32_t*>(base + S::kOffSlot);
+  const uint32_t bar = base_s + S::kOffBar;
+  __shared__ int s_seq[NT], s_nb[NT];
+  __shared__ int64_t s_off[NT];
+  __shared__ float s_w[NT][kIdxHeads];
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int t0 = blockIdx.y * NT;
+
+  // ---- before the wait: tensor memory, barrier, tokens, query tile
+  if (warp == 0) tmem_alloc(base_s + S::kOffTmem, S::kTmemCols);
+  if (tid == 0) mbar_init(bar, 1);
+  if (tid < NT) {
+    const int t = t0 + tid;
+    int seq = -1, nb = 0;
+    int64_t off = 0;
+    if (t < a.n_tokens) {
+      const Tok tk = token_geometry(a, t, err, blockIdx.x == 0);
+      if (tk.ok) {
+        seq = a.tok_seq[t];
+        nb = tk.nb;
+        off = tk.off;
+      }
+    }
+    s_seq[tid] = seq;
+    s_nb[tid] = nb;
+    s_off[tid] = off;
+#pragma unroll
+    for (int h = 0; h < kIdxHeads; ++h) s_w[tid][h] = t < a.n_tokens ? a.w_idx[(int64_t)t * kIdxHeads + h] : 0.f;
+  }
+  for (int i = tid; i < S::N * (kIdxDim / 4); i += 256) {
+    const int n = i / (kIdxDim / 4), c16 = i % (kIdxDim / 4);
+    const int t = t0 + (n >> 2);
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (t < a.n_tokens)
+      v = __ldg(reinterpret_cast<const float4*>(a.q_idx + ((int64_t)t * kIdxHeads + (n & 3)) * kIdxDim) + c16);
+    const float4 vt = make_float4(tf32_trunc(v.x), tf32_trunc(v.y), tf32_trunc(v.z), tf32_trunc(v.w));
+    const float4 vl = make_float4(tf32_round(v.x - vt.x), tf32_round(v.y - vt.y), tf32_round(v.z - vt.z),
+                                  tf32_round(v.w - vt.w));
+    const uint32_t o = sw128((uint32_t)S::N, (uint32_t)n, (uint32_t)c16);
+    *reinterpret_cast<float4*>(base + S::kOffBt + o) = vt;
+    *reinterpret_cast<float4*>(base + S::kOffBl + o) = vl;
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<const uint32_t*>(base + S::kOffTmem);
+
+  // ---- pooled rows are written by the preceding pool update / append
+  grid_dep_wait();
+  grid_dep_launch();
+
+  uint32_t phase = 0;
+  bool timed_out = false;
+  const int row = tid >> 1, half = tid & 1;             // gather: half a row chunk per thread
+  constexpr int kMine = KC / 8;                         // 16-byte pieces per thread per chunk
+  const int erow = 32 * (warp & 3) + lane;              // epilogue: TMEM lane = row of the tile
+  const int ehalf = warp >> 2;                          // epilogue: tokens [ehalf * NT/2, +NT/2)
+  unsigned done = 0;
+  for (int v = 0; v < NT; ++v)
+    if (s_seq[v] < 0) done |= 1u << v;
+  const unsigned all = (1u << NT) - 1u;
+  while (done != all) {
+    const int first = __ffs(~done) - 1;
+    const int seq = s_seq[first];
+    unsigned mask = 0;
+    int nbmax = 0;
+    for (int v = 0; v < NT; ++v)
+      if (s_seq[v] == seq) {
+        mask |= 1u << v;
+        nbmax = max(nbmax, s_nb[v]);
+      }
+    done |= mask;
+    const int64_t off = s_off[first];
+    const int64_t tiles = ceil_div((int64_t)nbmax, 128);
+    for (int64_t rt = blockIdx.x; rt < tiles; rt += gridDim.x) {
+      const int64_t j0 = rt * 128;
+      if (tid < 128) {
+        int sl = -1;
+        if (j0 + tid < nbmax) {
+          sl = a.seq_blk_slots[off + j0 + tid];
+          if (sl < 0 || sl >= a.n_slots) {
+            atomicOr(err, kErrSlot);
+            sl = -1;
+          }
+        }
+        s_slot[tid] = sl;
+      }
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+      const int sl = s_slot[row];
+      const float* src = a.pooled + (int64_t)(sl < 0 ? 0 : sl) * kIdxDim;
+      for (int c = 0; c < kIdxDim / KC; ++c) {
+        // raw rows, dims [c KC, c KC + KC), into t(A); zeros for rows without a slot
+#pragma unroll
+        for (int m = 0; m < kMine; ++m) {
+          const int q = half * kMine + m;
+          cp_async16(base_s + S::kOffAt + sw128(128u, (uint32_t)row, (uint32_t)q), src + c * KC + q * 4, sl >= 0);
+        }
+        asm volatile("cp.async.wait_all;\n" ::: "memory");
+        // split my pieces in place: t(A) truncated, l(A) rounded
+#pragma unroll
+        for (int m = 0; m < kMine; ++m) {
+          const int q = half * kMine + m;
+          const uint32_t o = sw128(128u, (uint32_t)row, (uint32_t)q);
+          const float4 x = *reinterpret_cast<const float4*>(base + S::kOffAt + o);
+          const float4 xt = make_float4(tf32_trunc(x.x), tf32_trunc(x.y), tf32_trunc(x.z), tf32_trunc(x.w));
+          const float4 xl = make_float4(tf32_round(x.x - xt.x), tf32_round(x.y - xt.y), tf32_round(x.z - xt.z),
+                                        tf32_round(x.w - xt.w));
+          *reinterpret_cast<float4*>(base + S::kOffAt + o) = xt;
+          *reinterpret_cast<float4*>(base + S::kOffAl + o) = xl;
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (tid == 0) {
+#pragma unroll
+          for (int kk = 0; kk < KC / 8; ++kk) {
+            const int kg = c * (KC / 8) + kk;     // K step of 8 dims over the whole row
+            const uint32_t ka = (uint32_t)(kk >> 2) * (128u * 128u) + (uint32_t)(kk & 3) * 32u;
+            const uint32_t kb = (uint32_t)(kg >> 2) * ((uint32_t)S::N * 128u) + (uint32_t)(kg & 3) * 32u;
+            const uint64_t at = smem_desc(base_s + S::kOffAt + ka, 16, 1024);
+            const uint64_t al = smem_desc(base_s + S::kOffAl + ka, 16, 1024);
+            const uint64_t bt = smem_desc(base_s + S::kOffBt + kb, 16, 1024);
+            const uint64_t bl = smem_desc(base_s + S::kOffBl + kb, 16, 1024);
+            mma_tf32(tmem, at, bt, S::kIdesc, kg > 0 ? 1u : 0u);
+            mma_tf32(tmem, at, bl, S::kIdesc, 1u);
+            mma_tf32(tmem, al, bt, S::kIdesc, 1u);
+          }
+          mma_commit(bar);
+        }
+        if (!mbar_wait(bar, phase)) timed_out = true;
+        phase ^= 1;
+        tc_fence_after();
+      }
+      // ---- epilogue: row erow, tokens of this warp's half
+      {
+        constexpr int kHalfCols = NT * 2;                 // NT/2 tokens x 4 heads
+        uint32_t r[kHalfCols];
+#pragma unroll
+        for (int g = 0; g < kHalfCols / 16; ++g)
+          tmem_ld16_nowait(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(ehalf * kHalfCols + 16 * g),
+                           r + 16 * g);
+        tmem_wait_ld();
+        const int64_t j = j0 + erow;
+        const bool rok = s_slot[erow] >= 0;
+#pragma unroll
+        for (int uu = 0; uu < NT / 2; ++uu) {
+          const int u = ehalf * (NT / 2) + uu;
+          if (((mask >> u) & 1u) && j < s_nb[u]) {
+            float v[kIdxHeads];
+#pragma unroll
+            for (int h = 0; h < kIdxHeads; ++h) v[h] = s_w[u][h] * fmaxf(__uint_as_float(r[uu * 4 + h]), 0.f);
+            scores[(int64_t)(t0 + u) * a.max_blocks + j] = rok ? (v[0] + v[1]) + (v[2] + v[3]) : -INFINITY;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncthreads();   // TMEM read and slots used before the next tile
+      tc_fence_after();
+    }
+  }
+  if (!kTopk) {
+    // -inf for the blocks of this CTA's row tiles a token does not see
+    const int64_t all_tiles = ceil_div(a.max_blocks, 128);
+    for (int64_t rt = blockIdx.x; rt < all_tiles; rt += gridDim.x)
+      for (int i = tid; i < NT * 128; i += 256) {
+        const int v = i / 128;
+        const int64_t j = rt * 128 + i % 128;
+        const int t = t0 + v;
+        if (t < a.n_tokens && j < a.max_blocks && j >= s_nb[v]) scores[(int64_t)t * a.max_blocks + j] = -INFINITY;
+      }
+  }
+  if (timed_out) atomicOr(err, kErrTimeout);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, S::kTmemCols);
+}
+
+// ------------------------------------------------------------------ k_hist
+// Threshold-bin histogram of the scores written by k_score_tc (k_score builds
+// it while scoring): a CTA takes kHistChunk blocks of one token, counts
+// them in shared memory and adds only the bins it touched to the token's
+// histogram.
+constexpr int kHistChunk = 8192;
+
+__global__ void __launch_bounds__(256)
+k_hist(const IndexArgs a, void* ws, const float* __restrict__ scores) {
+  __shared__ unsigned s_hist[kHistBins];
+  __shared__ unsigned short s_touched[kHistBins];
+  __shared__ unsigned s_ntouched;
+  const int t = blockIdx.y, tid = threadIdx.x;
+  const Tok tk = token_geometry(a, t, nullptr, false);
+  const int64_t j0 = (int64_t)blockIdx.x * kHistChunk;
+  const int64_t j1 = min((int64_t)tk.nb, j0 + kHistChunk);
+  for (int i = tid; i < kHistBins; i += 256) s_hist[i] = 0u;
+  if (tid == 0) s_ntouched = 0u;
+  __syncthreads();
+  grid_dep_wait();
+  grid_dep_launch();
+  const float* srow = scores + (int64_t)t * a.max_blocks;
+  for (int64_t j = j0 + tid; j < j1; j += 256) {
+    const unsigned bin = score_key(__ldcg(srow + j)) >> (32 - kHistBits);
+    if (atomicAdd(&s_hist[bin], 1u) == 0u) s_touched[atomicAdd(&s_ntouched, 1u)] = (unsigned short)bin;
+  }
+  __syncthreads();
+  unsigned* gh = hist_of(ws, t);
+  const unsigned nt = s_ntouched;
+  for (unsigned i = tid; i < nt; i += 256) {
+    const unsigned b = s_touched[i];
+    atomicAdd(gh + b, s_hist[b]);
   }
 }
 
@@ -936,13 +1207,35 @@ cudaError_t index_setup(int* sms) {
     e = cudaFuncSetAttribute(k_select, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)(sizeof(int32_t) * (kSelSlots + kSelList)));
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_score_tc<16, 32, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)TcShape<16, 32>::kSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_score_tc<16, 32, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)TcShape<16, 32>::kSmem);
+    if (e != cudaSuccess) return e;
     sm_count[dev] = n;
   }
   *sms = sm_count[dev];
   return cudaSuccess;
 }
 
+// Launches the token-tiled scores on the tensor cores: 16 tokens per CTA, 32
+// dims per gather, 2 CTAs per SM, the row tiles dealt to about 2 CTAs per SM.
+template <bool kTopk>
+cudaError_t launch_tiled(const IndexArgs& a, float* scores, unsigned* err, cudaStream_t stream, int sms) {
+  const int64_t row_tiles = ceil_div(a.max_blocks, 128);
+  const int64_t tt = ceil_div(a.n_tokens, 16);
+  const int64_t x = std::min<int64_t>(row_tiles, std::max<int64_t>(1, 2 * (int64_t)sms / tt));
+  return launch_pdl(k_score_tc<16, 32, kTopk>, dim3((unsigned)std::max<int64_t>(x, 1), (unsigned)tt), dim3(256),
+                    TcShape<16, 32>::kSmem, stream, 1, a, scores, err);
+}
+
 }  // namespace
+
+// Up to 8 tokens, the per-token pass is faster even when they share a
+// sequence: their CTAs read the same rows at about the same time and L2
+// serves the repeats.
+bool index_tiled(int n_tokens, int n_seq) { return n_tokens > 8 && n_tokens >= 2 * n_seq; }
 
 int64_t index_max_blocks_limit() { return (int64_t)kSelCluster * kSelMaxWords * 32; }
 
@@ -961,6 +1254,7 @@ cudaError_t launch_index_scores(const IndexArgs& a, float* scores, unsigned* err
   int sms = 0;
   cudaError_t e = index_setup(&sms);
   if (e != cudaSuccess) return e;
+  if (index_tiled(a.n_tokens, a.n_seq)) return launch_tiled<false>(a, scores, err, stream, sms);
   const int chunk = score_chunk(a.n_tokens, a.max_blocks, sms);
   const dim3 grid((unsigned)ceil_div(a.max_blocks, chunk), (unsigned)a.n_tokens);
   return launch_pdl(k_score<false>, grid, dim3(kScoreThreads), kScoreSmem, stream, 1, a, (void*)nullptr, scores,
@@ -977,12 +1271,26 @@ cudaError_t launch_index_topk(const IndexArgs& a, int32_t* cells, int32_t* count
   IndexArgs b = a;
   b.max_blocks = a.max_blocks > 0 ? a.max_blocks : 1;
   float* sc = scores_of(ws, a.max_tokens);
-  const int chunk = score_chunk(a.n_tokens, b.max_blocks, sms);
-  const dim3 g1((unsigned)ceil_div(b.max_blocks, chunk), (unsigned)a.n_tokens);
-  prof_before(kKScore, stream);
-  e = launch_pdl(k_score<true>, g1, dim3(kScoreThreads), kScoreSmem, stream, 1, b, ws, sc, chunk, err);
-  prof_after(kKScore, stream);
-  if (e != cudaSuccess) return e;
+  if (index_tiled(a.n_tokens, a.n_seq)) {
+    // tokens sharing sequences: rows read once per token tile, then the
+    // histogram from the written scores
+    prof_before(kKScore, stream);
+    e = launch_tiled<true>(b, sc, err, stream, sms);
+    prof_after(kKScore, stream);
+    if (e != cudaSuccess) return e;
+    prof_before(kKHist, stream);
+    const dim3 gh((unsigned)ceil_div(b.max_blocks, kHistChunk), (unsigned)a.n_tokens);
+    e = launch_pdl(k_hist, gh, dim3(256), 0, stream, 1, b, ws, (const float*)sc);
+    prof_after(kKHist, stream);
+    if (e != cudaSuccess) return e;
+  } else {
+    const int chunk = score_chunk(a.n_tokens, b.max_blocks, sms);
+    const dim3 g1((unsigned)ceil_div(b.max_blocks, chunk), (unsigned)a.n_tokens);
+    prof_before(kKScore, stream);
+    e = launch_pdl(k_score<true>, g1, dim3(kScoreThreads), kScoreSmem, stream, 1, b, ws, sc, chunk, err);
+    prof_after(kKScore, stream);
+    if (e != cudaSuccess) return e;
+  }
   prof_before(kKFinal, stream);
   const int nc = select_cluster(a.n_tokens, b.max_blocks, sms);
   e = launch_pdl(k_select, dim3((unsigned)nc, (unsigned)a.n_tokens), dim3(kSelThreads), slot_bytes, stream,

@@ -168,7 +168,7 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 
 // ------------------------------------------------------ measurement hook
 // Kernel ids of qsa_profile_kernel (include/qsa.h).
-enum KernelId : int { kKPool = 0, kKScore = 1, kKReserved = 2, kKFinal = 3, kKAttn = 4, kKAppend = 5,
+enum KernelId : int { kKPool = 0, kKScore = 1, kKHist = 2, kKFinal = 3, kKAttn = 4, kKAppend = 5,
                       kNumKernels = 6 };
 struct ProfileHook {
   cudaEvent_t before[kNumKernels];
@@ -217,6 +217,9 @@ struct IndexArgs {
 };
 
 size_t index_workspace_bytes(int max_tokens, int64_t max_blocks);
+// Whether qsa_index_topk / qsa_index_scores score with the token-tiled kernel
+// (tokens share sequences: more than 8 tokens and 2 per sequence on average).
+bool index_tiled(int n_tokens, int n_seq);
 // Largest max_blocks the selection kernel supports (per-CTA bitmap capacity).
 int64_t index_max_blocks_limit();
 // Byte range of the workspace that must be zero when a call starts.

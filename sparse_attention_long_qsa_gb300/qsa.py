@@ -28,10 +28,10 @@ EXPORTS = ("qsa_config_init", "qsa_cells_per_token", "qsa_pool_update", "qsa_ind
            "qsa_index_topk_workspace_size", "qsa_index_topk", "qsa_index_topk_noalloc",
            "qsa_sparse_attn_workspace_size",
            "qsa_sparse_attn", "qsa_kv_append", "qsa_blocks_dirty", "qsa_debug_check", "qsa_profile_kernel",
-           "qsa_status_string")
+           "qsa_index_topk_kernels", "qsa_status_string")
 
 # Kernel ids of qsa_profile_kernel.
-KERNELS = {"pool": 0, "score": 1, "select": 3, "attn": 4, "append": 5}
+KERNELS = {"pool": 0, "score": 1, "hist": 2, "select": 3, "attn": 4, "append": 5}
 
 
 class QSAError(RuntimeError):
@@ -95,6 +95,8 @@ def lib():
     L.qsa_debug_check.restype = _I32
     L.qsa_profile_kernel.argtypes = [_I32, _P, _P]
     L.qsa_profile_kernel.restype = _I32
+    L.qsa_index_topk_kernels.argtypes = [_I32, _I32]
+    L.qsa_index_topk_kernels.restype = ctypes.c_uint32
     L.qsa_status_string.argtypes = [_I32]
     L.qsa_status_string.restype = ctypes.c_char_p
     _lib = L
@@ -275,9 +277,16 @@ def blocks_dirty(old_tbl: np.ndarray, new_tbl: np.ndarray, pad_pow2_min: int = 4
     return out[:n.value]
 
 
+def index_topk_kernels(n_tokens: int, n_seq: int) -> list:
+    """Names of the kernels one index_topk call of n_tokens tokens over n_seq
+    sequences launches (token-tiled scoring adds "hist")."""
+    m = int(lib().qsa_index_topk_kernels(int(n_tokens), int(n_seq)))
+    return [k for k, v in KERNELS.items() if (m >> v) & 1]
+
+
 def profile_kernel(kernel: str, before=None, after=None):
     """Record torch.cuda.Event `before`/`after` around each launch of the
-    named kernel (pool, score, filter, final, attn, combine); None clears."""
+    named kernel (see KERNELS); None clears."""
     for ev in (before, after):
         if ev is not None and not ev.cuda_event:
             ev.record()   # torch creates the CUDA event on first record

@@ -142,3 +142,18 @@ def test_kv_append_host_checks(L):
     assert call(a16=0) == -1                    # no sequence
     assert call(a21=f) == -1                    # re-pooling needs slot_block_idx and norm_w
     assert L.qsa_kv_append(ctypes.byref(qsa.config(kv_type=7)), *base[1:]) == -1
+
+
+def test_index_topk_kernel_plan(L):
+    """Token-tiled scoring (score + hist + select) exactly when tokens share
+    sequences: n_tokens > 8 and n_tokens >= 2 * n_seq."""
+    plain, tiled = ["score", "select"], ["score", "hist", "select"]
+    assert qsa.index_topk_kernels(1, 1) == plain
+    assert qsa.index_topk_kernels(5, 5) == plain
+    assert qsa.index_topk_kernels(5, 1) == plain
+    assert qsa.index_topk_kernels(8, 1) == plain
+    assert qsa.index_topk_kernels(9, 5) == plain
+    assert qsa.index_topk_kernels(9, 1) == tiled
+    assert qsa.index_topk_kernels(10, 5) == tiled
+    assert qsa.index_topk_kernels(512, 1) == tiled
+    assert L.qsa_index_topk_kernels(0, 1) == 0

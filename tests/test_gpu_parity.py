@@ -98,6 +98,18 @@ def test_multi_token_select_cluster_sizes(T):
         assert np.all(res["cells"][t, :cnt] <= st.tok_pos[t])
 
 
+@pytest.mark.parametrize("n_seq,tps,kv_type", [(3, 3, "f16"), (2, 6, "q8_0"), (2, 12, "f16")])
+def test_batched_verify_several_sequences(n_seq, tps, kv_type):
+    """Several tokens per sequence for several sequences (token-tiled scoring
+    with more than one sequence in a token tile, shuffled slots and cells)."""
+    wl = make_workload(n_seq=n_seq, prompt_len=[4001 + 997 * s for s in range(n_seq)], n_steps=2,
+                       tokens_per_step=tps, seed=40 + tps, shuffled=True, kv_type=kv_type)
+    assert "hist" in qsa.index_topk_kernels(n_seq * tps, n_seq)
+    run = Runner(wl)
+    for i in range(2):
+        check_step(run, i)
+
+
 @pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 7, 2048, 2050, 2051, 2052, 2055])
 def test_degenerate_and_budget_edges(n):
     """n <= top_k + r - 1: dense causal attention over all n cells; past it
