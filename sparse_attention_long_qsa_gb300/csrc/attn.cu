@@ -68,13 +68,41 @@ constexpr uint32_t kOffXS = kOffXV + kOvf * 512;    // fp32 [kOvf][8] scores / p
 constexpr uint32_t kOffXO = kOffXS + kOvf * 8 * 4;  // fp32 [8][256] partial output
 constexpr uint32_t kOffXM = kOffXO + 8 * 256 * 4;   // fp32 [8] max, [8] sum
 constexpr uint32_t kOffXC = kOffXM + 64;            // int [kOvf] cells
-constexpr uint32_t kOffW = kOffXC + kOvf * 4;        // fp32 [16][8] combine weights, [8] denominators
-constexpr uint32_t kSmemBytes = kOffW + (kMaxCluster * 8 + 8) * 4 + 1024;   // + alignment slack
+constexpr uint32_t kSmemBytes = kOffXC + kOvf * 4 + 1024;   // + alignment slack
 
 // Instruction descriptor, kind::f16: fp32 accumulate, fp16 A and B,
 // M = 128, N = 16; A K-major (QK) or MN-major (PV), B K-major.
 constexpr uint32_t kIdescQK = (1u << 4) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
 constexpr uint32_t kIdescPV = kIdescQK | (1u << 15);
+
+// Reduces v[0..7] over the 32 lanes of a warp by a reduce-scatter (9
+// shuffles for the 8 values): every lane returns the total of value
+// (lane >> 2).
+template <class Op>
+__device__ __forceinline__ float warp_reduce8(const float (&v)[8], int lane, Op op) {
+  const bool b4 = (lane & 16) != 0, b3 = (lane & 8) != 0, b2 = (lane & 4) != 0;
+  float x4[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float keep = b4 ? v[i + 4] : v[i], send = b4 ? v[i] : v[i + 4];
+    x4[i] = op(keep, __shfl_xor_sync(kFull, send, 16));
+  }
+  float x2[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float keep = b3 ? x4[i + 2] : x4[i], send = b3 ? x4[i] : x4[i + 2];
+    x2[i] = op(keep, __shfl_xor_sync(kFull, send, 8));
+  }
+  float x = op(b2 ? x2[1] : x2[0], __shfl_xor_sync(kFull, b2 ? x2[0] : x2[1], 4));
+  x = op(x, __shfl_xor_sync(kFull, x, 2));
+  return op(x, __shfl_xor_sync(kFull, x, 1));
+}
+struct OpMax {
+  __device__ __forceinline__ float operator()(float a, float b) const { return fmaxf(a, b); }
+};
+struct OpAdd {
+  __device__ __forceinline__ float operator()(float a, float b) const { return a + b; }
+};
 
 // Barrier among the 128 threads of warps 0-3 (id 1) or of warps 4-7 (id 2).
 __device__ __forceinline__ void bar_half(int id) { asm volatile("bar.sync %0, 128;\n" ::"r"(id) : "memory"); }
@@ -184,6 +212,24 @@ k_attn_tc(const AttnArgs a, unsigned* err) {
   const int loop_tiles = use_ovf ? (int)NC : n_tiles;
   const bool my_ovf = use_ovf && rank == 0;
 
+  // the overflow cells' ids load with the first tile's (warps 4-7 of CTA 0)
+  int* xc = reinterpret_cast<int*>(base + kOffXC);
+  if (my_ovf && warp >= 4 && tid - 128 < kOvf) {
+    const int tx = tid - 128;
+    int c = -1;
+    if (tx < ovf_n) {
+      c = crow[(int)NC * kTile + tx];
+      if (c < 0 || c >= a.n_cells) {
+        atomicOr(err, kErrCell);
+        c = -1;
+      }
+    }
+    xc[tx] = c;
+  }
+  // fp16: with overflow cells, warps 0-3 gather the MMA tile alone while warps
+  // 4-7 gather and attend the overflow cells from the start
+  const bool split = !kQ8 && my_ovf;
+
   for (int tile = (int)rank; tile < loop_tiles; tile += (int)NC) {
     const int c0 = tile * kTile;
     const int nv = min(kTile, cnt - c0);
@@ -198,20 +244,27 @@ k_attn_tc(const AttnArgs a, unsigned* err) {
       }
       scell[tid] = c;
     }
-    __syncthreads();
+    if (split) {
+      if (warp < 4) bar_half(1);
+    } else {
+      __syncthreads();
+    }
     QSA_TS(attn, 3 + 10 * (tile / (int)NC));
 
     // 1. gather K and V rows of KV head g into the swizzled tiles
     if constexpr (!kQ8) {
       const __half* kb = static_cast<const __half*>(a.k_cache);
       const __half* vb = static_cast<const __half*>(a.v_cache);
-      for (int i = tid; i < kTile * 32; i += kThreads) {
-        const int row = i >> 5, c16 = i & 31, c = scell[row];
-        const int64_t off = ((int64_t)(c < 0 ? 0 : c) * G + g) * kHeadDim + c16 * 8;
-        cp_async16(sK + sw128(kTile, row, c16), kb + off, c >= 0);
-        cp_async16(sV + sw128(kTile, row, c16), vb + off, c >= 0);
+      if (!split || warp < 4) {
+        const int nthr = split ? 128 : kThreads;
+        for (int i = tid; i < kTile * 32; i += nthr) {
+          const int row = i >> 5, c16 = i & 31, c = scell[row];
+          const int64_t off = ((int64_t)(c < 0 ? 0 : c) * G + g) * kHeadDim + c16 * 8;
+          cp_async16(sK + sw128(kTile, row, c16), kb + off, c >= 0);
+          cp_async16(sV + sw128(kTile, row, c16), vb + off, c >= 0);
+        }
+        asm volatile("cp.async.wait_all;\n" ::: "memory");
       }
-      asm volatile("cp.async.wait_all;\n" ::: "memory");
     } else {
       // thread -> (row, half): 128 int8 of K and of V plus their 4 scales each
       const int8_t* kq = static_cast<const int8_t*>(a.k_cache);
@@ -253,7 +306,11 @@ k_attn_tc(const AttnArgs a, unsigned* err) {
     }
     fence_async_smem();
     tc_fence_before();
-    __syncthreads();
+    if (split) {
+      if (warp < 4) bar_half(1);
+    } else {
+      __syncthreads();
+    }
     tc_fence_after();
     QSA_TS(attn, 4 + 10 * (tile / (int)NC));
 
@@ -273,45 +330,42 @@ k_attn_tc(const AttnArgs a, unsigned* err) {
       tc_fence_after();
       QSA_TS(attn, 5 + 10 * (tile / (int)NC));
 
-      // 3. tile softmax statistics and P (one cell per thread)
-      float sv[kGqa], tmax[kGqa], tsum[kGqa];
+      // 3. tile softmax statistics and P (one cell per thread); per-warp
+      // statistics by reduce-scatter, lanes 4k hold head k's
+      float sv[kGqa], tmax[kGqa], tsum[kGqa], pe[kGqa];
       tmem_ld8(tmem + ((uint32_t)(32 * warp) << 16) + 0, sv);
+      if (tile < (int)NC) QSA_TS(attn, 8);
       const int cell = 32 * warp + lane;
       const bool valid = cell < nv && scell[cell] >= 0;
 #pragma unroll
-      for (int h = 0; h < kGqa; ++h) {
-        sv[h] = valid ? sv[h] * scale2 : -INFINITY;
-        float m = sv[h];
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
-        if (lane == 0) sred[warp * 8 + h] = m;
+      for (int h = 0; h < kGqa; ++h) sv[h] = valid ? sv[h] * scale2 : -INFINITY;
+      {
+        const float m = warp_reduce8(sv, lane, OpMax());
+        if ((lane & 3) == 0) sred[warp * 8 + (lane >> 2)] = m;
       }
       bar_half(1);
+      if (tile < (int)NC) QSA_TS(attn, 9);
+#pragma unroll
+      for (int h = 0; h < kGqa; ++h) tmax[h] = fmaxf(fmaxf(sred[h], sred[8 + h]), fmaxf(sred[16 + h], sred[24 + h]));
 #pragma unroll
       for (int h = 0; h < kGqa; ++h) {
-        tmax[h] = fmaxf(fmaxf(sred[h], sred[8 + h]), fmaxf(sred[16 + h], sred[24 + h]));
         const float p = (tmax[h] == -INFINITY) ? 0.f : exp2f(sv[h] - tmax[h]);
         const __half ph = __float2half_rn(p);
-        // the sum uses the rounded p the MMA sees
-        float e = __half2float(ph);
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) e += __shfl_xor_sync(kFull, e, o);
-        if (lane == 0) sred[32 + warp * 8 + h] = e;
+        pe[h] = __half2float(ph);   // the sum uses the rounded p the MMA sees
         // P row h, column `cell`: atom cell/64, chunk (cell%64)/8, element cell%8
         const uint32_t off = (uint32_t)(cell >> 6) * (16 * 128) + h * 128 +
                              ((((uint32_t)(cell & 63) >> 3) ^ (uint32_t)(h & 7)) << 4) + (cell & 7) * 2;
         *reinterpret_cast<__half*>(base + kOffP + off) = ph;
       }
+      if (tile < (int)NC) QSA_TS(attn, 10);
       fence_async_smem();
       tc_fence_before();
       bar_half(1);
       tc_fence_after();
-#pragma unroll
-      for (int h = 0; h < kGqa; ++h)
-        tsum[h] = (sred[32 + h] + sred[40 + h]) + (sred[48 + h] + sred[56 + h]);
       QSA_TS(attn, 6 + 10 * (tile / (int)NC));
 
-      // 4. O^T[dim][head] = V^T . P^T, two halves of 128 dims
+      // 4. O^T[dim][head] = V^T . P^T, two halves of 128 dims; the tile's
+      // row sums are reduced while the MMAs run
       if (tid == 0) {
 #pragma unroll
         for (int mh = 0; mh < 2; ++mh) {
@@ -324,6 +378,14 @@ k_attn_tc(const AttnArgs a, unsigned* err) {
         }
         mma_commit(bar);
       }
+      {
+        const float e = warp_reduce8(pe, lane, OpAdd());
+        if ((lane & 3) == 0) sred[32 + warp * 8 + (lane >> 2)] = e;
+      }
+      bar_half(1);
+#pragma unroll
+      for (int h = 0; h < kGqa; ++h)
+        tsum[h] = (sred[32 + h] + sred[40 + h]) + (sred[48 + h] + sred[56 + h]);
       if (!mbar_wait(bar, phase)) timed_out = true;
       phase ^= 1;
       tc_fence_after();
@@ -344,23 +406,12 @@ k_attn_tc(const AttnArgs a, unsigned* err) {
         run_m[h] = mn;
       }
     } else if (my_ovf && tile == (int)rank) {
-      // Overflow cells on warps 4-7 (128 threads, tx = 0..127)
+      // Overflow cells on warps 4-7 (128 threads, tx = 0..127); their ids
+      // were loaded before the tile loop
       const int tx = tid - 128;
-      int* xc = reinterpret_cast<int*>(base + kOffXC);
       float* xs = reinterpret_cast<float*>(base + kOffXS);
       float* xo = reinterpret_cast<float*>(base + kOffXO);
       float* xm = reinterpret_cast<float*>(base + kOffXM);
-      if (tx < kOvf) {
-        int c = -1;
-        if (tx < ovf_n) {
-          c = crow[(int)NC * kTile + tx];
-          if (c < 0 || c >= a.n_cells) {
-            atomicOr(err, kErrCell);
-            c = -1;
-          }
-        }
-        xc[tx] = c;
-      }
       bar_half(2);
       // gather the rows as plain fp16 [cell][256]
       if constexpr (!kQ8) {
@@ -466,6 +517,7 @@ k_attn_tc(const AttnArgs a, unsigned* err) {
         }
       }
     }
+    if (tile < (int)NC) QSA_TS(attn, 12);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -490,7 +542,8 @@ k_attn_tc(const AttnArgs a, unsigned* err) {
 
   // ---- push this CTA's partial to the CTAs that own each dim range, then
   // every CTA reduces its range from its own shared memory
-  const int dpc = (kHeadDim + (int)NC - 1) / (int)NC;   // dims per owner
+  QSA_TS(attn, 11);
+  const int dpc = (kHeadDim + (int)NC - 1) / (int)NC;   // dims per owner (a multiple of 4)
   if (warp < 4) {
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
@@ -502,40 +555,31 @@ k_attn_tc(const AttnArgs a, unsigned* err) {
     }
   }
   if (tid < (int)NC) {
-#pragma unroll
-    for (int h = 0; h < kGqa; ++h) {
-      st_dsmem_f32(dsmem_addr(&sml[(int)rank * 16 + h], (uint32_t)tid), run_m[h]);
-      st_dsmem_f32(dsmem_addr(&sml[(int)rank * 16 + 8 + h], (uint32_t)tid), run_l[h]);
-    }
+    const uint32_t dst = dsmem_addr(&sml[(int)rank * 16], (uint32_t)tid);
+    st_dsmem_f32x4(dst, make_float4(run_m[0], run_m[1], run_m[2], run_m[3]));
+    st_dsmem_f32x4(dst + 16, make_float4(run_m[4], run_m[5], run_m[6], run_m[7]));
+    st_dsmem_f32x4(dst + 32, make_float4(run_l[0], run_l[1], run_l[2], run_l[3]));
+    st_dsmem_f32x4(dst + 48, make_float4(run_l[4], run_l[5], run_l[6], run_l[7]));
   }
   QSA_TS(attn, 25);
   cluster_sync();   // all pushes have landed; nobody touches a peer after this
   QSA_TS(attn, 26);
   {
-    // per (partial, head) weight exp2(m_p - max_p m_p) once, then the
-    // denominators, then every output dim is a weighted sum of the partials
-    float* sw = reinterpret_cast<float*>(base + kOffW);           // [NC][8] weights, then [8] denominators
-    if (tid < (int)NC * kGqa) {
-      const int p = tid / kGqa, h = tid - p * kGqa;
-      float mx = -INFINITY;
-      for (int q = 0; q < (int)NC; ++q) mx = fmaxf(mx, sml[q * 16 + h]);
-      const float mp = sml[p * 16 + h];
-      sw[tid] = (mp == -INFINITY || mx == -INFINITY) ? 0.f : exp2f(mp - mx);
-    }
-    __syncthreads();
-    if (tid < kGqa) {
-      float den = 0.f;
-      for (int p = 0; p < (int)NC; ++p) den = fmaf(sw[p * kGqa + tid], sml[p * 16 + 8 + tid], den);
-      sw[kMaxCluster * kGqa + tid] = den;
-    }
-    __syncthreads();
+    // output (head h, dim d0 + e) = sum_p w_p o_p / sum_p w_p l_p with
+    // w_p = exp2(m_p - max_p m_p), one output per thread
     const int d0 = (int)rank * dpc;
     for (int i = tid; i < kGqa * dpc; i += kThreads) {
       const int h = i / dpc, e = i % dpc, d = d0 + e;
       if (d >= kHeadDim) continue;
-      float num = 0.f;
-      for (int p = 0; p < (int)NC; ++p) num = fmaf(sw[p * kGqa + h], so[(p * kGqa + h) * dpc + e], num);
-      const float den = sw[kMaxCluster * kGqa + h];
+      float mx = -INFINITY;
+      for (int p = 0; p < (int)NC; ++p) mx = fmaxf(mx, sml[p * 16 + h]);
+      float num = 0.f, den = 0.f;
+      for (int p = 0; p < (int)NC; ++p) {
+        const float mp = sml[p * 16 + h];
+        const float w = (mp == -INFINITY) ? 0.f : exp2f(mp - mx);
+        den = fmaf(w, sml[p * 16 + 8 + h], den);
+        num = fmaf(w, so[(p * kGqa + h) * dpc + e], num);
+      }
       a.out[((int64_t)t * Hq + g * kGqa + h) * kHeadDim + d] = den > 0.f ? num / den : 0.f;
     }
   }

@@ -819,6 +819,7 @@ k_select(const IndexArgs a, void* ws, const float* __restrict__ scores,
       __syncthreads();
       for (unsigned i = tid; i < nall; i += kSelThreads) atomicAdd(&hh[(unsigned)(sm.allc[i] >> 48) & 255u], 1u);
       __syncthreads();
+      QSA_TS(index, 24);
       if (warp == 0) {
         unsigned hv[8], sum = 0;
 #pragma unroll
@@ -845,6 +846,7 @@ k_select(const IndexArgs a, void* ws, const float* __restrict__ scores,
       }
       if (tid == 0) sm.ncut = 0u;
       __syncthreads();
+      QSA_TS(index, 25);
       const unsigned dstar = (unsigned)sm.digit;
       need -= sm.above;
       // keys above the cut-off digit are chosen; the digit's own keys (a few)
@@ -861,6 +863,7 @@ k_select(const IndexArgs a, void* ws, const float* __restrict__ scores,
         }
       }
       __syncthreads();
+      QSA_TS(index, 26);
       const unsigned ncut = sm.ncut;
       for (unsigned i = tid; i < ncut; i += kSelThreads) {
         const unsigned long long c = sm.cand[i];
@@ -873,6 +876,7 @@ k_select(const IndexArgs a, void* ws, const float* __restrict__ scores,
       }
     }
     __syncthreads();
+    QSA_TS(index, 27);
     // ordered list of the chosen blocks (block prefix over the bitmap words)
     const int W = (int)ceil_div(nb, 32);
     const int wq = (int)ceil_div(W, kSelThreads);
@@ -881,6 +885,7 @@ k_select(const IndexArgs a, void* ws, const float* __restrict__ scores,
     for (int w = q0; w < q1; ++w) mine += __popc(sm.bitmap[w]);
     unsigned total_sel = 0;
     unsigned k = block_prefix_exclusive(mine, sm.warp_tmp, &total_sel);
+    QSA_TS(index, 28);
     if (tid == 0) sm.sel = total_sel;
     for (int w = q0; w < q1; ++w) {
       unsigned bits = sm.bitmap[w];
