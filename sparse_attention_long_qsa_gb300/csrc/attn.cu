@@ -128,7 +128,10 @@ __device__ __forceinline__ uint4 dq8(uint2 raw, __half2 s2) {
   return o;
 }
 
-template <bool kQ8>
+// kPipe (fp16 only): the launch gives CTAs several tiles each; the pipelined
+// tile loop is compiled only into this variant, so the one-tile decode
+// variant keeps its code small (it runs from a cold instruction cache).
+template <bool kQ8, bool kPipe>
 __global__ void __launch_bounds__(kThreads, 1)
 k_attn_tc(const AttnArgs a, unsigned* err) {
   extern __shared__ unsigned char smem_raw[];
@@ -230,6 +233,179 @@ k_attn_tc(const AttnArgs a, unsigned* err) {
   // 4-7 gather and attend the overflow cells from the start
   const bool split = !kQ8 && my_ovf;
 
+  // Per-tile steps of warps 0-3 (tile: for the phase stamps only)
+  float tmax[kGqa], pe[kGqa];
+  auto qk_mma = [&](int tile) {
+    // 2. S[cell][head] = K . Q^T
+    if (tid == 0) {
+#pragma unroll
+      for (int kk = 0; kk < 16; ++kk) {
+        const uint64_t ad = smem_desc(sK + (kk >> 2) * (kTile * 128) + (kk & 3) * 32, 16, 1024);
+        const uint64_t bd = smem_desc(sQ + (kk >> 2) * (16 * 128) + (kk & 3) * 32, 16, 1024);
+        mma_f16(tmem, ad, bd, kIdescQK, kk > 0);
+      }
+      mma_commit(bar);
+    }
+    if (!mbar_wait(bar, phase)) timed_out = true;
+    phase ^= 1;
+    tc_fence_after();
+    QSA_TS(attn, 5 + 10 * (tile / (int)NC));
+  };
+  auto softmax_p = [&](int tile, const int* cells, int nv) {
+    // 3. tile softmax statistics and P (one cell per thread); per-warp
+    // statistics by reduce-scatter, lanes 4k hold head k's
+    float sv[kGqa];
+    tmem_ld8(tmem + ((uint32_t)(32 * warp) << 16) + 0, sv);
+    if (tile < (int)NC) QSA_TS(attn, 8);
+    const int cell = 32 * warp + lane;
+    const bool valid = cell < nv && cells[cell] >= 0;
+#pragma unroll
+    for (int h = 0; h < kGqa; ++h) sv[h] = valid ? sv[h] * scale2 : -INFINITY;
+    {
+      const float m = warp_reduce8(sv, lane, OpMax());
+      if ((lane & 3) == 0) sred[warp * 8 + (lane >> 2)] = m;
+    }
+    bar_half(1);
+    if (tile < (int)NC) QSA_TS(attn, 9);
+#pragma unroll
+    for (int h = 0; h < kGqa; ++h) tmax[h] = fmaxf(fmaxf(sred[h], sred[8 + h]), fmaxf(sred[16 + h], sred[24 + h]));
+#pragma unroll
+    for (int h = 0; h < kGqa; ++h) {
+      const float p = (tmax[h] == -INFINITY) ? 0.f : exp2f(sv[h] - tmax[h]);
+      const __half ph = __float2half_rn(p);
+      pe[h] = __half2float(ph);   // the sum uses the rounded p the MMA sees
+      // P row h, column `cell`: atom cell/64, chunk (cell%64)/8, element cell%8
+      const uint32_t off = (uint32_t)(cell >> 6) * (16 * 128) + h * 128 +
+                           ((((uint32_t)(cell & 63) >> 3) ^ (uint32_t)(h & 7)) << 4) + (cell & 7) * 2;
+      *reinterpret_cast<__half*>(base + kOffP + off) = ph;
+    }
+    if (tile < (int)NC) QSA_TS(attn, 10);
+    fence_async_smem();
+    tc_fence_before();
+    bar_half(1);
+    tc_fence_after();
+    QSA_TS(attn, 6 + 10 * (tile / (int)NC));
+  };
+  auto pv_merge = [&](int tile) {
+    // 4. O^T[dim][head] = V^T . P^T, two halves of 128 dims; the tile's
+    // row sums are reduced while the MMAs run
+    if (tid == 0) {
+#pragma unroll
+      for (int mh = 0; mh < 2; ++mh) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t ad = smem_desc(sV + mh * 2 * (kTile * 128) + kk * 2048, kTile * 128, 1024);
+          const uint64_t bd = smem_desc(sP + (kk >> 2) * (16 * 128) + (kk & 3) * 32, 16, 1024);
+          mma_f16(tmem + 16 + 16 * mh, ad, bd, kIdescPV, kk > 0);
+        }
+      }
+      mma_commit(bar);
+    }
+    {
+      const float e = warp_reduce8(pe, lane, OpAdd());
+      if ((lane & 3) == 0) sred[32 + warp * 8 + (lane >> 2)] = e;
+    }
+    bar_half(1);
+    float tsum[kGqa];
+#pragma unroll
+    for (int h = 0; h < kGqa; ++h)
+      tsum[h] = (sred[32 + h] + sred[40 + h]) + (sred[48 + h] + sred[56 + h]);
+    if (!mbar_wait(bar, phase)) timed_out = true;
+    phase ^= 1;
+    tc_fence_after();
+    QSA_TS(attn, 7 + 10 * (tile / (int)NC));
+
+    // 5. merge the tile into the running state (dims 32w+lane and +128)
+    float o0[8], o1[8];
+    tmem_ld8(tmem + ((uint32_t)(32 * warp) << 16) + 16, o0);
+    tmem_ld8(tmem + ((uint32_t)(32 * warp) << 16) + 32, o1);
+#pragma unroll
+    for (int h = 0; h < kGqa; ++h) {
+      const float mn = fmaxf(run_m[h], tmax[h]);
+      const float fa = (run_m[h] == -INFINITY) ? 0.f : exp2f(run_m[h] - mn);
+      const float fb = (tmax[h] == -INFINITY) ? 0.f : exp2f(tmax[h] - mn);
+      acc[0][h] = acc[0][h] * fa + o0[h] * fb;
+      acc[1][h] = acc[1][h] * fa + o1[h] * fb;
+      run_l[h] = run_l[h] * fa + tsum[h] * fb;
+      run_m[h] = mn;
+    }
+  };
+
+  // fp16 with several tiles per CTA (and no overflow cells): the next tile's
+  // K rows are gathered while this tile's softmax and P.V run, its V rows
+  // while the next Q.K^T runs (one cp.async group for K and one for V per
+  // tile; the next tile's cells go to a second list).
+  const bool pipe = kPipe && !kQ8 && !use_ovf && (int)rank + (int)NC < loop_tiles;
+  if constexpr (kPipe && !kQ8) {
+    if (pipe) {
+      const __half* kb = static_cast<const __half*>(a.k_cache);
+      const __half* vb = static_cast<const __half*>(a.v_cache);
+      int* cur = scell;
+      int* nxt = reinterpret_cast<int*>(base + kOffXS);   // free without overflow cells
+      auto load_cells = [&](int tile, int* dst, int tx) {
+        const int c0 = tile * kTile, nvt = min(kTile, cnt - c0);
+        int c = -1;
+        if (tx < nvt) {
+          c = (tile == (int)rank) ? cfirst : crow[c0 + tx];
+          if (c < 0 || c >= a.n_cells) {
+            atomicOr(err, kErrCell);
+            c = -1;
+          }
+        }
+        dst[tx] = c;
+      };
+      auto issue = [&](uint32_t sdst, const __half* src, const int* cells) {
+        for (int i = tid; i < kTile * 32; i += kThreads) {
+          const int row = i >> 5, c16 = i & 31, c = cells[row];
+          const int64_t off = ((int64_t)(c < 0 ? 0 : c) * G + g) * kHeadDim + c16 * 8;
+          cp_async16(sdst + sw128(kTile, row, c16), src + off, c >= 0);
+        }
+        asm volatile("cp.async.commit_group;\n" ::: "memory");
+      };
+      if (tid < kTile) load_cells((int)rank, cur, tid);
+      __syncthreads();
+      issue(sK, kb, cur);
+      issue(sV, vb, cur);
+      for (int tile = (int)rank; tile < loop_tiles; tile += (int)NC) {
+        const int nv = min(kTile, cnt - tile * kTile);
+        const bool has_next = tile + (int)NC < loop_tiles;
+        asm volatile("cp.async.wait_group 1;\n" ::: "memory");   // this tile's K
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (warp < 4) {
+          qk_mma(tile);
+        } else if (has_next) {
+          load_cells(tile + (int)NC, nxt, tid - 128);
+        }
+        tc_fence_before();
+        __syncthreads();   // K tile free, next cells listed
+        tc_fence_after();
+        if (has_next) issue(sK, kb, nxt);
+        if (warp < 4) softmax_p(tile, cur, nv);
+        if (has_next) {
+          asm volatile("cp.async.wait_group 1;\n" ::: "memory");   // this tile's V
+        } else {
+          asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (warp < 4) pv_merge(tile);
+        tc_fence_before();
+        __syncthreads();   // V tile free, tensor memory read
+        tc_fence_after();
+        if (has_next) issue(sV, vb, nxt);
+        int* sw = cur;
+        cur = nxt;
+        nxt = sw;
+      }
+    }
+  }
+
+  if (!pipe)
   for (int tile = (int)rank; tile < loop_tiles; tile += (int)NC) {
     const int c0 = tile * kTile;
     const int nv = min(kTile, cnt - c0);
@@ -315,96 +491,9 @@ k_attn_tc(const AttnArgs a, unsigned* err) {
     QSA_TS(attn, 4 + 10 * (tile / (int)NC));
 
     if (warp < 4) {
-      // 2. S[cell][head] = K . Q^T
-      if (tid == 0) {
-#pragma unroll
-        for (int kk = 0; kk < 16; ++kk) {
-          const uint64_t ad = smem_desc(sK + (kk >> 2) * (kTile * 128) + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = smem_desc(sQ + (kk >> 2) * (16 * 128) + (kk & 3) * 32, 16, 1024);
-          mma_f16(tmem, ad, bd, kIdescQK, kk > 0);
-        }
-        mma_commit(bar);
-      }
-      if (!mbar_wait(bar, phase)) timed_out = true;
-      phase ^= 1;
-      tc_fence_after();
-      QSA_TS(attn, 5 + 10 * (tile / (int)NC));
-
-      // 3. tile softmax statistics and P (one cell per thread); per-warp
-      // statistics by reduce-scatter, lanes 4k hold head k's
-      float sv[kGqa], tmax[kGqa], tsum[kGqa], pe[kGqa];
-      tmem_ld8(tmem + ((uint32_t)(32 * warp) << 16) + 0, sv);
-      if (tile < (int)NC) QSA_TS(attn, 8);
-      const int cell = 32 * warp + lane;
-      const bool valid = cell < nv && scell[cell] >= 0;
-#pragma unroll
-      for (int h = 0; h < kGqa; ++h) sv[h] = valid ? sv[h] * scale2 : -INFINITY;
-      {
-        const float m = warp_reduce8(sv, lane, OpMax());
-        if ((lane & 3) == 0) sred[warp * 8 + (lane >> 2)] = m;
-      }
-      bar_half(1);
-      if (tile < (int)NC) QSA_TS(attn, 9);
-#pragma unroll
-      for (int h = 0; h < kGqa; ++h) tmax[h] = fmaxf(fmaxf(sred[h], sred[8 + h]), fmaxf(sred[16 + h], sred[24 + h]));
-#pragma unroll
-      for (int h = 0; h < kGqa; ++h) {
-        const float p = (tmax[h] == -INFINITY) ? 0.f : exp2f(sv[h] - tmax[h]);
-        const __half ph = __float2half_rn(p);
-        pe[h] = __half2float(ph);   // the sum uses the rounded p the MMA sees
-        // P row h, column `cell`: atom cell/64, chunk (cell%64)/8, element cell%8
-        const uint32_t off = (uint32_t)(cell >> 6) * (16 * 128) + h * 128 +
-                             ((((uint32_t)(cell & 63) >> 3) ^ (uint32_t)(h & 7)) << 4) + (cell & 7) * 2;
-        *reinterpret_cast<__half*>(base + kOffP + off) = ph;
-      }
-      if (tile < (int)NC) QSA_TS(attn, 10);
-      fence_async_smem();
-      tc_fence_before();
-      bar_half(1);
-      tc_fence_after();
-      QSA_TS(attn, 6 + 10 * (tile / (int)NC));
-
-      // 4. O^T[dim][head] = V^T . P^T, two halves of 128 dims; the tile's
-      // row sums are reduced while the MMAs run
-      if (tid == 0) {
-#pragma unroll
-        for (int mh = 0; mh < 2; ++mh) {
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t ad = smem_desc(sV + mh * 2 * (kTile * 128) + kk * 2048, kTile * 128, 1024);
-            const uint64_t bd = smem_desc(sP + (kk >> 2) * (16 * 128) + (kk & 3) * 32, 16, 1024);
-            mma_f16(tmem + 16 + 16 * mh, ad, bd, kIdescPV, kk > 0);
-          }
-        }
-        mma_commit(bar);
-      }
-      {
-        const float e = warp_reduce8(pe, lane, OpAdd());
-        if ((lane & 3) == 0) sred[32 + warp * 8 + (lane >> 2)] = e;
-      }
-      bar_half(1);
-#pragma unroll
-      for (int h = 0; h < kGqa; ++h)
-        tsum[h] = (sred[32 + h] + sred[40 + h]) + (sred[48 + h] + sred[56 + h]);
-      if (!mbar_wait(bar, phase)) timed_out = true;
-      phase ^= 1;
-      tc_fence_after();
-      QSA_TS(attn, 7 + 10 * (tile / (int)NC));
-
-      // 5. merge the tile into the running state (dims 32w+lane and +128)
-      float o0[8], o1[8];
-      tmem_ld8(tmem + ((uint32_t)(32 * warp) << 16) + 16, o0);
-      tmem_ld8(tmem + ((uint32_t)(32 * warp) << 16) + 32, o1);
-#pragma unroll
-      for (int h = 0; h < kGqa; ++h) {
-        const float mn = fmaxf(run_m[h], tmax[h]);
-        const float fa = (run_m[h] == -INFINITY) ? 0.f : exp2f(run_m[h] - mn);
-        const float fb = (tmax[h] == -INFINITY) ? 0.f : exp2f(tmax[h] - mn);
-        acc[0][h] = acc[0][h] * fa + o0[h] * fb;
-        acc[1][h] = acc[1][h] * fa + o1[h] * fb;
-        run_l[h] = run_l[h] * fa + tsum[h] * fb;
-        run_m[h] = mn;
-      }
+      qk_mma(tile);
+      softmax_p(tile, scell, nv);
+      pv_merge(tile);
     } else if (my_ovf && tile == (int)rank) {
       // Overflow cells on warps 4-7 (128 threads, tx = 0..127); their ids
       // were loaded before the tile loop
@@ -605,10 +694,16 @@ cudaError_t pick_cluster(const AttnArgs& a, int* nc_out) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    e = cudaFuncSetAttribute(k_attn_tc<kQ8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    e = cudaFuncSetAttribute(k_attn_tc<kQ8, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k_attn_tc<kQ8>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    e = cudaFuncSetAttribute(k_attn_tc<kQ8, false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
+    if (!kQ8) {
+      e = cudaFuncSetAttribute(k_attn_tc<kQ8, !kQ8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+      if (e != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(k_attn_tc<kQ8, !kQ8>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+    }
     for (int i = 0; i < 5; ++i) {
       const int nc = 16 >> i;
       cudaLaunchConfig_t cfg = {};
@@ -623,7 +718,7 @@ cudaError_t pick_cluster(const AttnArgs& a, int* nc_out) {
       cfg.attrs = &attr;
       cfg.numAttrs = 1;
       int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, k_attn_tc<kQ8>, &cfg) != cudaSuccess) {
+      if (cudaOccupancyMaxActiveClusters(&n, k_attn_tc<kQ8, false>, &cfg) != cudaSuccess) {
         (void)cudaGetLastError();
         n = 0;
       }
@@ -683,7 +778,10 @@ cudaError_t launch_tc(const AttnArgs& a, unsigned* err, cudaStream_t stream) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, k_attn_tc<kQ8>, a, err);
+  // several tiles per CTA: the pipelined variant (fp16)
+  const int tiles = (int)ceil_div(a.cells_pitch, kTile);
+  if (!kQ8 && 2 * nc <= tiles) return cudaLaunchKernelEx(&cfg, k_attn_tc<kQ8, !kQ8>, a, err);
+  return cudaLaunchKernelEx(&cfg, k_attn_tc<kQ8, false>, a, err);
 }
 
 }  // namespace
