@@ -721,14 +721,18 @@ k_select(const IndexArgs a, void* ws, const float* __restrict__ scores,
     v0[b] = (w < nwords && j < j1) ? __ldcg(srow + j) : -INFINITY;
   }
   {
-    constexpr int kPer = kHistBins / kSelThreads;   // 8 bins per thread
+    constexpr int kPer = kHistBins / kSelThreads;   // 8 consecutive bins per thread, 2 vector loads
+    static_assert(kPer == 8, "histogram split");
     unsigned h[kPer];
     unsigned sum = 0;
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      h[i] = __ldcg(gh + tid * kPer + i);
-      sum += h[i];
+    {
+      const uint4 q0 = __ldcg(reinterpret_cast<const uint4*>(gh + tid * kPer));
+      const uint4 q1 = __ldcg(reinterpret_cast<const uint4*>(gh + tid * kPer) + 1);
+      h[0] = q0.x, h[1] = q0.y, h[2] = q0.z, h[3] = q0.w;
+      h[4] = q1.x, h[5] = q1.y, h[6] = q1.z, h[7] = q1.w;
     }
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) sum += h[i];
     if (tid == 0) {
       sm.thr = -1;
       sm.need = 0;
