@@ -278,6 +278,15 @@ k_score(const IndexArgs a, void* ws, float* __restrict__ scores, int chunk, unsi
   if (!kTopk) {
     const int64_t f1 = min(a.max_blocks, j0 + chunk);
     for (int64_t j = max((int64_t)nb, j0) + tid; j < f1; j += kScoreThreads) srow[j] = -INFINITY;
+  } else {
+    // the selection expands its chosen blocks through their table rows: ask
+    // L2 for the rows of this CTA's blocks now (16 bytes each, ~3 % of the
+    // pooled bytes), so the expansion does not wait on DRAM
+    for (int i = tid; i < nrows; i += kScoreThreads) {
+      const int sl = s_slot[i];
+      if (sl >= 0 && sl < a.n_slots)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(a.blk_cells + (int64_t)sl * a.r));
+    }
   }
 
   // ---- this warp's rows [r0, r1), 4 per stage
