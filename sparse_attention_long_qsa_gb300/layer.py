@@ -12,6 +12,7 @@ It holds no arithmetic of its own.
 """
 from __future__ import annotations
 
+import contextlib
 from typing import Optional
 
 import numpy as np
@@ -143,6 +144,45 @@ def step_inputs(st, device="cuda", new_cells=False):
         d.update(cells=_dev(st.cells, device=device), k_new=_dev(st.k_new, device=device),
                  v_new=_dev(st.v_new, device=device), idx_new=_dev(st.idx_new, device=device))
     return d
+
+
+class PackedInputs:
+    """A step's input tensors laid out back to back (256-byte aligned) in one
+    pinned host buffer and one device buffer, so that moving a step's inputs
+    to the device is a single copy.  `views` are the device tensors to pass to
+    the layer's calls; `pack` fills a pinned host buffer from host arrays."""
+
+    def __init__(self, fields: dict, device="cuda", pin=True):
+        self.fields = {}
+        off = 0
+        for k, (shape, dtype) in fields.items():
+            n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+            self.fields[k] = (off, tuple(shape), dtype, n)
+            off += -(-n // 256) * 256
+        self.nbytes = off
+        self.pin = pin
+        self.dev = torch.empty(max(off, 256), dtype=torch.uint8, device=device)
+        self.views = {k: self.dev[o:o + n].view(dtype).view(shape) for k, (o, shape, dtype, n) in self.fields.items()}
+
+    def pack(self, arrays: dict):
+        """A (pinned) host buffer holding `arrays` (numpy, same shapes and
+        dtypes as the fields) in this layout."""
+        host = torch.zeros(max(self.nbytes, 256), dtype=torch.uint8)
+        if self.pin:
+            host = host.pin_memory()
+        hv = host.numpy()
+        for k, (o, shape, dtype, n) in self.fields.items():
+            a = np.ascontiguousarray(arrays[k])
+            if a.nbytes != n or tuple(a.shape) != shape:
+                raise ValueError(f"{k}: expected {shape} ({n} bytes), got {a.shape} ({a.nbytes} bytes)")
+            hv[o:o + n] = a.view(np.uint8).reshape(-1)
+        return host
+
+    def upload(self, host, stream=None):
+        """One host-to-device copy of a packed step (asynchronous on `stream`,
+        default the current stream)."""
+        with torch.cuda.stream(stream) if stream is not None else contextlib.nullcontext():
+            self.dev[:host.numel()].copy_(host, non_blocking=True)
 
 
 def append_rows(wl, step: int):

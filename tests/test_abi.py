@@ -157,3 +157,23 @@ def test_index_topk_kernel_plan(L):
     assert qsa.index_topk_kernels(10, 5) == tiled
     assert qsa.index_topk_kernels(512, 1) == tiled
     assert L.qsa_index_topk_kernels(0, 1) == 0
+
+
+def test_packed_inputs_layout_round_trip():
+    """One-copy staging of a step's inputs: 256-byte aligned fields, the
+    views read back exactly the packed arrays (host-only check)."""
+    import numpy as np
+    import torch
+    from sparse_attention_long_qsa_gb300.layer import PackedInputs
+    rng = np.random.default_rng(0)
+    arrs = {"tok_seq": np.array([3], dtype=np.int32), "q": rng.standard_normal((1, 16, 256)).astype(np.float16),
+            "q_idx": rng.standard_normal((1, 4, 128)).astype(np.float32), "w": np.arange(5, dtype=np.int64)}
+    fields = {k: (a.shape, {np.int32: torch.int32, np.float16: torch.float16, np.float32: torch.float32,
+                            np.int64: torch.int64}[a.dtype.type]) for k, a in arrs.items()}
+    p = PackedInputs(fields, device="cpu", pin=False)
+    offs = [o for o, *_ in p.fields.values()]
+    assert all(o % 256 == 0 for o in offs) and offs == sorted(offs)
+    host = p.pack(arrs)
+    p.dev[:host.numel()].copy_(host)
+    for k, a in arrs.items():
+        np.testing.assert_array_equal(p.views[k].numpy(), a)
