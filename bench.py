@@ -42,6 +42,14 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "QSA-layer decode tokens/s at 50k/250k ctx (1 and 5 seqs); HBM GB/s vs peak"
+# DRAM bytes (read + write) of one launch of a workload's roofline kernel,
+# from an ncu capture of the current kernel (profiles/<kernel>_<workload>.md);
+# a workload or kernel missing here reports null.  Update or remove an entry
+# whenever the kernel changes.
+NCU_TRAFFIC = {
+    ("50k", "score"): 6_688_256,           # profiles/k_score_50k.md
+    ("5x250k_q8", "score"): 169_715_456,   # profiles/k_score_5x250k.md
+}
 FLUSH_BYTES = [1 << 30]   # L2 flush buffer (--flush-mb)
 FLUSH_READ_BYTES = 256 << 20   # read after the flush write (> the 129 MB L2)
 
@@ -520,6 +528,7 @@ def run_native(args, rank, world, local):
                 "kernels_gbs": {k: round(v, 1) for k, v in r2["kern_gbs"].items()},
                 "dominant": r2["dominant"], "longest": r2["longest"],
                 "dominant_frac_of_hbm": r2["dom_bytes"] / (r2["dom_ms"] * 1e-3) / 1e9 / hbm,
+                "dominant_traffic": NCU_TRAFFIC.get((name, r2["dominant"])),
             }
 
     cpu = None
@@ -560,7 +569,8 @@ def run_native(args, rank, world, local):
                      "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "peak_source": f"hbm_gbs {peak_src}",
                      "bytes_per_launch": res["dom_bytes"], "us_per_launch": res["dom_ms"] * 1e3,
-                     "traffic": None},
+                     "traffic": NCU_TRAFFIC.get((args.config, res["dominant"])),
+                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch"},
         "step_us_p50": res["step_us_p50"], "step_us_p90": res["step_us_p90"],
         "kernels_us": {k: round(v, 3) for k, v in res["kern_us"].items()},
         "kernels_gbs": {k: round(v, 1) for k, v in res["kern_gbs"].items()},
