@@ -476,6 +476,18 @@ def measure_config(name, K, W, dev, *, path="full", e2e=True, clocks=None):
     return res
 
 
+def replica_value(local_ms: float, tokens: int, world: int, dist=None, device="cpu"):
+    """Whole-job tokens/s of `world` replicas that each processed `tokens` in
+    their own `local_ms`: all replicas' tokens over the slowest replica's
+    time (max over ranks).  Returns (tokens/s, max ms)."""
+    import torch
+    if dist is not None and world > 1:
+        t = torch.tensor([float(local_ms)], device=device, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        local_ms = float(t.item())
+    return world * tokens / (local_ms / 1e3), local_ms
+
+
 def run_native(args, rank, world, local):
     import torch
     import __graft_entry__
@@ -499,12 +511,7 @@ def run_native(args, rank, world, local):
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
-        t = torch.tensor([res["ms_per_step"] * args.steps], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        max_ms = float(t.item())
-    else:
-        max_ms = res["ms_per_step"] * args.steps
-    value = world * res["tokens"] / (max_ms / 1e3)
+    value, max_ms = replica_value(res["ms_per_step"] * args.steps, res["tokens"], world, dist, dev)
 
     other = "calls" if args.path == "full" else "full"
     paths = {args.path: {"value": res["value"], "ms_per_step": res["ms_per_step"],
