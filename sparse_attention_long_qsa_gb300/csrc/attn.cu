@@ -207,13 +207,18 @@ k_attn_tc(const AttnArgs a, unsigned* err) {
   uint32_t phase = 0;
   bool timed_out = false;
 
-  // Cells past NC full tiles: when there are at most kOvf of them, CTA 0's
-  // warps 4-7 attend them on CUDA cores while warps 0-3 run its MMA tile;
-  // otherwise CTAs take further tiles in turn.
-  const int ovf_n = (n_tiles == (int)NC + 1) ? cnt - (int)NC * kTile : 0;
+  // A short last tile (at most kOvf cells past the full tiles) is attended on
+  // CUDA cores by warps 4-7 of CTA (n_tiles - 1) mod NC, the CTA that would
+  // otherwise run one MMA tile more than the others, while its warps 0-3 run
+  // their MMA tiles: for q8_0 whenever the tiles outnumber the CTAs (several
+  // tiles per CTA happen at 5 tokens and 250k), for fp16 when every CTA holds
+  // one full tile (n_tiles = NC + 1; the pipelined fp16 variant covers the
+  // rest).
+  const int ovf_n = (kQ8 ? n_tiles > (int)NC : n_tiles == (int)NC + 1) ? cnt - (n_tiles - 1) * kTile : 0;
   const bool use_ovf = ovf_n > 0 && ovf_n <= kOvf;
-  const int loop_tiles = use_ovf ? (int)NC : n_tiles;
-  const bool my_ovf = use_ovf && rank == 0;
+  const int loop_tiles = use_ovf ? n_tiles - 1 : n_tiles;
+  const int ovf_rank = (n_tiles - 1) % (int)NC;
+  const bool my_ovf = use_ovf && (int)rank == ovf_rank;
 
   // the overflow cells' ids load with the first tile's (warps 4-7 of CTA 0)
   int* xc = reinterpret_cast<int*>(base + kOffXC);
@@ -221,7 +226,7 @@ k_attn_tc(const AttnArgs a, unsigned* err) {
     const int tx = tid - 128;
     int c = -1;
     if (tx < ovf_n) {
-      c = crow[(int)NC * kTile + tx];
+      c = crow[(n_tiles - 1) * kTile + tx];
       if (c < 0 || c >= a.n_cells) {
         atomicOr(err, kErrCell);
         c = -1;
@@ -231,7 +236,7 @@ k_attn_tc(const AttnArgs a, unsigned* err) {
   }
   // fp16: with overflow cells, warps 0-3 gather the MMA tile alone while warps
   // 4-7 gather and attend the overflow cells from the start
-  const bool split = !kQ8 && my_ovf;
+  const bool split = !kQ8 && my_ovf && loop_tiles <= (int)NC;   // this CTA runs one MMA tile
 
   // Per-tile steps of warps 0-3 (tile: for the phase stamps only)
   float tmax[kGqa], pe[kGqa];
