@@ -57,6 +57,7 @@ DESCR = {
     "50k": "decode, 1 seq, 50,000-cell fp16 K/V prompt + 1 cell/step (tails cycle 1,2,3,0), "
            "16q/2kv heads x 256, indexer 4x128, r=4, top_k=2048",
     "250k_q8": "decode, 1 seq, 250,000-cell q8_0 K/V prompt + 1 cell/step, same heads, top_k=2048",
+    "250k_f16": "decode, 1 seq, 250,000-cell fp16 K/V prompt + 1 cell/step, same heads, top_k=2048",
     "5x250k_q8": "decode, 5 seqs x 250,000 cells in one 1.25M-cell q8_0 cache, 5 tokens/step, top_k=2048 per seq",
     "tiny": "decode, 1 seq, 4,096 cells fp16, top_k=2048",
     "prefill": "prefill ubatch, 512 tokens appended to a 250,000-cell fp16 prompt, 128 dirty blocks",

@@ -21,7 +21,7 @@ from typing import List, Optional
 
 import numpy as np
 
-CONFIG_NAMES = ("tiny", "50k", "250k_q8", "5x250k_q8", "prefill", "verify5_250k_q8")
+CONFIG_NAMES = ("tiny", "50k", "250k_q8", "250k_f16", "5x250k_q8", "prefill", "verify5_250k_q8")
 
 
 def default_cfg(**over) -> dict:
@@ -184,6 +184,8 @@ PRESETS = {
     "tiny": (1, 4095, 1, 1, "f16"),
     "50k": (1, 50_000, 128, 1, "f16"),
     "250k_q8": (1, 250_000, 128, 1, "q8_0"),
+    # the same depth with fp16 K/V (attention time flat in n_kv: compare with 50k)
+    "250k_f16": (1, 250_000, 128, 1, "f16"),
     "5x250k_q8": (5, 250_000, 128, 1, "q8_0"),
     "prefill": (1, 250_000, 1, 512, "f16"),
     # speculative verify batch: 5 consecutive query tokens of one sequence per step
