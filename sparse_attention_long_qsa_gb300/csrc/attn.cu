@@ -128,8 +128,9 @@ __device__ __forceinline__ uint4 dq8(uint2 raw, __half2 s2) {
   return o;
 }
 
-// kPipe (fp16 only): the launch gives CTAs several tiles each; the pipelined
-// tile loop is compiled only into this variant, so the one-tile decode
+// kPipe: the launch gives CTAs several tiles each; the pipelined tile loops
+// (fp16: cp.async groups into shared memory; q8_0: the next tile's rows in
+// registers) are compiled only into this variant, so the one-tile decode
 // variant keeps its code small (it runs from a cold instruction cache).
 template <bool kQ8, bool kPipe>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -410,10 +411,79 @@ k_attn_tc(const AttnArgs a, unsigned* err) {
     }
   }
 
+  // q8_0: thread -> (row tid / 2, half tid % 2) of the tile: 128 int8 of K
+  // and of V plus their 4 scales each, fetched to registers, then
+  // dequantised into the swizzled fp16 tiles
+  const int qrow = tid >> 1, qhalf = tid & 1;
+  uint4 qk[8], qv[8];
+  uint2 qks = make_uint2(0, 0), qvs = make_uint2(0, 0);
+  auto q8_fetch = [&](int c) {
+    if (c >= 0) {
+      const int8_t* kq = static_cast<const int8_t*>(a.k_cache);
+      const int8_t* vq = static_cast<const int8_t*>(a.v_cache);
+      const int64_t nq = a.n_cells * (int64_t)G * kHeadDim;
+      const int64_t cg = (int64_t)c * G + g;
+      const uint4* kp = reinterpret_cast<const uint4*>(kq + cg * kHeadDim + qhalf * 128);
+      const uint4* vp = reinterpret_cast<const uint4*>(vq + cg * kHeadDim + qhalf * 128);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        qk[j] = __ldg(kp + j);
+        qv[j] = __ldg(vp + j);
+      }
+      qks = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const __half*>(kq + nq) + cg * 8 + qhalf * 4));
+      qvs = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const __half*>(vq + nq) + cg * 8 + qhalf * 4));
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) qk[j] = qv[j] = make_uint4(0, 0, 0, 0);
+      qks = qvs = make_uint2(0, 0);
+    }
+  };
+  auto q8_store = [&]() {
+    const __half* ksh = reinterpret_cast<const __half*>(&qks);
+    const __half* vsh = reinterpret_cast<const __half*>(&qvs);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      // 16 int8 = dims half*128 + 16j .. +15 -> two 16-byte fp16 chunks
+      const __half2 skf = __half2half2(ksh[j >> 1]), svf = __half2half2(vsh[j >> 1]);
+      const int c16 = qhalf * 16 + 2 * j;
+      *reinterpret_cast<uint4*>(base + kOffK + sw128(kTile, qrow, c16)) = dq8(make_uint2(qk[j].x, qk[j].y), skf);
+      *reinterpret_cast<uint4*>(base + kOffK + sw128(kTile, qrow, c16 + 1)) = dq8(make_uint2(qk[j].z, qk[j].w), skf);
+      *reinterpret_cast<uint4*>(base + kOffV + sw128(kTile, qrow, c16)) = dq8(make_uint2(qv[j].x, qv[j].y), svf);
+      *reinterpret_cast<uint4*>(base + kOffV + sw128(kTile, qrow, c16 + 1)) = dq8(make_uint2(qv[j].z, qv[j].w), svf);
+    }
+  };
+  // q8_0 with several tiles per CTA (kPipe): the registers hold the next
+  // tile's rows while this tile's MMAs and softmax run; the row's cell id
+  // is read one tile earlier still, and checked only when it is used, so no
+  // warp waits on it before its MMAs.
+  int qc = -1, qraw = 0;   // the fetched row's checked cell; the next row's raw id
+  auto q8_cell = [&](int tile, int raw) {
+    const int i = tile * kTile + qrow;
+    if (tile >= loop_tiles || i >= cnt) return -1;
+    if (raw < 0 || raw >= a.n_cells) {
+      atomicOr(err, kErrCell);
+      return -1;
+    }
+    return raw;
+  };
+  auto q8_raw = [&](int tile) {
+    const int i = tile * kTile + qrow;
+    return (tile < loop_tiles && i < cnt) ? crow[i] : 0;
+  };
+  if constexpr (kQ8 && kPipe) {
+    qc = q8_cell((int)rank, q8_raw((int)rank));
+    q8_fetch(qc);
+    qraw = q8_raw((int)rank + (int)NC);
+  }
+
   if (!pipe)
   for (int tile = (int)rank; tile < loop_tiles; tile += (int)NC) {
     const int c0 = tile * kTile;
     const int nv = min(kTile, cnt - c0);
+    if constexpr (kQ8 && kPipe) {
+      if (qhalf == 0) scell[qrow] = qc;
+      q8_store();
+    } else {
     if (tid < kTile) {
       int c = -1;
       if (tid < nv) {
@@ -447,43 +517,9 @@ k_attn_tc(const AttnArgs a, unsigned* err) {
         asm volatile("cp.async.wait_all;\n" ::: "memory");
       }
     } else {
-      // thread -> (row, half): 128 int8 of K and of V plus their 4 scales each
-      const int8_t* kq = static_cast<const int8_t*>(a.k_cache);
-      const int8_t* vq = static_cast<const int8_t*>(a.v_cache);
-      const int64_t nq = a.n_cells * (int64_t)G * kHeadDim;
-      const __half* kd = reinterpret_cast<const __half*>(kq + nq);
-      const __half* vd = reinterpret_cast<const __half*>(vq + nq);
-      const int row = tid >> 1, half = tid & 1;
-      const int c = scell[row];
-      const int64_t cg = (int64_t)(c < 0 ? 0 : c) * G + g;
-      uint4 kr[8], vr[8];
-      uint2 ks = make_uint2(0, 0), vs = make_uint2(0, 0);
-      if (c >= 0) {
-        const uint4* kp = reinterpret_cast<const uint4*>(kq + cg * kHeadDim + half * 128);
-        const uint4* vp = reinterpret_cast<const uint4*>(vq + cg * kHeadDim + half * 128);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          kr[j] = __ldg(kp + j);
-          vr[j] = __ldg(vp + j);
-        }
-        ks = __ldg(reinterpret_cast<const uint2*>(kd + cg * 8 + half * 4));
-        vs = __ldg(reinterpret_cast<const uint2*>(vd + cg * 8 + half * 4));
-      } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) kr[j] = vr[j] = make_uint4(0, 0, 0, 0);
-      }
-      const __half* ksh = reinterpret_cast<const __half*>(&ks);
-      const __half* vsh = reinterpret_cast<const __half*>(&vs);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        // 16 int8 = dims half*128 + 16j .. +15 -> two 16-byte fp16 chunks
-        const __half2 skf = __half2half2(ksh[j >> 1]), svf = __half2half2(vsh[j >> 1]);
-        const int c16 = half * 16 + 2 * j;
-        *reinterpret_cast<uint4*>(base + kOffK + sw128(kTile, row, c16)) = dq8(make_uint2(kr[j].x, kr[j].y), skf);
-        *reinterpret_cast<uint4*>(base + kOffK + sw128(kTile, row, c16 + 1)) = dq8(make_uint2(kr[j].z, kr[j].w), skf);
-        *reinterpret_cast<uint4*>(base + kOffV + sw128(kTile, row, c16)) = dq8(make_uint2(vr[j].x, vr[j].y), svf);
-        *reinterpret_cast<uint4*>(base + kOffV + sw128(kTile, row, c16 + 1)) = dq8(make_uint2(vr[j].z, vr[j].w), svf);
-      }
+      q8_fetch(scell[qrow]);
+      q8_store();
+    }
     }
     fence_async_smem();
     tc_fence_before();
@@ -494,6 +530,13 @@ k_attn_tc(const AttnArgs a, unsigned* err) {
     }
     tc_fence_after();
     QSA_TS(attn, 4 + 10 * (tile / (int)NC));
+    if constexpr (kQ8 && kPipe) {
+      if (tile + (int)NC < loop_tiles) {
+        qc = q8_cell(tile + (int)NC, qraw);
+        q8_fetch(qc);
+        qraw = q8_raw(tile + 2 * (int)NC);
+      }
+    }
 
     if (warp < 4) {
       qk_mma(tile);
@@ -703,12 +746,10 @@ cudaError_t pick_cluster(const AttnArgs& a, int* nc_out) {
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(k_attn_tc<kQ8, false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
-    if (!kQ8) {
-      e = cudaFuncSetAttribute(k_attn_tc<kQ8, !kQ8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-      if (e != cudaSuccess) return e;
-      e = cudaFuncSetAttribute(k_attn_tc<kQ8, !kQ8>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-      if (e != cudaSuccess) return e;
-    }
+    e = cudaFuncSetAttribute(k_attn_tc<kQ8, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_attn_tc<kQ8, true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
     for (int i = 0; i < 5; ++i) {
       const int nc = 16 >> i;
       cudaLaunchConfig_t cfg = {};
@@ -783,9 +824,9 @@ cudaError_t launch_tc(const AttnArgs& a, unsigned* err, cudaStream_t stream) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  // several tiles per CTA: the pipelined variant (fp16)
+  // several tiles per CTA: the pipelined variant
   const int tiles = (int)ceil_div(a.cells_pitch, kTile);
-  if (!kQ8 && 2 * nc <= tiles) return cudaLaunchKernelEx(&cfg, k_attn_tc<kQ8, !kQ8>, a, err);
+  if (2 * nc <= tiles) return cudaLaunchKernelEx(&cfg, k_attn_tc<kQ8, true>, a, err);
   return cudaLaunchKernelEx(&cfg, k_attn_tc<kQ8, false>, a, err);
 }
 

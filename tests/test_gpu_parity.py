@@ -232,14 +232,45 @@ def test_out_of_range_indices_are_masked_and_flagged():
     assert qsa.debug_check()[0] == 0
 
 
-@pytest.mark.parametrize("top_k,n", [(16, 403), (256, 9_001), (512, 600), (4096, 30_003)])
-def test_other_budgets_cover_every_tile_layout(top_k, n):
+@pytest.mark.parametrize("top_k,n,kv_type", [(16, 403, "f16"), (256, 9_001, "f16"), (512, 600, "f16"),
+                                              (4096, 30_003, "f16"), (256, 9_001, "q8_0"),
+                                              (4096, 30_003, "q8_0")])
+def test_other_budgets_cover_every_tile_layout(top_k, n, kv_type):
     """Budgets other than 2048 exercise the other attention layouts: one tile
     (top_k 16), a 2-CTA cluster plus overflow cells (256), exactly NC tiles
-    (512 with a full budget), and several tiles per CTA (4096)."""
-    wl = make_workload(n_seq=1, prompt_len=n - 1, n_steps=3, seed=200 + top_k, cfg={"top_k": top_k})
+    (512 with a full budget), and several tiles per CTA (4096: the pipelined
+    loops, cp.async for fp16 and register prefetch for q8_0)."""
+    wl = make_workload(n_seq=1, prompt_len=n - 1, n_steps=3, seed=200 + top_k, cfg={"top_k": top_k},
+                       kv_type=kv_type)
     run = Runner(wl)
     for i in range(3):
         res, _ = check_step(run, i)
         nb = (n + i) // 4
         assert int(res["count"][0]) == min(nb, top_k // 4) * 4 + (n + i) % 4
+
+
+def test_q8_bad_indices_in_later_tiles_are_masked_and_flagged():
+    """q8_0 with two 128-cell tiles per CTA (the register-prefetch loop) and
+    overflow cells: bad ids in a CTA's second tile and among the overflow
+    cells are skipped and reported, the rest attended exactly."""
+    wl = make_workload(n_seq=1, prompt_len=30_002, n_steps=1, seed=13, kv_type="q8_0", cfg={"top_k": 4096})
+    L = QSALayer.from_workload(wl, 0)
+    qsa.debug_check()
+    q = torch.from_numpy(wl.steps[0].q).cuda()
+    rng = np.random.default_rng(14)
+    cnt = 4096 + 3
+    assert L.cells.shape[1] >= cnt
+    cells = rng.choice(30_002, cnt, replace=False).astype(np.int32)
+    bad = {16 * 128 + 5: wl.n_cells + 9, 31 * 128 + 127: -2, 4097: wl.n_cells}
+    for i, c in bad.items():
+        cells[i] = c
+    L.cells[0] = -1
+    L.cells[0, :cnt] = torch.from_numpy(cells)
+    L.count[0] = cnt
+    L.sparse_attn(q, 1)
+    st, flags = qsa.debug_check()
+    assert st == -6 and (flags & 2)
+    keep = np.array([c for i, c in enumerate(cells) if i not in bad])
+    ref = O.attend(wl.cfg, wl.steps[0].q[0], wl.k_cache, wl.v_cache, wl.n_cells, keep)
+    assert max_rel(to_np(L.out[0]), ref) <= ATTN_TOL["q8_0"]
+    assert qsa.debug_check()[0] == 0
