@@ -411,10 +411,13 @@ k_attn_tc(const AttnArgs a, unsigned* err) {
     }
   }
 
-  // q8_0: thread -> (row tid / 2, half tid % 2) of the tile: 128 int8 of K
-  // and of V plus their 4 scales each, fetched to registers, then
-  // dequantised into the swizzled fp16 tiles
-  const int qrow = tid >> 1, qhalf = tid & 1;
+  // q8_0: thread -> (row, half) of the tile: 128 int8 of K and of V plus
+  // their 4 scales each, fetched to registers, then dequantised into the
+  // swizzled fp16 tiles.  Each 8 consecutive threads take one half of 8
+  // consecutive rows, so the 16-byte stores of a quarter warp land on 8
+  // distinct swizzled chunks (all 32 banks); the two halves of one row sit
+  // 16 KB apart on the same banks.
+  const int qrow = (tid & 7) | ((tid >> 4) << 3), qhalf = (tid >> 3) & 1;
   uint4 qk[8], qv[8];
   uint2 qks = make_uint2(0, 0), qvs = make_uint2(0, 0);
   auto q8_fetch = [&](int c) {
