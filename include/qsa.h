@@ -26,6 +26,11 @@
  *    range-checked by the kernels: an out-of-range index is skipped (treated
  *    as absent / masked) and recorded in a device error word that
  *    qsa_debug_check reads.  No kernel traps or spin-waits.
+ *  - Host threads: calls may come from several host threads at once; each
+ *    device's one-time kernel set-up (shared-memory limits, cluster
+ *    occupancy) runs under a lock.  Calls that share output or workspace
+ *    buffers must still be ordered by the caller, and qsa_index_topk_noalloc
+ *    and qsa_profile_kernel carry the further limits stated with them.
  *  - Shapes: one instantiated geometry, the qwen4exp QSA layer: head_dim 256,
  *    8 query heads per KV head (n_q_heads = 8 * n_kv_heads), idx_dim 128,
  *    n_idx_heads 4, compress_ratio 4, top_k a multiple of compress_ratio.

@@ -33,7 +33,9 @@
 // Waits on the MMA completion barrier are bounded: on timeout the CTA records
 // an error bit and keeps going through every barrier (its output is then
 // meaningless but nothing hangs).
+#include <atomic>
 #include <cstring>
+#include <mutex>
 
 #include "qsa_internal.cuh"
 #include "tc_util.cuh"
@@ -738,42 +740,48 @@ constexpr int kMaxDevices = 64;
 // else the largest smaller power of two that fits them.
 template <bool kQ8>
 cudaError_t pick_cluster(const AttnArgs& a, int* nc_out) {
-  static int max_active[kMaxDevices][5];   // per device: clusters of 16, 8, 4, 2, 1
-  static bool configured[kMaxDevices];
+  // per device: clusters of 16, 8, 4, 2, 1 that fit at once, measured once
+  // under a lock and published by `configured`
+  static int max_active[kMaxDevices][5];
+  static std::atomic<bool> configured[kMaxDevices];
+  static std::mutex mu;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
-    e = cudaFuncSetAttribute(k_attn_tc<kQ8, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k_attn_tc<kQ8, false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k_attn_tc<kQ8, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k_attn_tc<kQ8, true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-    for (int i = 0; i < 5; ++i) {
-      const int nc = 16 >> i;
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3((unsigned)nc, 1, 1);
-      cfg.blockDim = dim3(kThreads, 1, 1);
-      cfg.dynamicSmemBytes = kSmemBytes;
-      cudaLaunchAttribute attr;
-      attr.id = cudaLaunchAttributeClusterDimension;
-      attr.val.clusterDim.x = (unsigned)nc;
-      attr.val.clusterDim.y = 1;
-      attr.val.clusterDim.z = 1;
-      cfg.attrs = &attr;
-      cfg.numAttrs = 1;
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, k_attn_tc<kQ8, false>, &cfg) != cudaSuccess) {
-        (void)cudaGetLastError();
-        n = 0;
+  if (!configured[dev].load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!configured[dev].load(std::memory_order_relaxed)) {
+      e = cudaFuncSetAttribute(k_attn_tc<kQ8, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+      if (e != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(k_attn_tc<kQ8, false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(k_attn_tc<kQ8, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+      if (e != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(k_attn_tc<kQ8, true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+      for (int i = 0; i < 5; ++i) {
+        const int nc = 16 >> i;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)nc, 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = kSmemBytes;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = (unsigned)nc;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, k_attn_tc<kQ8, false>, &cfg) != cudaSuccess) {
+          (void)cudaGetLastError();
+          n = 0;
+        }
+        max_active[dev][i] = n;
       }
-      max_active[dev][i] = n;
+      configured[dev].store(true, std::memory_order_release);
     }
-    configured[dev] = true;
   }
   const int tiles = (int)ceil_div(a.cells_pitch, kTile);
   const int want = tiles < kMaxCluster ? tiles : kMaxCluster;

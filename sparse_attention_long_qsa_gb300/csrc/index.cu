@@ -38,7 +38,9 @@
 //             token's list (blocks ascending), CTA 0 appends the tail cells
 //             and clears the histogram for the next call.
 #include <algorithm>
+#include <atomic>
 #include <cstring>
+#include <mutex>
 
 #include "qsa_internal.cuh"
 #include "tc_util.cuh"
@@ -1207,15 +1209,23 @@ int select_cluster(int T, int64_t max_blocks, int sms) {
   return best_nc;
 }
 
-// Per-device set-up of the index kernels: SM count, shared-memory limits.
+// Per-device set-up of the index kernels (SM count, shared-memory limits):
+// done once per device under a lock, then read from the published count.
 cudaError_t index_setup(int* sms) {
-  static int sm_count[64];
+  static std::atomic<int> sm_count[64];
+  static std::mutex mu;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (sm_count[dev] == 0) {
-    int n = 0;
+  int n = sm_count[dev].load(std::memory_order_acquire);
+  if (n > 0) {
+    *sms = n;
+    return cudaSuccess;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  n = sm_count[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(k_score<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScoreSmem);
@@ -1231,9 +1241,10 @@ cudaError_t index_setup(int* sms) {
     e = cudaFuncSetAttribute(k_score_tc<16, 32, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)TcShape<16, 32>::kSmem);
     if (e != cudaSuccess) return e;
-    sm_count[dev] = n;
+    if (n <= 0) return cudaErrorInvalidDevice;
+    sm_count[dev].store(n, std::memory_order_release);
   }
-  *sms = sm_count[dev];
+  *sms = n;
   return cudaSuccess;
 }
 
