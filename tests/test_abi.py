@@ -177,3 +177,20 @@ def test_packed_inputs_layout_round_trip():
     p.dev[:host.numel()].copy_(host)
     for k, a in arrs.items():
         np.testing.assert_array_equal(p.views[k].numpy(), a)
+
+
+def test_index_topk_noalloc_host_limits(L):
+    """The no-allocation entry point refuses, before any CUDA call, what its
+    static scratch array cannot hold (more than 8 tokens or 262,144 blocks per
+    sequence), and validates like qsa_index_topk otherwise."""
+    c = qsa.config()
+    f = ctypes.c_void_p(0x10000)
+    def call(n_tokens, max_blocks, cells=f, cfg=c):
+        return L.qsa_index_topk_noalloc(ctypes.byref(cfg), n_tokens, f, f, f, f, f, f, 100, f, f, 1,
+                                        max_blocks, 1000, cells, f, None)
+    assert call(9, 1000) == -4
+    assert call(1, 262_145) == -4
+    assert call(0, 262_144) == 0                 # nothing to do
+    assert call(1, 1000, cells=None) == -1
+    assert call(1, -1) == -1
+    assert call(1, 1000, cfg=qsa.config(head_dim=128)) == -3
