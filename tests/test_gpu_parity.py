@@ -274,3 +274,47 @@ def test_q8_bad_indices_in_later_tiles_are_masked_and_flagged():
     ref = O.attend(wl.cfg, wl.steps[0].q[0], wl.k_cache, wl.v_cache, wl.n_cells, keep)
     assert max_rel(to_np(L.out[0]), ref) <= ATTN_TOL["q8_0"]
     assert qsa.debug_check()[0] == 0
+
+
+@pytest.mark.parametrize("T", [1, 40])
+def test_selection_paths_past_65536_blocks(T):
+    """Past 65,536 blocks per token the selection cannot finish in CTA 0 of
+    the cluster.  Pooled rows c_s * v make every score c_s times one factor
+    per token; 400 slots get c in [2^12, 2^16), K slots c within 1e-4 of 2^8
+    (one histogram bin), the rest c in [1, 16), so the 512-block cut falls in
+    a bin of exactly K keys: K = 600 ranks them directly across the cluster,
+    1,500 runs radix rounds over the kept candidates, 5,000 radix rounds that
+    re-scan the scores.  One token takes an 8-CTA cluster; 40 tokens take
+    2-CTA clusters whose ranges exceed the cached slot ids.  Each choice
+    equals a stable sort of the GPU's own scores."""
+    wl = make_workload(n_seq=1, prompt_len=280_000, n_steps=1, tokens_per_step=T, seed=300 + T)
+    L = QSALayer.from_workload(wl, 0)
+    L.set_cells(*append_rows(wl, 0))
+    st = wl.steps[0]
+    inp = step_inputs(st)
+    table = wl.blk_cells_state(1)
+    g = torch.Generator(device="cpu").manual_seed(T)
+    v = torch.from_numpy(st.q_idx[0, 0].astype(np.float32))   # token 0, head 0: a positive factor
+    sc = torch.empty((T, L.max_blocks), dtype=torch.float32, device="cuda")
+    for k_bin in (600, 1_500, 5_000):
+        perm = torch.randperm(L.n_slots, generator=g)
+        u = torch.rand(L.n_slots, generator=g, dtype=torch.float64)
+        c = torch.exp2(u * 4.0)                                   # below the cut
+        c[perm[:400]] = torch.exp2(12.0 + u[perm[:400]] * 4.0)    # above it
+        mid = perm[400:400 + k_bin]
+        c[mid] = 256.0 * (1.0 + 1e-4 * u[mid])                    # the cut's bin
+        L.pooled.copy_((c.float()[:, None] * v[None, :]).cuda())
+        L.index_topk(inp["tok_seq"], inp["tok_pos"], inp["q_idx"], inp["w_idx"])
+        qsa.index_scores(L.cfg, inp["q_idx"], inp["w_idx"], inp["tok_seq"], inp["tok_pos"], L.pooled,
+                         L.seq_blk_off, L.seq_blk_slots, L.max_blocks, sc)
+        torch.cuda.synchronize()
+        scores = to_np(sc)
+        for t in range(T):
+            seq, pos = int(st.tok_seq[t]), int(st.tok_pos[t])
+            nb = (pos + 1) // 4
+            assert nb > 65_536
+            sel = O.select_blocks(scores[t, :nb], 512)
+            want = O.expand_cells(wl.cfg, sel, seq, pos, table, wl.seq_blk_off, wl.seq_blk_slots)
+            np.testing.assert_array_equal(to_np(L.cells[t, :len(want)]), want)
+            assert int(L.count[t]) == len(want)
+    assert_no_device_errors()
