@@ -44,6 +44,8 @@ def _poison_new_cells(wl, L):
     dict(n_seq=3, prompt_len=[3001, 9002, 1203], n_steps=5, kv_type="q8_0", shuffled=True),
     dict(n_seq=1, prompt_len=7003, n_steps=3, tokens_per_step=5, kv_type="q8_0"),
     dict(n_seq=1, prompt_len=2001, n_steps=1, tokens_per_step=96, kv_type="f16", shuffled=True),
+    # the per-call maximum: 1,024 new tokens (512 per sequence), ~260 blocks re-pooled in the launch
+    dict(n_seq=2, prompt_len=[3001, 5002], n_steps=1, tokens_per_step=512, kv_type="q8_0", shuffled=True),
 ])
 def test_append_matches_oracle_bit_for_bit(kw):
     wl = make_workload(seed=41, **kw)
