@@ -271,7 +271,10 @@ def q8_0_block(x32: np.ndarray):
     q = np.zeros(32, dtype=np.int8)
     for i, v in enumerate(x):
         t = np.float32(v * inv)
-        m = int(np.floor(np.float32(abs(t)) + np.float32(0.5)))   # half away from zero
+        a = np.float32(abs(t))
+        m = int(np.trunc(a))
+        if np.float32(a - np.float32(m)) >= np.float32(0.5):   # half away from zero (a - m is exact)
+            m += 1
         m = min(m, 127)
         q[i] = -m if t < 0 else m
     return q, np.float16(d)

@@ -53,8 +53,10 @@ def quantize_q8_0(x: np.ndarray):
     nz = d > 0
     inv[nz] = np.float32(1.0) / d[nz]
     v = xb * inv[..., None]
-    q = np.sign(v) * np.floor(np.abs(v) + np.float32(0.5))
-    q = np.clip(q, -127, 127).astype(np.int8)
+    a = np.abs(v)
+    m = np.trunc(a)
+    m = m + (a - m >= np.float32(0.5))          # half away from zero; a - m is exact in float32
+    q = np.clip(np.sign(v) * m, -127, 127).astype(np.int8)
     return q.reshape(x.shape), d.astype(np.float16)
 
 

@@ -229,7 +229,11 @@ k_append(const AppendArgs a, const Turns turns, unsigned* err) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const float v = x[i] * inv;
-      float m = floorf(fabsf(v) + 0.5f);             // half away from zero
+      // half away from zero, exactly: |v| - trunc(|v|) is exact in fp32,
+      // while floor(|v| + 0.5) would round 0.5 - 2^-25 up to 1
+      const float av = fabsf(v);
+      float m = truncf(av);
+      if (av - m >= 0.5f) m += 1.0f;
       m = fminf(m, 127.f);
       qb[i] = (signed char)(v < 0.f ? -(int)m : (int)m);
     }

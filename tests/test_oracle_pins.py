@@ -395,6 +395,19 @@ def test_q8_0_block_closed_forms(name, case):
     assert float(d) == case["d"]
 
 
+@pytest.mark.parametrize("name,case", _q8_cases())
+def test_input_encoder_closed_forms(name, case):
+    """The workload generator's own q8_0 encoder on the same hand-derived
+    blocks (its codes are the bytes the GPU append must reproduce)."""
+    x = np.zeros((1, 32), np.float32)
+    x[0, :len(case["x"])] = case["x"]
+    qs, d = quantize_q8_0(x)
+    want = np.zeros(32, np.int8)
+    want[:len(case["q"])] = case["q"]
+    np.testing.assert_array_equal(qs[0], want)
+    assert float(d[0, 0]) == case["d"]
+
+
 def test_q8_0_block_error_bound_and_extremes():
     rng = np.random.default_rng(5)
     for _ in range(200):
