@@ -16,7 +16,9 @@
  *
  * Conventions for every call:
  *  - Pointers named as device buffers are DEVICE pointers owned by the caller.
- *    The library never allocates, frees or keeps them.
+ *    The library never allocates, frees or keeps them.  Kernels launch on the
+ *    calling thread's current device (cudaGetDevice), so every device buffer
+ *    of a call must be that device's memory.
  *  - Calls are asynchronous on `stream` and never synchronise it (only
  *    qsa_debug_check does).  Results are deterministic: identical inputs give
  *    bit-identical outputs.

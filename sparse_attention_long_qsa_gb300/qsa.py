@@ -146,6 +146,10 @@ def _ptr(t, dtype, name, allow_none=False):
         raise TypeError(f"{name} must be a torch tensor")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor (libqsa has no CPU path)")
+    if t.get_device() != torch.cuda.current_device():
+        # the library launches on the current device: another device's
+        # memory would be read through an address that is not mapped there
+        raise ValueError(f"{name} is on {t.device}, the current device is cuda:{torch.cuda.current_device()}")
     if dtype is not None and t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
