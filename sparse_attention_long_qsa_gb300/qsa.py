@@ -9,6 +9,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import threading
 from typing import Optional
 
 import numpy as np
@@ -50,6 +51,7 @@ class Config(ctypes.Structure):
 
 
 _lib = None
+_lib_lock = threading.Lock()
 _P = ctypes.c_void_p
 _I32 = ctypes.c_int32
 _I64 = ctypes.c_int64
@@ -57,7 +59,15 @@ _SZ = ctypes.c_size_t
 
 
 def lib():
-    """Load libqsa.so (built in-tree by sparse_attention_long_qsa_gb300.build)."""
+    """Load libqsa.so (built in-tree by sparse_attention_long_qsa_gb300.build);
+    safe to call from several threads."""
+    if _lib is not None:
+        return _lib
+    with _lib_lock:
+        return _load()
+
+
+def _load():
     global _lib
     if _lib is not None:
         return _lib
