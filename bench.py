@@ -42,13 +42,19 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "QSA-layer decode tokens/s at 50k/250k ctx (1 and 5 seqs); HBM GB/s vs peak"
-# DRAM bytes (read + write) of one launch of a workload's roofline kernel,
-# from an ncu capture of the current kernel (profiles/<kernel>_<workload>.md);
-# a workload or kernel missing here reports null.  Update or remove an entry
-# whenever the kernel changes.
-NCU_TRAFFIC = {
-    ("50k", "score"): 6_688_256,           # profiles/k_score_50k.md
-    ("5x250k_q8", "score"): 169_715_456,   # profiles/k_score_5x250k.md
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
+# a workload's roofline kernel, taken by ncu from the kernel built from the
+# sources whose hash is stored beside it.  The line reports the number only
+# while the kernel's sources still hash to that value (null otherwise, and for
+# a workload or kernel without an entry).
+NCU_TRAFFIC = {}
+KERNEL_SOURCES = {
+    "append": ("append.cu", "pool_row.cuh", "qsa_internal.cuh"),
+    "pool": ("pool.cu", "pool_row.cuh", "qsa_internal.cuh"),
+    "score": ("index.cu", "tc_util.cuh", "qsa_internal.cuh"),
+    "hist": ("index.cu", "qsa_internal.cuh"),
+    "select": ("index.cu", "qsa_internal.cuh"),
+    "attn": ("attn.cu", "tc_util.cuh", "qsa_internal.cuh"),
 }
 FLUSH_BYTES = [1 << 30]   # L2 flush buffer (--flush-mb)
 FLUSH_READ_BYTES = 256 << 20   # read after the flush write (> the 129 MB L2)
@@ -64,6 +70,37 @@ DESCR = {
     "verify5_250k_q8": "verify batch, 1 seq, 250,000-cell q8_0 K/V prompt + 5 consecutive query tokens/step, "
                        "same heads, top_k=2048",
 }
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """sha256 (first 16 hex digits) of the CUDA sources a kernel is built from."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "sparse_attention_long_qsa_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str, kernel: str):
+    """(bytes, source note) of the stored ncu traffic of this kernel build, or
+    (None, reason)."""
+    e = NCU_TRAFFIC.get((workload, kernel))
+    if e is None:
+        return None, "no ncu capture of this kernel on this workload"
+    if e["source"] != kernel_source_hash(kernel):
+        return None, "the kernel's sources changed since its ncu capture"
+    return e["bytes"], ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch "
+                        f"({e['capture']}; sources {e['source']})")
+
+
+L2_NOTE = ("GPU arm: L2 flushed before every step (a 1 GiB write, then a 256 MiB read of its head so that "
+           "no dirty line is left), outside the step's events")
+
+
+def bench_config(name: str, tokens_per_step: int) -> dict:
+    """The `config` object of both arms' lines (identical for the same workload)."""
+    return {"workload": DESCR[name], "name": name, "tokens_per_step": int(tokens_per_step), "l2": L2_NOTE}
 
 
 def _env_rank():
@@ -186,8 +223,7 @@ class OracleRunner:
 
     def __init__(self, wl, max_tokens_per_step: int = 8):
         from oracle import qsa_oracle as O
-        from sparse_attention_long_qsa_gb300.layer import append_rows
-        self.O, self.append_rows, self.wl = O, append_rows, wl
+        self.O, self.wl = O, wl
         self.cap = max_tokens_per_step
         cfg = wl.cfg
         self.table0 = wl.blk_cells_state(0)
@@ -274,7 +310,7 @@ def run_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": DESCR[args.config], "name": args.config},
+        "config": bench_config(args.config, len(wl.steps[0].tok_pos)),
         "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -489,6 +525,52 @@ def replica_value(local_ms: float, tokens: int, world: int, dist=None, device="c
     return world * tokens / (local_ms / 1e3), local_ms
 
 
+def launch_note(res, path):
+    return ("the K timed steps captured as one CUDA graph (per step: L2 flush, start event, "
+            + ("qsa_kv_append (re-pooling the blocks it dirties) + qsa_index_topk + qsa_sparse_attn"
+               if path == "full" else
+               "table append outside the events, qsa_pool_update + qsa_index_topk + qsa_sparse_attn")
+            + f" = {res['launches_per_step']} kernels ({', '.join(res['kernels'])})"
+            + " chained by programmatic dependent launch, end event), replayed once")
+
+
+def roofline_of(res, name, hbm, peak_src):
+    """The roofline object of a measured workload: its dominant kernel's
+    algorithmic bytes over that kernel's live event time."""
+    achieved = res["dom_bytes"] / (res["dom_ms"] * 1e-3) / 1e9
+    traffic, tsrc = ncu_traffic(name, res["dominant"])
+    return {"kernel": res["dominant"], "choice": "kernel moving the most algorithmic bytes per step",
+            "longest_kernel": res["longest"], "bound": "hbm", "achieved": achieved,
+            "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+            "peak_source": f"hbm_gbs {peak_src}",
+            "bytes_per_launch": res["dom_bytes"], "us_per_launch": res["dom_ms"] * 1e3,
+            "traffic": traffic, "traffic_source": tsrc}
+
+
+def workload_line(res, name, hbm, peak_src, cpu=None):
+    """Per-workload results: throughput, end to end, roofline, kernel times."""
+    return {
+        "workload": DESCR[name], "value": res["value"], "unit": "tokens/s",
+        "ms_per_step": res["ms_per_step"],
+        "step_us_p50": res["step_us_p50"], "step_us_p90": res["step_us_p90"],
+        "e2e": res.get("e2e"), "cpu_baseline": cpu,
+        "roofline": roofline_of(res, name, hbm, peak_src),
+        "kernels_us": {k: round(v, 3) for k, v in res["kern_us"].items()},
+        "kernels_gbs": {k: round(v, 1) for k, v in res["kern_gbs"].items()},
+        "step_bytes": res["step_bytes"],
+        "step_gbs": res["step_bytes"] / (res["ms_per_step"] * 1e-3) / 1e9,
+    }
+
+
+def cpu_line(wl, name, seconds):
+    rate, steps, secs, threads = cpu_oracle_rate(wl, seconds)
+    per = min(len(wl.steps[0].tok_pos), 8)
+    return {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{steps} consecutive steps of the {name} workload, full oracle step each (append, "
+                      f"pool the dirty blocks, score every block, select, expand, attend {per} token(s)), "
+                      f"{secs:.1f} s"}
+
+
 def run_native(args, rank, world, local):
     import torch
     import __graft_entry__
@@ -523,72 +605,55 @@ def run_native(args, rank, world, local):
                         "launches_per_step": ro["launches_per_step"],
                         "kernels_us": {k: round(v, 3) for k, v in ro["kern_us"].items()}}
 
+    # the 250k q8_0 decode (the long-context target) on a complete line of its
+    # own: end to end, CPU baseline, roofline
+    target = None
+    if args.target and args.target != args.config and rank == 0:
+        rt = measure_config(args.target, min(args.steps, 256), args.warmup, dev, path=args.path)
+        cpu_t = None if args.no_cpu else cpu_line(rt["wl"], args.target, args.cpu_seconds)
+        target = workload_line(rt, args.target, hbm, peak_src, cpu_t)
+        target["config"] = bench_config(args.target, len(rt["wl"].steps[0].tok_pos))
+        del rt
+
     secondary = {}
     if args.secondary and rank == 0:
         for name in args.secondary.split(","):
-            if name == args.config or name in ("", "none"):
+            if name in (args.config, args.target, "", "none"):
                 continue
             r2 = measure_config(name, min(args.steps, 128), args.warmup, dev, path=args.path, e2e=False)
-            secondary[name] = {
-                "workload": DESCR[name], "value": r2["value"], "unit": "tokens/s",
-                "ms_per_step": r2["ms_per_step"],
-                "kernels_us": {k: round(v, 3) for k, v in r2["kern_us"].items()},
-                "kernels_gbs": {k: round(v, 1) for k, v in r2["kern_gbs"].items()},
-                "dominant": r2["dominant"], "longest": r2["longest"],
-                "dominant_frac_of_hbm": r2["dom_bytes"] / (r2["dom_ms"] * 1e-3) / 1e9 / hbm,
-                "dominant_traffic": NCU_TRAFFIC.get((name, r2["dominant"])),
-            }
+            secondary[name] = workload_line(r2, name, hbm, peak_src)
+            del r2
 
     cpu = None
     if rank == 0 and not args.no_cpu:
-        rate, steps, secs, threads = cpu_oracle_rate(res["wl"], args.cpu_seconds)
-        cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-               "sample": f"{steps} consecutive decode steps of the {args.config} workload, full oracle "
-                         f"step each (pool dirty block, score all blocks, select, expand, attend), "
-                         f"{secs:.1f} s"}
+        cpu = cpu_line(res["wl"], args.config, args.cpu_seconds)
     if rank != 0:
         if dist:
             dist.destroy_process_group()
         return
     wl = res["wl"]
-    achieved = res["dom_bytes"] / (res["dom_ms"] * 1e-3) / 1e9
+    main_line = workload_line(res, args.config, hbm, peak_src, cpu)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16" if wl.cfg["kv_type"] == "f16" else "q8_0",
         "data": "synthetic (seeded N(0,1) K/V/keys, U(0,1) weights)",
-        "config": {"workload": DESCR[args.config], "name": args.config,
-                   "tokens_per_step": len(wl.steps[0].tok_pos),
-                   "path": args.path,
-                   "launch": ("the K timed steps captured as one CUDA graph (per step: L2 flush, start event, "
-                              + ("qsa_kv_append (re-pooling the blocks it dirties) + qsa_index_topk + "
-                                 "qsa_sparse_attn"
-                                 if args.path == "full" else
-                                 "table append outside the events, qsa_pool_update + qsa_index_topk + "
-                                 "qsa_sparse_attn")
-                              + f" = {res['launches_per_step']} kernels ({', '.join(res['kernels'])})"
-                              + " chained by programmatic dependent launch, end event), replayed once"),
-                   "l2": (f"flushed before every step ({FLUSH_BYTES[0] >> 20} MiB write, then a {FLUSH_READ_BYTES >> 20} MiB "
-                          "read of its head so that no dirty line is left), outside the step's events"),
+        "config": bench_config(args.config, len(wl.steps[0].tok_pos)),
+        "launch": {"path": args.path, "steps": launch_note(res, args.path),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "roofline": {"kernel": res["dominant"], "choice": "kernel moving the most algorithmic bytes per step",
-                     "longest_kernel": res["longest"], "bound": "hbm", "achieved": achieved,
-                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "peak_source": f"hbm_gbs {peak_src}",
-                     "bytes_per_launch": res["dom_bytes"], "us_per_launch": res["dom_ms"] * 1e3,
-                     "traffic": NCU_TRAFFIC.get((args.config, res["dominant"])),
-                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch"},
+        "roofline": main_line["roofline"],
         "step_us_p50": res["step_us_p50"], "step_us_p90": res["step_us_p90"],
-        "kernels_us": {k: round(v, 3) for k, v in res["kern_us"].items()},
-        "kernels_gbs": {k: round(v, 1) for k, v in res["kern_gbs"].items()},
+        "kernels_us": main_line["kernels_us"],
+        "kernels_gbs": main_line["kernels_gbs"],
         "step_bytes": res["step_bytes"],
-        "step_gbs": res["step_bytes"] / (res["ms_per_step"] * 1e-3) / 1e9,
+        "step_gbs": main_line["step_gbs"],
         "cpu_baseline": cpu,
         "e2e": res.get("e2e"),
         "gpu_launches": res["launches_per_step"] * args.steps,
         "paths": paths,
         "clocks": res["clocks"],
+        "target": target,
         "secondary": secondary or None,
     }
     print(json.dumps(line), flush=True)
@@ -603,7 +668,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--config", default="50k", choices=list(DESCR))
-    ap.add_argument("--secondary", default="250k_q8,5x250k_q8",
+    ap.add_argument("--target", default="250k_q8",
+                    help="workload given a complete line of its own under `target` (rank 0; '' for none)")
+    ap.add_argument("--secondary", default="250k_f16,5x250k_q8",
                     help="comma list of further workloads timed on rank 0 ('none': no others)")
     ap.add_argument("--path", default="full", choices=["full", "calls"],
                     help="full: append (with the pool update) + index + attention (the layer's whole step); "

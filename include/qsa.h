@@ -152,7 +152,11 @@ qsa_status qsa_kv_append(const qsa_config* cfg, int32_t n_new,
  *   out = NeoX RoPE of x at position slot_block_idx[s] * r, theta = rope_theta
  *         (pair (d, d + idx_dim/2) turns by pos * theta^(-2d/idx_dim))
  *   pooled[s] = out (fp32).  A slot with no present cell gets zeros.
- * Only the dirty rows of `pooled` are written.  Computed in fp64, rounded once.
+ * Only the dirty rows of `pooled` are written.  Mean and RMSNorm are fp32;
+ * the rotation angle is reduced exactly in integers (each frequency a 64-bit
+ * fixed-point fraction of a turn, computed on the host) and only the
+ * remaining fraction of a turn goes through fp32 sincospi.  No fp64 runs on
+ * the device.
  * Errors: QSA_ERR_INVALID_ARG (null pointer with n_dirty > 0, negative sizes),
  * QSA_ERR_UNSUPPORTED (geometry).  A dirty slot >= n_slots or a member cell
  * >= n_cells is skipped and flagged in the device error word. */
@@ -243,9 +247,11 @@ qsa_status qsa_index_topk(const qsa_config* cfg, int32_t n_tokens, int32_t max_t
  * Limits: n_tokens <= 8 and max_blocks <= 262144 (1,048,576 cells per
  * sequence at r = 4); larger calls return QSA_ERR_WORKSPACE and launch
  * nothing.  The array takes 9 MiB on every GPU that loads the library, until
- * the process exits.  The first call on a device looks up the array's device
- * address (cudaGetSymbolAddress, with that device current) and caches it:
- * make that first call before any stream capture.  All calls on a device share
+ * the process exits.  Every call looks up the array's address in the current
+ * device's context (cudaGetSymbolAddress, as every call of the library looks
+ * up its device error word); nothing is cached between calls, so the call
+ * stays valid after cudaDeviceReset or under another context for the same
+ * device.  All calls on a device share
  * the one array: calls whose work overlaps on the GPU (other streams, other
  * host threads) race and corrupt each other's results; serialise them.  Each
  * call clears the part of the array that must start at zero. */

@@ -3,7 +3,6 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
-#include <mutex>
 
 #include "qsa_internal.cuh"
 
@@ -320,33 +319,24 @@ const char* qsa_status_string(qsa_status s) {
 //
 // The array lives in this library's device image: every GPU that loads the
 // library holds kNoAllocScratchBytes of it until the process exits.  Host code
-// cannot use the symbol as a device address, so the device address is looked
-// up once per device (with that device current) and cached.
+// cannot use the symbol as a device address; the address belongs to the
+// current device's context, so every call looks it up with its device current
+// (as the error word is looked up), and nothing is cached between calls.
 namespace {
 
 constexpr int kNoAllocMaxTokens = 8;
 constexpr int64_t kNoAllocMaxBlocks = 262144;        // 1,048,576 cells per sequence at r = 4
 constexpr size_t kNoAllocScratchBytes = 9u << 20;    // >= the workspace of 8 tokens x 262144 blocks
-constexpr int kNoAllocMaxDevices = 256;
+static_assert(qsa::index_workspace_bytes_max(kNoAllocMaxTokens, kNoAllocMaxBlocks) <= kNoAllocScratchBytes,
+              "the scratch array holds the workspace of the largest call it accepts");
 
 __device__ __align__(256) unsigned char g_qsa_noalloc_scratch[kNoAllocScratchBytes];
 
-std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
-
-// Device address of the scratch array on the current device (set-up on the
-// first call per device).
+// Device address of the scratch array in the current device's context.
 qsa_status noalloc_scratch(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return QSA_ERR_CUDA;
-  if (dev < 0 || dev >= kNoAllocMaxDevices) return QSA_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (g_noalloc_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_qsa_noalloc_scratch) != cudaSuccess || p == nullptr) return QSA_ERR_CUDA;
-    g_noalloc_ptr[dev] = p;
-  }
-  *out = g_noalloc_ptr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_qsa_noalloc_scratch) != cudaSuccess || p == nullptr) return QSA_ERR_CUDA;
+  *out = p;
   return QSA_OK;
 }
 

@@ -18,6 +18,8 @@
 // rows are inputs, not outputs of the preceding kernel); only the stores wait.
 #include "pool_row.cuh"
 
+QSA_TS_DECLARE(append)
+
 namespace qsa {
 namespace {
 
@@ -83,6 +85,11 @@ __device__ __forceinline__ int token_slot(const AppendArgs& a, int t, int* in_bl
 
 __global__ void __launch_bounds__(kAppThreads)
 k_append(const AppendArgs a, const Turns turns, unsigned* err) {
+  QSA_TS_SCOPE_LAST(append, 1);
+  QSA_TS(append, 0);
+  // The successor may launch at once: the index kernels read nothing this
+  // launch writes before their own dependency wait (see qsa_internal.cuh).
+  grid_dep_launch();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (blockIdx.x == gridDim.x - 1) {
     // ---- the dirty list (n_new <= kAppendMaxTokens, 4 tokens per thread)
@@ -130,7 +137,7 @@ k_append(const AppendArgs a, const Turns turns, unsigned* err) {
       rank[k] = below;
     }
     grid_dep_wait();
-    grid_dep_launch();
+    QSA_TS_IF(append, 2, tid == 0);
 #pragma unroll
     for (int k = 0; k < kAppendMaxTokens / kAppThreads; ++k)
       if (rank[k] >= 0 && rank[k] < a.n_dirty) {
@@ -204,7 +211,6 @@ k_append(const AppendArgs a, const Turns turns, unsigned* err) {
     const uint4 raw = ok ? __ldg(reinterpret_cast<const uint4*>(src) + lane) : make_uint4(0, 0, 0, 0);
     if (!a.kv_q8) {
       grid_dep_wait();
-      grid_dep_launch();
       if (ok) reinterpret_cast<uint4*>(cache + (c * a.G + g) * kHeadDim * 2)[lane] = raw;
       return;
     }
@@ -238,7 +244,6 @@ k_append(const AppendArgs a, const Turns turns, unsigned* err) {
       qb[i] = (signed char)(v < 0.f ? -(int)m : (int)m);
     }
     grid_dep_wait();
-    grid_dep_launch();
     if (ok) {
       reinterpret_cast<uint2*>(cache + (c * a.G + g) * kHeadDim)[lane] = qs;
       if ((lane & 3) == 0) {
@@ -252,7 +257,6 @@ k_append(const AppendArgs a, const Turns turns, unsigned* err) {
   uint4 raw = make_uint4(0, 0, 0, 0);
   if (ok && lane < 16) raw = __ldg(reinterpret_cast<const uint4*>(a.idx_new + (int64_t)t * kIdxDim) + lane);
   grid_dep_wait();
-  grid_dep_launch();
   if (!ok) return;
   if (lane < 16) reinterpret_cast<uint4*>(a.idx_k + c * kIdxDim)[lane] = raw;
   if (lane == 0) a.blk_cells[(int64_t)slot * a.r + ib] = (int32_t)c;

@@ -137,6 +137,7 @@ __device__ __forceinline__ uint4 dq8(uint2 raw, __half2 s2) {
 template <bool kQ8, bool kPipe>
 __global__ void __launch_bounds__(kThreads, 1)
 k_attn_tc(const AttnArgs a, unsigned* err) {
+  QSA_TS_SCOPE_LAST(attn, 28);
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
   const uint32_t base_s = (raw_s + 1023u) & ~1023u;

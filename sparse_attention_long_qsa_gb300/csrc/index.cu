@@ -163,6 +163,24 @@ __device__ __forceinline__ unsigned block_prefix_exclusive(unsigned v, unsigned*
   return x - v + below;
 }
 
+__device__ __forceinline__ void cp_async16_ptr(void* sdst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"((uint32_t)__cvta_generic_to_shared(sdst)),
+               "l"(gsrc)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* sdst, const void* gsrc) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"((uint32_t)__cvta_generic_to_shared(sdst)),
+               "l"(gsrc)
+               : "memory");
+}
+
+// A cell id read from the block table, passed on as read (the attention masks
+// it) with the error bit set when it is out of range.
+__device__ __forceinline__ int flag_cell(int c, int64_t n_cells, unsigned* err) {
+  if (c < 0 || c >= n_cells) atomicOr(err, kErrCell);
+  return c;
+}
+
 // Unique 56-bit selection key of a block inside the threshold bin: the 20
 // low bits of the score key above the bitwise complement of the block index,
 // so a larger key means a larger score, or an equal score at a lower index.
@@ -199,6 +217,7 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
 template <bool kTopk>
 __global__ void __launch_bounds__(kScoreThreads, 2)
 k_score(const IndexArgs a, void* ws, float* __restrict__ scores, int chunk, unsigned* err) {
+  QSA_TS_SCOPE_LAST(index, 4);
   // Shared memory: the warps' row rings, the slot ids of this CTA's range,
   // and a histogram of this CTA's scores plus the list of bins it touched (so
   // the flush to the token's global histogram costs one atomic per touched
@@ -229,11 +248,10 @@ k_score(const IndexArgs a, void* ws, float* __restrict__ scores, int chunk, unsi
   unsigned* ghist = kTopk ? hist_of(ws, t) : nullptr;
   const int32_t* slots = a.seq_blk_slots + tk.off;
   for (int i = tid; i < nrows; i += kScoreThreads) s_slot[i] = __ldg(slots + j0 + i);
-  const bool use_hint = kTopk && a.recomputed != nullptr && a.n_recomputed <= kMaxHint && blockIdx.x != 0;
+  const bool use_hint = kTopk && a.recomputed != nullptr && a.n_recomputed <= kMaxHint;
   // caller's assertion: the preceding call recomputed only blocks holding
   // the query tokens' own positions (an append of exactly these tokens)
-  const bool query_hint = kTopk && a.recomputed == nullptr && a.n_recomputed == QSA_HINT_QUERY_BLOCKS &&
-                          blockIdx.x != 0;
+  const bool query_hint = kTopk && a.recomputed == nullptr && a.n_recomputed == QSA_HINT_QUERY_BLOCKS;
   if (use_hint)
     for (int i = tid; i < a.n_recomputed; i += kScoreThreads) s_rec[i] = a.recomputed[i];
 
@@ -253,8 +271,9 @@ k_score(const IndexArgs a, void* ws, float* __restrict__ scores, int chunk, unsi
 
   // ---- pooled rows are written by the pool update.  With the list of slots
   // that update recomputed, a CTA none of whose rows is in it reads nothing
-  // the update writes and skips the wait; CTA 0 always waits, so this
-  // kernel still completes after the update.
+  // the update writes and starts scoring without waiting; CTA x = 0 of each
+  // token then waits at its end instead, so this kernel still completes after
+  // the update and every later kernel that waits on it is ordered after both.
   bool must_wait = true;
   if (use_hint) {
     int hit = 0;
@@ -379,6 +398,8 @@ k_score(const IndexArgs a, void* ws, float* __restrict__ scores, int chunk, unsi
       atomicAdd(ghist + b, s_hist[b]);
     }
   }
+  // the kernel completes only after its predecessor (see above)
+  if (!must_wait && blockIdx.x == 0) grid_dep_wait();
 }
 
 // ------------------------------------------------------------- k_score_tc
@@ -668,18 +689,21 @@ struct SelSmem {
 __global__ void __launch_bounds__(kSelThreads, 1)
 k_select(const IndexArgs a, void* ws, const float* __restrict__ scores,
          int32_t* __restrict__ cells, int32_t* __restrict__ count, unsigned* err) {
+  QSA_TS_SCOPE_LAST(index, 19);
   __shared__ SelSmem sm;
-  extern __shared__ int32_t s_dyn[];
-  int32_t* s_slots = s_dyn;                // slot ids of this CTA's range (prefetched)
-  int* s_list = s_dyn + kSelSlots;         // chosen blocks of this CTA, ascending
+  extern __shared__ __align__(16) int32_t s_dyn[];
+  int* s_list = s_dyn + kSelSlots + 4;     // chosen blocks of this CTA, ascending
   const int t = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t rank = cluster_rank(), NC = cluster_size();
   const int r = a.r;
   const int B = a.n_sel_blocks;
 
-  // ---- before the wait: geometry, this CTA's slot ids and the tail cells
-  // (block lists and the block table are not written by the score kernel)
+  // ---- before the wait: geometry only (the token ids and block lists are
+  // inputs no kernel of the library writes); the slot ids and the tail cells
+  // are fetched after the wait, under the threshold search and the
+  // classification, since the block table is written by the append that may
+  // still be running when this kernel starts
   QSA_TS(index, 10);
   const Tok tk = token_geometry(a, t, err, false);
   const int nb = tk.nb;
@@ -687,26 +711,11 @@ k_select(const IndexArgs a, void* ws, const float* __restrict__ scores,
   const int64_t j0 = (int64_t)rank * per;
   const int64_t j1 = min((int64_t)nb, j0 + per);
   const int nwords = j1 > j0 ? (int)ceil_div(j1 - j0, 32) : 0;
-  const bool slots_cached = per <= kSelSlots;
-  const bool all_cached = rank == 0 && nb <= kSelSlots;   // CTA 0 holds every slot id
   const int32_t* slots = a.seq_blk_slots + tk.off;
-  if (all_cached) {
-    for (int64_t j = tid; j < nb; j += kSelThreads) s_slots[j] = slots[j];
-  } else if (slots_cached) {
-    for (int64_t j = j0 + tid; j < j1; j += kSelThreads) s_slots[j - j0] = slots[j];
-  }
   int tail = 0;
   if (tk.ok && tk.nb == tk.nb_full) tail = tk.p + 1 - (int)(tk.nb_full * r);
   const bool tail_missing = tail > 0 && tk.nb_full >= tk.len;
   if (tail_missing) tail = 0;
-  if (rank == 0 && tid < tail) {
-    const int slot = slots[tk.nb_full];
-    const bool sok = slot >= 0 && slot < a.n_slots;
-    if (!sok) atomicOr(err, kErrSlot);
-    const int cidx = sok ? a.blk_cells[(int64_t)slot * r + tid] : -1;
-    if (cidx < 0 || cidx >= a.n_cells) atomicOr(err, kErrCell);
-    sm.tail_cells[tid] = cidx;
-  }
   if (tid == 0) {
     sm.ncand = 0u;
     sm.ncent = 0u;
@@ -731,6 +740,8 @@ k_select(const IndexArgs a, void* ws, const float* __restrict__ scores,
     const int64_t j = j0 + (int64_t)w * 32 + lane;
     v0[b] = (w < nwords && j < j1) ? __ldcg(srow + j) : -INFINITY;
   }
+  // the tail block's slot (its member cells are copied once it arrives)
+  const int tslot = (rank == 0 && tid < tail) ? slots[tk.nb_full] : -1;
   {
     constexpr int kPer = kHistBins / kSelThreads;   // 8 consecutive bins per thread, 2 vector loads
     static_assert(kPer == 8, "histogram split");
@@ -767,6 +778,25 @@ k_select(const IndexArgs a, void* ws, const float* __restrict__ scores,
   }
   const int thr = sm.thr, ncand_all = sm.ncand_all;
   const bool fast = thr < 0 || ncand_all <= kSelLocalCand;
+  // Which path resolves the cut (central: CTA 0 ranks, orders and expands
+  // alone), and the slot ids the expansion will read (copied into shared
+  // memory after the classification, waited for only before the expansion).
+  const bool central = nb <= kCentralBlocks && (thr < 0 || ncand_all <= kRankMax);
+  const bool all_cached = central && rank == 0 && nb <= kSelSlots;   // CTA 0 holds every slot id
+  const bool slots_cached = !central && per <= kSelSlots;
+  const int64_t slot_lo = all_cached ? 0 : j0, slot_hi = all_cached ? nb : j1;
+  // s_slots[j - slot_lo] = slots[j]; the array starts 0-3 ints into the
+  // buffer so that it shares the block list's alignment modulo 16 bytes
+  int32_t* s_slots = s_dyn + ((reinterpret_cast<uintptr_t>(slots + slot_lo) >> 2) & 3);
+  if (tid < tail && rank == 0) {
+    if (tslot >= 0 && tslot < a.n_slots) {
+      cp_async4(&sm.tail_cells[tid], a.blk_cells + (int64_t)tslot * r + tid);
+    } else {
+      atomicOr(err, kErrSlot);
+      sm.tail_cells[tid] = -1;
+    }
+  }
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
 
   // ---- phase A: classify this CTA's blocks
   for (int wb = 0; wb * kSelWarps * kSelBatch < nwords; ++wb) {
@@ -804,6 +834,17 @@ k_select(const IndexArgs a, void* ws, const float* __restrict__ scores,
   }
   __syncthreads();
   QSA_TS(index, 13);
+  if (all_cached || slots_cached) {
+    // 16-byte copies where the list is 16-byte aligned, single ids at the ends
+    const int64_t n = slot_hi - slot_lo;
+    const int64_t head = min(n, (int64_t)((4 - ((reinterpret_cast<uintptr_t>(slots + slot_lo) >> 2) & 3)) & 3));
+    const int64_t body = (n - head) / 4;
+    if (tid < head) cp_async4(s_slots + tid, slots + slot_lo + tid);
+    for (int64_t q = tid; q < body; q += kSelThreads)
+      cp_async16_ptr(s_slots + head + 4 * q, slots + slot_lo + head + 4 * q);
+    for (int64_t i = head + 4 * body + tid; i < n; i += kSelThreads) cp_async4(s_slots + i, slots + slot_lo + i);
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+  }
   cluster_wait();
 
   if (nb <= kCentralBlocks && (thr < 0 || ncand_all <= kRankMax)) {
@@ -910,6 +951,7 @@ k_select(const IndexArgs a, void* ws, const float* __restrict__ scores,
         bits &= bits - 1u;
       }
     }
+    asm volatile("cp.async.wait_all;\n" ::: "memory");   // slot ids and tail cells
     __syncthreads();
     QSA_TS(index, 15);
     const unsigned total = sm.sel;
@@ -930,7 +972,7 @@ k_select(const IndexArgs a, void* ws, const float* __restrict__ scores,
         crow[(int64_t)i * r + m] = cv[m];
       }
     }
-    if (tid < tail) crow[nsel * r + tid] = sm.tail_cells[tid];
+    if (tid < tail) crow[nsel * r + tid] = flag_cell(sm.tail_cells[tid], a.n_cells, err);
     if (tid == 0) {
       if (tail_missing) atomicOr(err, kErrBlockList);
       count[t] = nsel * r + tail;
@@ -1110,6 +1152,8 @@ k_select(const IndexArgs a, void* ws, const float* __restrict__ scores,
   QSA_TS(index, 14);
 
   // ---- phase C: ordered expansion of this CTA's chosen blocks at `base`
+  asm volatile("cp.async.wait_all;\n" ::: "memory");   // slot ids and tail cells
+  __syncthreads();
   unsigned mine = 0;
   for (int w = w0; w < w1; ++w) mine += __popc(sm.bitmap[w]);
   unsigned local_total = 0;
@@ -1167,7 +1211,7 @@ k_select(const IndexArgs a, void* ws, const float* __restrict__ scores,
   QSA_TS(index, 16);
   const int nsel = (int)min(total, (unsigned)B);
   if (rank == 0) {
-    if (tid < tail) crow[nsel * r + tid] = sm.tail_cells[tid];
+    if (tid < tail) crow[nsel * r + tid] = flag_cell(sm.tail_cells[tid], a.n_cells, err);
     if (tid == 0) {
       if (tail_missing) atomicOr(err, kErrBlockList);
       count[t] = nsel * r + tail;
@@ -1233,7 +1277,7 @@ cudaError_t index_setup(int* sms) {
     e = cudaFuncSetAttribute(k_score<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScoreSmem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(k_select, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(sizeof(int32_t) * (kSelSlots + kSelList)));
+                             (int)(sizeof(int32_t) * (kSelSlots + 4 + kSelList)));
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(k_score_tc<16, 32, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)TcShape<16, 32>::kSmem);
@@ -1269,8 +1313,8 @@ bool index_tiled(int n_tokens, int n_seq) { return n_tokens > 8 && n_tokens >= 2
 int64_t index_max_blocks_limit() { return (int64_t)kSelCluster * kSelMaxWords * 32; }
 
 size_t index_workspace_bytes(int max_tokens, int64_t max_blocks) {
-  return (size_t)round_up((int64_t)max_tokens * kCtrlBytes, 256) +
-         (size_t)round_up((int64_t)max_tokens * max_blocks * (int64_t)sizeof(float), 256);
+  static_assert(kCtrlBytes == (size_t)kIndexCtrlBytes, "workspace layout");
+  return (size_t)index_workspace_bytes_max(max_tokens, max_blocks);
 }
 
 void index_workspace_zero_range(int n_tokens, int64_t, size_t* offset, size_t* bytes) {
@@ -1296,7 +1340,7 @@ cudaError_t launch_index_topk(const IndexArgs& a, int32_t* cells, int32_t* count
   int sms = 0;
   cudaError_t e = index_setup(&sms);
   if (e != cudaSuccess) return e;
-  const size_t slot_bytes = sizeof(int32_t) * (kSelSlots + kSelList);
+  const size_t slot_bytes = sizeof(int32_t) * (kSelSlots + 4 + kSelList);
   IndexArgs b = a;
   b.max_blocks = a.max_blocks > 0 ? a.max_blocks : 1;
   float* sc = scores_of(ws, a.max_tokens);

@@ -48,11 +48,17 @@ __host__ __device__ __forceinline__ int64_t round_up(int64_t a, int64_t b) { ret
 // ------------------------------------------------ launch chaining, clusters
 // Programmatic dependent launch: every kernel of the library is launched with
 // programmatic stream serialisation, so it may start while its predecessor in
-// the stream finishes.  A kernel reads or writes nothing its predecessor
-// produces or consumes before grid_dep_wait() (which returns once the
-// predecessor grid has completed and its memory is visible), and lets its own
-// successor launch (grid_dep_launch) only after that wait, so a successor's
-// early part never overlaps anything but this kernel.
+// the stream finishes.  Before grid_dep_wait() (which returns once the
+// predecessor grid has completed and its memory is visible) a kernel writes
+// nothing outside its own shared memory and reads only the call's inputs that
+// no kernel of the library writes (token ids and positions, queries and
+// weights, sequence block lists, the new rows of an append, a host-written
+// hint).  Most kernels let their successor launch (grid_dep_launch) right
+// after that wait; the append lets it launch at its start, and a score CTA
+// that has no row to wait for lets it launch before its own wait, which it
+// takes at its end.  Either way a kernel completes only after its
+// predecessor, so every write of a kernel is visible to any kernel that
+// waits on a later one in the stream.
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
 
@@ -149,7 +155,23 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   __device__ long long g_qsa_ts_##tu[64];                                               \
   extern "C" int qsa_probe_read_##tu(long long* host) {                                 \
     return (int)cudaMemcpyFromSymbol(host, g_qsa_ts_##tu, sizeof(long long) * 64);      \
+  }                                                                                     \
+  extern "C" int qsa_probe_reset_##tu() {                                               \
+    static const long long z[64] = {};                                                  \
+    return (int)cudaMemcpyToSymbol(g_qsa_ts_##tu, z, sizeof(z));                        \
   }
+// Latest globaltimer over every CTA of a kernel (thread 0 of each), at scope
+// exit of the enclosing block: the kernel's end as seen by its last CTA.
+#define QSA_TS_SCOPE_LAST(tu, i)                                                        \
+  struct QsaTsLast_ {                                                                   \
+    __device__ ~QsaTsLast_() {                                                          \
+      if (threadIdx.x == 0) {                                                           \
+        unsigned long long g_;                                                          \
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(g_));                          \
+        atomicMax(reinterpret_cast<unsigned long long*>(&g_qsa_ts_##tu[32 + (i)]), g_); \
+      }                                                                                 \
+    }                                                                                   \
+  } qsa_ts_last_
 #define QSA_TS_IF(tu, i, cond)                                                          \
   do {                                                                                  \
     if (cond) {                                                                         \
@@ -165,6 +187,9 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 #define QSA_TS_DECLARE(tu)
 #define QSA_TS_IF(tu, i, cond) \
   do {                         \
+  } while (0)
+#define QSA_TS_SCOPE_LAST(tu, i) \
+  do {                           \
   } while (0)
 #define QSA_TS(tu, i) \
   do {                \
@@ -221,6 +246,13 @@ struct IndexArgs {
   int n_recomputed;
 };
 
+// Workspace of qsa_index_topk: a 4096-bin histogram per token (the control
+// words, zero between calls), then the fp32 scores [max_tokens][max_blocks],
+// each part 256-byte aligned.
+constexpr int64_t kIndexCtrlBytes = (int64_t)sizeof(unsigned) * kHistBins;
+__host__ __device__ constexpr int64_t index_workspace_bytes_max(int64_t max_tokens, int64_t max_blocks) {
+  return (max_tokens * kIndexCtrlBytes + 255) / 256 * 256 + (max_tokens * max_blocks * 4 + 255) / 256 * 256;
+}
 size_t index_workspace_bytes(int max_tokens, int64_t max_blocks);
 // Whether qsa_index_topk / qsa_index_scores score with the token-tiled kernel
 // (tokens share sequences: more than 8 tokens and 2 per sequence on average).

@@ -2,8 +2,9 @@
 compare with the CPU oracle under the stated tolerances.
 
 Tolerances (stated once, used everywhere):
-  pooled keys   GPU: fp32 mean/RMS, fp64 angle reduction, fp32 sincos of the
-                reduced angle; oracle: float64 throughout:
+  pooled keys   GPU: fp32 mean/RMS, the angle reduced exactly in 64-bit
+                fixed-point turns (integer arithmetic), fp32 sincospi of the
+                remaining fraction of a turn; oracle: float64 throughout:
                 |gpu - oracle| <= 1e-6 * max|row|
   scores        fp32 GPU vs float64 oracle over the same pooled keys:
                 |gpu - oracle| <= 1e-5 * |oracle| + 1e-6 * max|row|

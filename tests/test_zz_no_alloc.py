@@ -53,6 +53,34 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls():
     assert st == 0, hex(flags)
 
 
+def test_noalloc_at_its_limits():
+    """8 tokens (one per sequence) with max_blocks = 262,144: the largest call
+    the scratch array takes, so the token scores use its last rows.  Two calls
+    in a row match qsa_index_topk run with a workspace of the same layout."""
+    wl = make_workload(n_seq=8, prompt_len=[2_001 + 997 * s for s in range(8)], n_steps=2, seed=23,
+                       shuffled=True)
+    L = QSALayer.from_workload(wl, 0, max_tokens=8)
+    L.max_blocks = 262_144
+    L.ws_index = torch.zeros(qsa.index_topk_workspace_size(L.cfg, 8, L.max_blocks), dtype=torch.uint8,
+                             device="cuda")
+    L.warm(torch.from_numpy(wl.prompt_dirty()).cuda())
+    T = len(wl.steps[0].tok_pos)
+    assert T == 8
+    for i in range(2):
+        L.set_cells(*append_rows(wl, i))
+        inp = step_inputs(wl.steps[i])
+        L.pool_update(inp["dirty"])
+        L.index_topk(inp["tok_seq"], inp["tok_pos"], inp["q_idx"], inp["w_idx"])
+        cells = torch.full((T, L.pitch), 7, dtype=torch.int32, device="cuda")
+        count = torch.full((T,), -5, dtype=torch.int32, device="cuda")
+        assert _noalloc(L, inp, cells, count) == 0
+        torch.cuda.synchronize()
+        assert torch.equal(count, L.count[:T]), (count, L.count[:T])
+        assert torch.equal(cells, L.cells[:T])
+    st, flags = qsa.debug_check()
+    assert st == 0, hex(flags)
+
+
 def test_noalloc_rejects_sizes_beyond_its_scratch():
     wl = make_workload(n_seq=1, prompt_len=100, n_steps=1, seed=22)
     L = QSALayer.from_workload(wl, 0, max_tokens=9)
