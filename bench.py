@@ -6,8 +6,8 @@
 A step is one decode step of one QSA layer over all sequences of the
 workload, through the C ABI on one stream: qsa_kv_append (the step's new
 cells, the device dirty list and the re-pooling of the dirtied blocks) ->
-qsa_index_topk (score, select, expand) -> qsa_sparse_attn (attention with its
-split merge).  --path calls times qsa_pool_update -> qsa_index_topk ->
+qsa_index_attn (score, select with expansion, attention with the split
+merge).  --path calls times qsa_pool_update -> qsa_index_topk ->
 qsa_sparse_attn with the table appended outside the timed region instead.
 Inputs are resident in HBM when the timed region starts; L2 is flushed
 before every step, outside the per-step events: a 1 GiB write, then a
@@ -51,10 +51,11 @@ NCU_TRAFFIC = {}
 KERNEL_SOURCES = {
     "append": ("append.cu", "pool_row.cuh", "qsa_internal.cuh"),
     "pool": ("pool.cu", "pool_row.cuh", "qsa_internal.cuh"),
-    "score": ("index.cu", "tc_util.cuh", "qsa_internal.cuh"),
-    "hist": ("index.cu", "qsa_internal.cuh"),
-    "select": ("index.cu", "qsa_internal.cuh"),
-    "attn": ("attn.cu", "tc_util.cuh", "qsa_internal.cuh"),
+    "score": ("index.cu", "index_util.cuh", "tc_util.cuh", "qsa_internal.cuh"),
+    "hist": ("index.cu", "index_util.cuh", "qsa_internal.cuh"),
+    "select": ("index.cu", "index_util.cuh", "qsa_internal.cuh"),
+    "attn": ("attn.cu", "index_util.cuh", "tc_util.cuh", "qsa_internal.cuh"),
+    "select_attn": ("attn.cu", "index_util.cuh", "tc_util.cuh", "qsa_internal.cuh"),
 }
 FLUSH_BYTES = [1 << 30]   # L2 flush buffer (--flush-mb)
 FLUSH_READ_BYTES = 256 << 20   # read after the flush write (> the 129 MB L2)
@@ -343,7 +344,7 @@ class _ExternalEvents:
             raise RuntimeError(f"cudaEventRecordWithFlags failed: {st}")
 
 
-def measure_config(name, K, W, dev, *, path="full", e2e=True, clocks=None):
+def measure_config(name, K, W, dev, *, path="full", e2e=True, clocks=None, in_cluster=False):
     """Time K decode steps of workload `name` on the device.  The K timed
     steps are captured as ONE CUDA graph: per step an L2 flush (write, then
     read; outside the step's events), a start event node, the step, an end event node.  Path
@@ -375,17 +376,24 @@ def measure_config(name, K, W, dev, *, path="full", e2e=True, clocks=None):
     rsum = torch.zeros((), dtype=torch.float32, device=dev)
     toks = [len(st.tok_pos) for st in wl.steps]
     alg = [algorithmic_bytes(wl, i) for i in range(n_steps)]
-    # path "full": the append kernel also re-pools the blocks it dirties
-    index_k = qsa.index_topk_kernels(toks[0], wl.n_seq)   # score (+ hist), select
-    kernels = (["append"] if full else ["pool"]) + index_k + ["attn"]
+    # path "full": the append kernel also re-pools the blocks it dirties, and
+    # one qsa_index_attn call scores, selects and attends (the selection inside
+    # the attention clusters where its limits hold)
+    if full:
+        kernels = ["append"] + qsa.index_attn_kernels(L.cfg, toks[0], wl.n_seq, L.max_blocks,
+                                                      in_cluster=in_cluster)
+    else:
+        kernels = ["pool"] + qsa.index_topk_kernels(toks[0], wl.n_seq) + ["attn"]
     for a in alg:
         if full:
             a["append"] += a.pop("pool")
         else:
             a.pop("append")
-        if "hist" not in index_k:
+        if "hist" not in kernels:
             a.pop("hist")
-    step_fn = L.full_step if full else L.step
+        if "select_attn" in kernels:
+            a["select_attn"] = a.pop("select") + a.pop("attn")
+    step_fn = (lambda **kw: L.full_step(**kw, in_cluster=in_cluster)) if full else L.step
     xev = _ExternalEvents()
 
     def do_append(i):
@@ -419,12 +427,16 @@ def measure_config(name, K, W, dev, *, path="full", e2e=True, clocks=None):
         ("cells", "k_new", "v_new", "idx_new") if full else ("dirty",))
     host = None
     if e2e:
-        # each step's inputs packed in one pinned buffer: one host-to-device
-        # copy per step into one device buffer whose views feed the calls
+        # each step's inputs packed in one pinned host buffer.  Path "full":
+        # the kernels read them in place over the host link and the attention
+        # writes its output straight into a pinned host buffer (no copy
+        # node); path "calls": one host-to-device copy of the packed inputs
+        # and one device-to-host copy of the output per step.
         staging = PackedInputs({k: (tuple(inputs[0][k].shape), inputs[0][k].dtype) for k in io_keys}, device=dev)
         host = []
         for i, st in enumerate(wl.steps):
             h = {"in": staging.pack({k: getattr(st, k) for k in io_keys})}
+            h["views"] = staging.host_views(h["in"])
             h["out"] = torch.empty((toks[i], wl.cfg["n_q_heads"], wl.cfg["head_dim"]),
                                    dtype=torch.float32).pin_memory()
             host.append(h)
@@ -448,12 +460,15 @@ def measure_config(name, K, W, dev, *, path="full", e2e=True, clocks=None):
                     qsa.profile_kernel(k, a, b)
                 xev.record(ev[n][0])
                 d = inputs[i]
-                if with_io:
-                    staging.upload(host[i]["in"])
-                    d = {**d, **staging.views}
-                step_fn(**d)
-                if with_io:
-                    host[i]["out"].copy_(L.out[:toks[i]], non_blocking=True)
+                if with_io and full:
+                    step_fn(**{**d, **host[i]["views"]}, out=host[i]["out"])
+                else:
+                    if with_io:
+                        staging.upload(host[i]["in"])
+                        d = {**d, **staging.views}
+                    step_fn(**d)
+                    if with_io:
+                        host[i]["out"].copy_(L.out[:toks[i]], non_blocking=True)
                 xev.record(ev[n][1])
         for k in hook:
             qsa.profile_kernel(k, None, None)
@@ -497,13 +512,21 @@ def measure_config(name, K, W, dev, *, path="full", e2e=True, clocks=None):
                step_us_p50=1e3 * float(np.median(ms)), step_us_p90=1e3 * float(np.percentile(ms, 90)))
 
     if e2e:
-        # the same steps from pinned host buffers: inputs H2D and the output
-        # D2H inside each step's events
+        # the same steps with the inputs in pinned host memory and the output
+        # going back to it, inside each step's events
         ms2, _ = run_graph(idx, with_io=True)
-        h2d = float(staging.nbytes)
+        h2d = float(sum(n for (_, _, _, n) in staging.fields.values()))
         d2h = float(np.mean([host[i]["out"].numel() * 4 for i in idx]))
         res["e2e"] = {"value": tokens / (float(np.sum(ms2)) / 1e3), "unit": "tokens/s",
-                      "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+                      "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                      "how": ("the step's inputs in pinned host memory, read in place by the kernels over NVLink-C2C; "
+                              "the output stored by the attention kernel into pinned host memory"
+                              if full else "one copy of the packed inputs to the device and one copy of the "
+                              "output back per step, inside the step's events")}
+        # the host sees the last step's output as the device-input run wrote it
+        last = idx[-1]
+        if full and not torch.equal(host[last]["out"], L.out[:toks[last]].cpu()):
+            raise RuntimeError("the in-place host-memory step differs from the device-memory step")
     res["clocks"] = clocks.stop() if clocks else None
     st, flags = qsa.debug_check()
     if st != 0:
@@ -527,7 +550,7 @@ def replica_value(local_ms: float, tokens: int, world: int, dist=None, device="c
 
 def launch_note(res, path):
     return ("the K timed steps captured as one CUDA graph (per step: L2 flush, start event, "
-            + ("qsa_kv_append (re-pooling the blocks it dirties) + qsa_index_topk + qsa_sparse_attn"
+            + ("qsa_kv_append (re-pooling the blocks it dirties) + qsa_index_attn"
                if path == "full" else
                "table append outside the events, qsa_pool_update + qsa_index_topk + qsa_sparse_attn")
             + f" = {res['launches_per_step']} kernels ({', '.join(res['kernels'])})"

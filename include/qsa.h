@@ -19,6 +19,15 @@
  *    The library never allocates, frees or keeps them.  Kernels launch on the
  *    calling thread's current device (cudaGetDevice), so every device buffer
  *    of a call must be that device's memory.
+ *  - A step's own inputs and outputs (q_idx, w_idx, tok_seq, tok_pos, q and
+ *    out; for qsa_kv_append tok_seq, tok_pos, cells, k_new, v_new and
+ *    idx_new) may instead be page-locked host memory that the device
+ *    addresses directly (cudaHostAlloc, or cudaHostRegister; with unified
+ *    addressing the host pointer itself): the kernels read and write them in
+ *    place over the host link (NVLink-C2C on a Grace system), so a step needs
+ *    no copy to or from the device.  The host must not write them (or read
+ *    `out`) before the stream has passed the calls.  Everything else is
+ *    device memory.
  *  - Calls are asynchronous on `stream` and never synchronise it (only
  *    qsa_debug_check does).  Results are deterministic: identical inputs give
  *    bit-identical outputs.
@@ -284,6 +293,50 @@ qsa_status qsa_sparse_attn(const qsa_config* cfg, int32_t n_tokens,
                            qsa_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * S2+S3+S4+S5+S6  qsa_index_attn  (issue #28734, fix summary, lever3, lever1
+ * and sparse256: block-granular top-k, then attention over only the chosen
+ * K/V set)
+ * qsa_index_topk followed by qsa_sparse_attn in one call: the arguments are
+ * the union of theirs, with their meanings, layouts and limits, and the
+ * workspace is qsa_index_topk's (same size, same zero-once contract, same
+ * scheduling hint).  Outputs: cells and count exactly as qsa_index_topk
+ * writes them, out as qsa_sparse_attn computes it.
+ * flags = 0: the two calls' kernels in order (score, selection with
+ * expansion, attention).
+ * flags = QSA_INDEX_ATTN_IN_CLUSTER: when max_blocks <= 65,536,
+ * top_k / r <= 1,024, r <= 8 and the attention's cluster size leaves each CTA
+ * at most 8 tiles of 128 cells (decode and small verify batches), the
+ * selection and the expansion of a token's blocks run inside the attention's
+ * thread-block clusters, one cluster per (token, KV head), so no kernel
+ * boundary and no global cell list separate them from the gather: the score
+ * kernels, then one kernel (otherwise as flags = 0).  The cells and counts
+ * are those of qsa_index_topk either way (the same exact selection), and the
+ * output equals the two calls' up to the rounding of the split merge.  On a
+ * GB300 this mode is slower than flags = 0 (its one large kernel waits longer
+ * for its instructions and for free SMs), so it is not the default.
+ * qsa_index_attn_kernels says which kernels a call runs.
+ * Errors: as qsa_index_topk and qsa_sparse_attn (all pointers required);
+ * QSA_ERR_INVALID_ARG for an unknown flag. */
+#define QSA_INDEX_ATTN_IN_CLUSTER 1u
+qsa_status qsa_index_attn(const qsa_config* cfg, int32_t n_tokens, int32_t max_tokens,
+                          const float* q_idx, const float* w_idx,
+                          const int32_t* tok_seq, const int32_t* tok_pos,
+                          const float* pooled, const int32_t* blk_cells, int64_t n_slots,
+                          const int64_t* seq_blk_off, const int32_t* seq_blk_slots,
+                          int32_t n_seq, int64_t max_blocks,
+                          const void* q, const void* k_cache, const void* v_cache, int64_t n_cells,
+                          int32_t* cells, int32_t* count, float* out,
+                          const int32_t* recomputed, int32_t n_recomputed, uint32_t flags,
+                          void* workspace, size_t ws_bytes, qsa_stream_t stream);
+
+/* Which kernels (bit k = kernel id k of qsa_profile_kernel) one
+ * qsa_index_attn call with these flags launches on the current device: the
+ * scores (1, plus 2 when token-tiled), then 3 and 4, or 6 (selection inside
+ * the attention clusters).  0 for an invalid configuration or no tokens. */
+uint32_t qsa_index_attn_kernels(const qsa_config* cfg, int32_t n_tokens, int32_t n_seq, int64_t max_blocks,
+                                uint32_t flags);
+
+/* ---------------------------------------------------------------------------
  * Host helpers (no GPU).
  *
  * qsa_blocks_dirty (issue #28734, fix summary, lever2: "host-side structural
@@ -313,7 +366,8 @@ qsa_status qsa_debug_check(qsa_stream_t stream, uint32_t* flags);
  * Kernel ids: 0 pool update (qsa_pool_update), 1 block scores (+ threshold
  * histogram when one token per sequence), 2 threshold histogram of
  * token-tiled scores, 3 cluster select + expansion (qsa_index_topk), 4
- * attention (qsa_sparse_attn), 5 append (qsa_kv_append).  `before`/`after`
+ * attention (qsa_sparse_attn), 5 append (qsa_kv_append), 6 selection,
+ * expansion and attention in one cluster kernel (qsa_index_attn).  `before`/`after`
  * are cudaEvent_t handles; NULL clears.  QSA_ERR_INVALID_ARG for an unknown
  * id. */
 qsa_status qsa_profile_kernel(int32_t kernel, void* before, void* after);

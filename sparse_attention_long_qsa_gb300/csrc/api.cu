@@ -214,6 +214,68 @@ qsa_status qsa_sparse_attn(const qsa_config* cfg, int32_t n_tokens, const void* 
   return from_cuda(launch_sparse_attn(a, workspace, err, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+qsa_status qsa_index_attn(const qsa_config* cfg, int32_t n_tokens, int32_t max_tokens, const float* q_idx,
+                          const float* w_idx, const int32_t* tok_seq, const int32_t* tok_pos,
+                          const float* pooled, const int32_t* blk_cells, int64_t n_slots,
+                          const int64_t* seq_blk_off, const int32_t* seq_blk_slots, int32_t n_seq,
+                          int64_t max_blocks, const void* q, const void* k_cache, const void* v_cache,
+                          int64_t n_cells, int32_t* cells, int32_t* count, float* out,
+                          const int32_t* recomputed, int32_t n_recomputed, uint32_t flags, void* workspace,
+                          size_t ws_bytes, qsa_stream_t stream) {
+  IndexArgs ia{};
+  qsa_status st = fill_index_args(cfg, n_tokens, max_tokens, q_idx, w_idx, tok_seq, tok_pos, pooled, n_slots,
+                                  seq_blk_off, seq_blk_slots, n_seq, max_blocks, &ia);
+  if (st != QSA_OK) return st;
+  if (n_cells < 0 || (flags & ~(uint32_t)QSA_INDEX_ATTN_IN_CLUSTER) != 0u) return QSA_ERR_INVALID_ARG;
+  if (n_cells > kMaxI32) return QSA_ERR_UNSUPPORTED;
+  if (n_tokens == 0) return QSA_OK;
+  if (!blk_cells || !cells || !count || !q || !k_cache || !v_cache || !out) return QSA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 4))
+    return QSA_ERR_INVALID_ARG;
+  if (workspace == nullptr || !aligned(workspace, 256) ||
+      ws_bytes < qsa_index_topk_workspace_size(cfg, max_tokens, max_blocks))
+    return QSA_ERR_WORKSPACE;
+  const bool query_hint = n_recomputed == QSA_HINT_QUERY_BLOCKS && recomputed == nullptr;
+  if ((n_recomputed < 0 && !query_hint) || (n_recomputed > 0 && recomputed == nullptr)) return QSA_ERR_INVALID_ARG;
+  ia.blk_cells = blk_cells;
+  ia.n_cells = n_cells;
+  ia.recomputed = recomputed;
+  ia.n_recomputed = n_recomputed;
+  AttnArgs a{};
+  a.n_tokens = n_tokens;
+  a.n_kv_heads = cfg->n_kv_heads;
+  a.kv_q8 = cfg->kv_type == QSA_KV_Q8_0;
+  a.q = static_cast<const __half*>(q);
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.n_cells = n_cells;
+  a.cells = cells;
+  a.cells_pitch = cfg->top_k + cfg->compress_ratio - 1;
+  a.count = count;
+  a.out = out;
+  a.attn_scale = cfg->attn_scale;
+  unsigned* err = error_word();
+  if (err == nullptr) return QSA_ERR_CUDA;
+  bool fused = false;
+  return from_cuda(launch_index_attn(ia, a, cells, count, workspace, (flags & QSA_INDEX_ATTN_IN_CLUSTER) != 0u,
+                                     err, reinterpret_cast<cudaStream_t>(stream), &fused));
+}
+
+uint32_t qsa_index_attn_kernels(const qsa_config* cfg, int32_t n_tokens, int32_t n_seq, int64_t max_blocks,
+                                uint32_t flags) {
+  if (check_cfg(cfg) != QSA_OK || n_tokens <= 0) return 0u;
+  bool fused = false;
+  if ((flags & QSA_INDEX_ATTN_IN_CLUSTER) != 0u && qsa::index_attn_plan(n_tokens, cfg->n_kv_heads, cfg->kv_type == QSA_KV_Q8_0,
+                           cfg->top_k + cfg->compress_ratio - 1, max_blocks > 0 ? max_blocks : 1,
+                           cfg->top_k / cfg->compress_ratio, cfg->compress_ratio, &fused) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0u;
+  }
+  const uint32_t scores = qsa_index_topk_kernels(n_tokens, n_seq) & ~(1u << qsa::kKFinal);
+  if (fused) return scores | (1u << qsa::kKFused);
+  return scores | (1u << qsa::kKFinal) | (1u << qsa::kKAttn);
+}
+
 qsa_status qsa_kv_append(const qsa_config* cfg, int32_t n_new, const int32_t* tok_seq, const int32_t* tok_pos,
                          const int32_t* cells, const void* k_new, const void* v_new, const void* idx_new,
                          void* k_cache, void* v_cache, void* idx_k, int64_t n_cells, int32_t* blk_cells,

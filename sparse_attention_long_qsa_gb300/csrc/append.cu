@@ -25,6 +25,7 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kAppThreads = 256;
+constexpr int kAppOffCache = 256;   // sequences whose block offsets a CTA preloads
 constexpr int kAppWarps = kAppThreads / 32;
 
 struct AppendArgs {
@@ -56,10 +57,17 @@ struct AppendArgs {
   float eps;
 };
 
-// Slot of the block holding token t's position, or -1 when any index is out
-// of range (flagged when `report`).
-__device__ __forceinline__ int token_slot(const AppendArgs& a, int t, int* in_block, unsigned* err, bool report) {
-  const int s = a.tok_seq[t], p = a.tok_pos[t], c = a.cell[t];
+// A new token's sequence, position and cell.
+struct NewTok {
+  int s, p, c;
+};
+__device__ __forceinline__ NewTok load_tok(const AppendArgs& a, int t) { return {a.tok_seq[t], a.tok_pos[t], a.cell[t]}; }
+
+// Slot of the block holding a token's position, or -1 when any index is out
+// of range (flagged when `report`); s_off: the preloaded block offsets or null.
+__device__ __forceinline__ int token_slot(const AppendArgs& a, NewTok k, const int64_t* s_off, int* in_block,
+                                          unsigned* err, bool report) {
+  const int s = k.s, p = k.p, c = k.c;
   if (s < 0 || s >= a.n_seq || p < 0) {
     if (report) atomicOr(err, kErrToken);
     return -1;
@@ -68,7 +76,8 @@ __device__ __forceinline__ int token_slot(const AppendArgs& a, int t, int* in_bl
     if (report) atomicOr(err, kErrCell);
     return -1;
   }
-  const int64_t off = a.seq_blk_off[s], len = a.seq_blk_off[s + 1] - off;
+  const int64_t off = s_off ? s_off[s] : a.seq_blk_off[s];
+  const int64_t len = (s_off ? s_off[s + 1] : a.seq_blk_off[s + 1]) - off;
   const int64_t j = p / a.r;
   if (j >= len) {
     if (report) atomicOr(err, kErrBlockList);
@@ -91,21 +100,44 @@ k_append(const AppendArgs a, const Turns turns, unsigned* err) {
   // launch writes before their own dependency wait (see qsa_internal.cuh).
   grid_dep_launch();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (blockIdx.x == gridDim.x - 1) {
+  constexpr int kPer = kAppendMaxTokens / kAppThreads;   // tokens per thread in the dirty-list CTA
+  const bool dirty_cta = blockIdx.x == gridDim.x - 1;
+  // this thread's tokens' ids, loaded together with the sequences' block
+  // offsets (one dependent load less on the way to the slots)
+  const int rows = 2 * a.G + 1;
+  const int64_t w = (int64_t)blockIdx.x * kAppWarps + warp;
+  const bool active = !dirty_cta && w < (int64_t)a.n_new * rows;
+  const int t = active ? (int)(w / rows) : 0;
+  NewTok mine[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int u = dirty_cta ? tid + k * kAppThreads : t;
+    mine[k] = ((dirty_cta && u < a.n_new) || (!dirty_cta && k == 0 && active)) ? load_tok(a, u) : NewTok{-1, -1, -1};
+  }
+  __shared__ int64_t s_off_buf[kAppOffCache + 1];
+  const int64_t* s_off = nullptr;
+  if (a.n_seq <= kAppOffCache) {
+    for (int i = tid; i <= a.n_seq; i += kAppThreads) s_off_buf[i] = a.seq_blk_off[i];
+    s_off = s_off_buf;
+  }
+  __syncthreads();
+  if (dirty_cta) {
     // ---- the dirty list (n_new <= kAppendMaxTokens, 4 tokens per thread)
     __shared__ int s_slot[kAppendMaxTokens];
     __shared__ unsigned char s_ib[kAppendMaxTokens];
     __shared__ int s_dslot[kAppendMaxTokens];
     __shared__ unsigned s_warp[kAppWarps];
-    for (int t = tid; t < a.n_new; t += kAppThreads) {
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int u = tid + k * kAppThreads;
+      if (u >= a.n_new) break;
       int ib = 0;
-      s_slot[t] = token_slot(a, t, &ib, err, false);
-      s_ib[t] = (unsigned char)ib;
+      s_slot[u] = token_slot(a, mine[k], s_off, &ib, err, false);
+      s_ib[u] = (unsigned char)ib;
     }
     __syncthreads();
     // token t leads its slot if no earlier token has it; leaders are ranked
     // by slot (ascending order of the list)
-    constexpr int kPer = kAppendMaxTokens / kAppThreads;
     __shared__ unsigned char s_lead[kAppendMaxTokens];
     int lead_slot[kPer];
     unsigned nlead = 0;
@@ -194,14 +226,10 @@ k_append(const AppendArgs a, const Turns turns, unsigned* err) {
   }
 
   // ---- one warp per (token, row)
-  const int rows = 2 * a.G + 1;
-  const int64_t w = (int64_t)blockIdx.x * kAppWarps + warp;
-  const bool active = w < (int64_t)a.n_new * rows;
-  const int t = active ? (int)(w / rows) : 0;
   const int kind = active ? (int)(w - (int64_t)t * rows) : 0;
   int ib = 0;
-  const int slot = active ? token_slot(a, t, &ib, err, kind == 2 * a.G && lane == 0) : -1;
-  const int64_t c = active ? a.cell[t] : 0;
+  const int slot = active ? token_slot(a, mine[0], s_off, &ib, err, kind == 2 * a.G && lane == 0) : -1;
+  const int64_t c = active ? mine[0].c : 0;
   const bool ok = active && slot >= 0;
 
   if (kind < 2 * a.G) {

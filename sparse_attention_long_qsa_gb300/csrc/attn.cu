@@ -37,6 +37,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "index_util.cuh"
 #include "qsa_internal.cuh"
 #include "tc_util.cuh"
 
@@ -71,6 +72,52 @@ constexpr uint32_t kOffXO = kOffXS + kOvf * 8 * 4;  // fp32 [8][256] partial out
 constexpr uint32_t kOffXM = kOffXO + 8 * 256 * 4;   // fp32 [8] max, [8] sum
 constexpr uint32_t kOffXC = kOffXM + 64;            // int [kOvf] cells
 constexpr uint32_t kSmemBytes = kOffXC + kOvf * 4 + 1024;   // + alignment slack
+
+// ---- the selection run by the attention clusters (kSel variants)
+constexpr int kFusedMaxList = 1024;                  // chosen blocks (top_k / r)
+constexpr int kFusedMaxTiles = 8;                    // 128-cell tiles per CTA
+constexpr int kFusedMaxWords = 2048;                 // bitmap words of CTA 0: 65,536 blocks
+constexpr int kFusedMaxBlocks = kFusedMaxWords * 32;
+constexpr int kFusedRankMax = 1024;                  // threshold-bin keys resolved in CTA 0
+constexpr int kFusedSlots = 8192;                    // slot ids a CTA keeps for its range
+constexpr int kFusedBatch = 16;                      // score words a warp loads before using any
+
+struct SelArgs {
+  IndexArgs ia;
+  void* ws;          // the qsa_index_topk workspace (histograms, scores)
+  int32_t* cells;    // outputs of the selection (written by the KV-head-0 clusters)
+  int32_t* count;
+};
+
+// Selection state that lives through the whole kernel (after the attention
+// layout).  `list`, `nsel`, `count` and `tail_cells` are CTA 0's, read by the
+// peers through distributed shared memory.
+struct SelFix {
+  int list[kFusedMaxList];                   // slots of the chosen blocks, ascending block index
+  int mycells[kFusedMaxTiles * kTile];       // this CTA's tiles' cells, tile-major
+  int tail_cells[8];
+  unsigned warp_tmp[8];
+  unsigned ncand, ncent, ncut, sel, cbase;
+  int thr, need, ncand_all, digit;
+  unsigned above, eq;
+  int nsel, count, last;
+};
+// Scratch of the selection, in the K and V tiles (free until the gather).
+struct SelScratch {
+  unsigned bitmap[kFusedMaxWords];           // CTA 0: every block; peers: their range
+  unsigned long long cand[kFusedRankMax];    // this CTA's threshold-bin keys
+  unsigned long long allc[kFusedRankMax];    // CTA 0: every CTA's threshold-bin keys
+  unsigned hist[2][256];
+  unsigned tot[256];
+  int slots[kFusedSlots + 4];                // slot ids of this CTA's range
+};
+static_assert(sizeof(SelScratch) <= 2u * kTile * 512u, "selection scratch fits in the K and V tiles");
+constexpr uint32_t kOffFix = (kOffXC + kOvf * 4 + 15u) & ~15u;
+constexpr uint32_t kSmemBytesSel = kOffFix + (uint32_t)sizeof(SelFix) + 1024;
+static_assert(kSmemBytesSel <= 227u * 1024u, "shared memory of the fused variant");
+
+template <bool kSel>
+constexpr uint32_t smem_bytes() { return kSel ? kSmemBytesSel : kSmemBytes; }
 
 // Instruction descriptor, kind::f16: fp32 accumulate, fp16 A and B,
 // M = 128, N = 16; A K-major (QK) or MN-major (PV), B K-major.
@@ -130,13 +177,443 @@ __device__ __forceinline__ uint4 dq8(uint2 raw, __half2 s2) {
   return o;
 }
 
+// Geometry of the fused selection for this CTA: the token's blocks are split
+// into NC ranges of `per` blocks (a multiple of 32), one per CTA.
+struct SelGeom {
+  Tok tk;
+  int nb;          // blocks that compete
+  int64_t per, j0, j1;
+  int nwords;      // bitmap words of this CTA's range
+  int tail;        // tail cells (positions past the last whole block, <= p)
+  bool tail_missing;
+};
+
+__device__ __forceinline__ SelGeom sel_geometry(const IndexArgs& ia, int t, uint32_t rank, uint32_t NC,
+                                                unsigned* err) {
+  SelGeom s;
+  s.tk = token_geometry(ia, t, err, false);
+  s.nb = s.tk.nb;
+  s.per = round_up(ceil_div(s.nb > 0 ? s.nb : 1, (int64_t)NC), 32);
+  s.j0 = (int64_t)rank * s.per;
+  s.j1 = min((int64_t)s.nb, s.j0 + s.per);
+  s.nwords = s.j1 > s.j0 ? (int)ceil_div(s.j1 - s.j0, 32) : 0;
+  s.tail = 0;
+  if (s.tk.ok && s.tk.nb == s.tk.nb_full) s.tail = s.tk.p + 1 - (int)(s.tk.nb_full * ia.r);
+  s.tail_missing = s.tail > 0 && s.tk.nb_full >= s.tk.len;
+  if (s.tail_missing) s.tail = 0;
+  return s;
+}
+
+// Block selection and expansion of token t by the CTAs of one cluster (the
+// method's lever3 steps, as k_select in index.cu runs them, here inside the
+// attention clusters so that no kernel boundary and no global cell list sit
+// between the selection and the gather).  Every cluster of the token (one per
+// KV head) computes the same selection; the KV-head-0 cluster writes the
+// cells and count outputs.  Steps:
+//   1. the threshold bin of the B-th largest score from the token's
+//      histogram (every CTA);
+//   2. each CTA classifies its range: blocks above the bin into a bitmap,
+//      blocks in the bin into unique 56-bit keys (ties to the lower index);
+//   3a. (bin <= kFusedRankMax keys) the CTAs push bitmap words and keys into
+//      CTA 0, which ranks the keys of the cut-off digit exactly and lists the
+//      chosen blocks' slots in block order;
+//   3b. (larger bins) a radix select over the bin's keys, one 8-bit digit per
+//      round with cluster-summed digit histograms, after which each CTA
+//      writes its chosen blocks' slots at its offset in CTA 0's list;
+//   4. every CTA expands the list positions of its own attention tiles
+//      (slot -> the block's member cells; then the tail cells).
+// Returns the token's cell count; this CTA's cells are in fx->mycells.
+__device__ __forceinline__ int select_in_cluster(const SelArgs& sa, const SelGeom& sg, int cells_pitch, int t,
+                                                 int g, int G, uint32_t rank, uint32_t NC, SelFix* fx,
+                                                 SelScratch* sx, unsigned* err) {
+  const IndexArgs& ia = sa.ia;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int kWarps = kThreads / 32;
+  const int r = ia.r, B = ia.n_sel_blocks;
+  const int nb = sg.nb, nwords = sg.nwords, tail = sg.tail;
+  const int64_t j0 = sg.j0, j1 = sg.j1, per = sg.per;
+  const int32_t* slots = ia.seq_blk_slots + sg.tk.off;
+  unsigned* gh = hist_of(sa.ws, t);
+  const float* srow = scores_of(sa.ws, ia.max_tokens) + (int64_t)t * ia.max_blocks;
+
+  // ---- 1. first scores in flight; the threshold bin (16 bins per thread)
+  float v0[kFusedBatch];
+#pragma unroll
+  for (int b = 0; b < kFusedBatch; ++b) {
+    const int w = warp + kWarps * b;
+    const int64_t j = j0 + (int64_t)w * 32 + lane;
+    v0[b] = (w < nwords && j < j1) ? __ldcg(srow + j) : -INFINITY;
+  }
+  const int tslot = (rank == 0 && tid < tail) ? slots[sg.tk.nb_full] : -1;
+  {
+    constexpr int kPer = kHistBins / kThreads;
+    static_assert(kPer == 16, "histogram split");
+    unsigned h[kPer];
+    unsigned sum = 0;
+#pragma unroll
+    for (int q = 0; q < kPer / 4; ++q) {
+      const uint4 v = __ldcg(reinterpret_cast<const uint4*>(gh + tid * kPer) + q);
+      h[4 * q] = v.x, h[4 * q + 1] = v.y, h[4 * q + 2] = v.z, h[4 * q + 3] = v.w;
+    }
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) sum += h[i];
+    if (tid == 0) {
+      fx->thr = -1;
+      fx->need = 0;
+      fx->ncand_all = 0;
+    }
+    unsigned cum = block_suffix_exclusive(sum, fx->warp_tmp);
+    const unsigned Bu = (unsigned)B;
+    if ((unsigned)nb > Bu) {
+#pragma unroll
+      for (int i = kPer - 1; i >= 0; --i) {
+        const unsigned nxt = cum + h[i];
+        if (cum < Bu && nxt >= Bu) {
+          fx->thr = tid * kPer + i;
+          fx->need = (int)(Bu - cum);
+          fx->ncand_all = (int)h[i];
+        }
+        cum = nxt;
+      }
+    }
+    __syncthreads();
+  }
+  // This CTA has read the histogram.  The last of the token's G x NC readers
+  // clears it for the next call (before this kernel lets its successor start).
+  if (tid == 0) fx->last = atomicAdd(readers_of(sa.ws, t), 1u) == (unsigned)(G * (int)NC) - 1u ? 1 : 0;
+  const int thr = fx->thr, ncand_all = fx->ncand_all;
+  const bool central = thr < 0 || ncand_all <= kFusedRankMax;
+  if (rank == 0 && tid < tail) {
+    if (tslot >= 0 && tslot < ia.n_slots) {
+      cp_async4(&fx->tail_cells[tid], ia.blk_cells + (int64_t)tslot * r + tid);
+    } else {
+      atomicOr(err, kErrSlot);
+      fx->tail_cells[tid] = -1;
+    }
+  }
+  QSA_TS(attn, 18);
+
+  // ---- 2. classify this CTA's blocks (words dealt round-robin to the warps)
+  for (int wb = 0; wb * kWarps * kFusedBatch < nwords; ++wb) {
+    const int wbase = wb * kWarps * kFusedBatch + warp;
+    float v[kFusedBatch];
+#pragma unroll
+    for (int b = 0; b < kFusedBatch; ++b) {
+      const int w = wbase + kWarps * b;
+      const int64_t j = j0 + (int64_t)w * 32 + lane;
+      v[b] = (wb == 0) ? v0[b] : ((w < nwords && j < j1) ? __ldcg(srow + j) : -INFINITY);
+    }
+#pragma unroll
+    for (int b = 0; b < kFusedBatch; ++b) {
+      const int w = wbase + kWarps * b;
+      if (w >= nwords) break;
+      const int64_t j = j0 + (int64_t)w * 32 + lane;
+      const bool in = j < j1;
+      const uint32_t key = score_key(v[b]);
+      const int bin = (int)(key >> (32 - kHistBits));
+      const unsigned am = __ballot_sync(kFull, in && bin > thr);
+      if (lane == 0) sx->bitmap[w] = am;
+      if (central && thr >= 0) {
+        const bool isc = in && bin == thr;
+        const unsigned cm = __ballot_sync(kFull, isc);
+        if (cm) {
+          const int leader = __ffs(cm) - 1;
+          unsigned basei = 0;
+          if (lane == leader) basei = atomicAdd(&fx->ncand, (unsigned)__popc(cm));
+          basei = __shfl_sync(kFull, basei, leader);
+          const unsigned idx = basei + __popc(cm & ((1u << lane) - 1u));
+          if (isc && idx < (unsigned)kFusedRankMax) sx->cand[idx] = cand_key(key, j);
+        }
+      }
+    }
+  }
+  // this range's slot ids (CTA 0 reads them through DSMEM to list the chosen
+  // blocks): 16-byte copies where the list is aligned, single ids at the ends
+  const bool slots_cached = per <= kFusedSlots;
+  auto slot_shift = [&](int64_t lo) { return (int)((reinterpret_cast<uintptr_t>(slots + lo) >> 2) & 3); };
+  int32_t* my_slots = sx->slots + slot_shift(j0);
+  if (slots_cached && j1 > j0) {
+    const int64_t n = j1 - j0;
+    const int64_t head = min(n, (int64_t)((4 - slot_shift(j0)) & 3));
+    const int64_t body = (n - head) / 4;
+    if (tid < head) cp_async4(my_slots + tid, slots + j0 + tid);
+    for (int64_t q = tid; q < body; q += kThreads) cp_async16_ptr(my_slots + head + 4 * q, slots + j0 + head + 4 * q);
+    for (int64_t i = head + 4 * body + tid; i < n; i += kThreads) cp_async4(my_slots + i, slots + j0 + i);
+  }
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+  __syncthreads();
+  QSA_TS(attn, 19);
+  // slot of block j (any range): from its owner's shared memory when cached
+  auto slot_of = [&](int64_t j) -> int {
+    if (!slots_cached) return slots[j];
+    const int64_t p = j / per;
+    return (int)ld_dsmem_u32(dsmem_addr(sx->slots + slot_shift(p * per) + (j - p * per), (uint32_t)p));
+  };
+
+  cluster_wait();   // pairs with the arrive before the dependency wait: every CTA's counters are set
+  if (central) {
+    // ---- 3a. bitmap words and threshold-bin keys into CTA 0
+    if (rank != 0)
+      for (int w = tid; w < nwords; w += kThreads)
+        st_dsmem_u32(dsmem_addr(&sx->bitmap[(int)(j0 >> 5) + w], 0), sx->bitmap[w]);
+    const unsigned ncl = min(fx->ncand, (unsigned)kFusedRankMax);
+    if (tid == 0) fx->cbase = ncl ? atom_add_dsmem(dsmem_addr(&fx->ncent, 0), ncl) : 0u;
+    __syncthreads();
+    for (unsigned i = tid; i < ncl; i += kThreads) {
+      const unsigned at = fx->cbase + i;
+      if (at < (unsigned)kFusedRankMax) st_dsmem_u64(dsmem_addr(&sx->allc[at], 0), sx->cand[i]);
+    }
+    asm volatile("cp.async.wait_all;\n" ::: "memory");   // slot ids (and CTA 0's tail cells)
+    cluster_sync();   // everything has landed in CTA 0; every range's slot ids are in place
+    QSA_TS(attn, 20);
+    if (rank == 0) {
+      const unsigned nall = min(fx->ncent, (unsigned)kFusedRankMax);
+      if (thr >= 0) {
+        // one 8-bit digit below the bin (key bits 19..12) splits the keys;
+        // keys above the cut-off digit are chosen, the digit's own keys are
+        // ranked exactly by full key
+        unsigned need = (unsigned)fx->need;
+        unsigned* hh = sx->hist[0];
+        hh[tid] = 0u;
+        __syncthreads();
+        for (unsigned i = tid; i < nall; i += kThreads) atomicAdd(&hh[(unsigned)(sx->allc[i] >> 48) & 255u], 1u);
+        __syncthreads();
+        if (warp == 0) {
+          unsigned hv[8], hs = 0;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            hv[i] = hh[lane * 8 + i];
+            hs += hv[i];
+          }
+          unsigned x = hs;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const unsigned y = __shfl_down_sync(kFull, x, o);
+            if (lane + o < 32) x += y;
+          }
+          unsigned cum = x - hs;
+#pragma unroll
+          for (int i = 7; i >= 0; --i) {
+            const unsigned nxt = cum + hv[i];
+            if (cum < need && nxt >= need) {
+              fx->digit = lane * 8 + i;
+              fx->above = cum;
+            }
+            cum = nxt;
+          }
+        }
+        if (tid == 0) fx->ncut = 0u;
+        __syncthreads();
+        const unsigned dstar = (unsigned)fx->digit;
+        need -= fx->above;
+        for (unsigned i = tid; i < nall; i += kThreads) {
+          const unsigned long long c = sx->allc[i];
+          const unsigned d = (unsigned)(c >> 48) & 255u;
+          if (d > dstar) {
+            const int64_t j = (int64_t)(~(uint32_t)(c >> 4));
+            atomicOr(&sx->bitmap[j >> 5], 1u << (j & 31));
+          } else if (d == dstar) {
+            sx->cand[atomicAdd(&fx->ncut, 1u)] = c;   // ncut <= nall <= kFusedRankMax
+          }
+        }
+        __syncthreads();
+        const unsigned ncut = fx->ncut;
+        for (unsigned i = tid; i < ncut; i += kThreads) {
+          const unsigned long long c = sx->cand[i];
+          unsigned above_c = 0;
+          for (unsigned m = 0; m < ncut; ++m) above_c += sx->cand[m] > c ? 1u : 0u;
+          if (above_c < need) {
+            const int64_t j = (int64_t)(~(uint32_t)(c >> 4));
+            atomicOr(&sx->bitmap[j >> 5], 1u << (j & 31));
+          }
+        }
+      }
+      __syncthreads();
+      // the chosen blocks in order, as slots
+      const int W = (int)ceil_div(nb, 32);
+      const int wq = (int)ceil_div(W, kThreads);
+      const int q0 = tid * wq, q1 = min(W, q0 + wq);
+      unsigned mine = 0;
+      for (int w = q0; w < q1; ++w) mine += __popc(sx->bitmap[w]);
+      unsigned total = 0;
+      unsigned k = block_prefix_exclusive(mine, fx->warp_tmp, &total);
+      for (int w = q0; w < q1; ++w) {
+        unsigned bits = sx->bitmap[w];
+        while (bits) {
+          if (k < (unsigned)B) fx->list[k] = w * 32 + (__ffs(bits) - 1);
+          ++k;
+          bits &= bits - 1u;
+        }
+      }
+      const int nsel = (int)min(total, (unsigned)B);
+      __syncthreads();
+      // block -> slot, the loads of each thread's positions issued together
+      constexpr int kPerT = kFusedMaxList / kThreads;
+      int sv[kPerT];
+#pragma unroll
+      for (int q = 0; q < kPerT; ++q) {
+        const int i = tid + q * kThreads;
+        sv[q] = i < nsel ? slot_of(fx->list[i]) : 0;
+      }
+#pragma unroll
+      for (int q = 0; q < kPerT; ++q) {
+        const int i = tid + q * kThreads;
+        if (i < nsel) fx->list[i] = sv[q];
+      }
+      if (tid == 0) {
+        fx->nsel = nsel;
+        fx->count = nsel * r + tail;
+      }
+    }
+    QSA_TS(attn, 21);
+    cluster_sync();   // CTA 0's list is complete
+  } else {
+    // ---- 3b. radix select over the threshold bin (thr >= 0 here)
+    unsigned long long prefix = 0;
+    int shift = 48;
+    unsigned need = (unsigned)fx->need;
+    int buf = 0;
+    for (;;) {
+      unsigned* hh = sx->hist[buf];
+      hh[tid] = 0u;
+      __syncthreads();
+      for (int64_t j = j0 + tid; j < j1; j += kThreads) {
+        const uint32_t key = score_key(__ldcg(srow + j));
+        if ((int)(key >> (32 - kHistBits)) != thr) continue;
+        const unsigned long long c = cand_key(key, j);
+        if ((c >> (shift + 8)) == prefix) atomicAdd(&hh[(unsigned)(c >> shift) & 255u], 1u);
+      }
+      cluster_sync();
+      {
+        unsigned sum = 0;
+        for (int p = 0; p < (int)NC; ++p) sum += ld_dsmem_u32(dsmem_addr(&hh[tid], (uint32_t)p));
+        sx->tot[tid] = sum;
+      }
+      __syncthreads();
+      if (warp == 0) {
+        unsigned hv[8], hs = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          hv[i] = sx->tot[lane * 8 + i];
+          hs += hv[i];
+        }
+        unsigned x = hs;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const unsigned y = __shfl_down_sync(kFull, x, o);
+          if (lane + o < 32) x += y;
+        }
+        unsigned cum = x - hs;
+#pragma unroll
+        for (int i = 7; i >= 0; --i) {
+          const unsigned nxt = cum + hv[i];
+          if (cum < need && nxt >= need) {
+            fx->digit = lane * 8 + i;
+            fx->above = cum;
+            fx->eq = hv[i];
+          }
+          cum = nxt;
+        }
+      }
+      __syncthreads();
+      need -= fx->above;
+      const unsigned eq = fx->eq;
+      prefix = (prefix << 8) | (unsigned long long)fx->digit;
+      buf ^= 1;
+      if (eq == need || shift == 0) break;
+      shift -= 8;
+    }
+    // every key of the bin whose bits down to `shift` are >= prefix is chosen
+    for (int64_t j = j0 + tid; j < j1; j += kThreads) {
+      const uint32_t key = score_key(__ldcg(srow + j));
+      if ((int)(key >> (32 - kHistBits)) != thr) continue;
+      if ((cand_key(key, j) >> shift) >= prefix) atomicOr(&sx->bitmap[(j - j0) >> 5], 1u << ((j - j0) & 31));
+    }
+    __syncthreads();
+    const int wpt = (int)ceil_div(nwords, kThreads);
+    const int w0 = tid * wpt, w1 = min(nwords, w0 + wpt);
+    unsigned mine = 0;
+    for (int w = w0; w < w1; ++w) mine += __popc(sx->bitmap[w]);
+    unsigned local_total = 0;
+    unsigned k = block_prefix_exclusive(mine, fx->warp_tmp, &local_total);
+    if (tid == 0) fx->sel = local_total;
+    asm volatile("cp.async.wait_all;\n" ::: "memory");
+    cluster_sync();   // every CTA's count is published
+    QSA_TS(attn, 20);
+    unsigned base = 0, total = 0;
+    for (int p = 0; p < (int)NC; ++p) {
+      const unsigned c = ld_dsmem_u32(dsmem_addr(&fx->sel, (uint32_t)p));
+      if (p < (int)rank) base += c;
+      total += c;
+    }
+    k += base;
+    for (int w = w0; w < w1; ++w) {
+      unsigned bits = sx->bitmap[w];
+      while (bits) {
+        const int64_t j = j0 + (int64_t)w * 32 + (__ffs(bits) - 1);
+        bits &= bits - 1u;
+        if (k < (unsigned)B)
+          st_dsmem_u32(dsmem_addr(&fx->list[k], 0),
+                       (unsigned)(slots_cached ? my_slots[j - j0] : slots[j]));
+        ++k;
+      }
+    }
+    if (rank == 0 && tid == 0) {
+      const int nsel = (int)min(total, (unsigned)B);
+      fx->nsel = nsel;
+      fx->count = nsel * r + tail;
+    }
+    QSA_TS(attn, 21);
+    cluster_sync();   // CTA 0's list is complete
+  }
+  QSA_TS(attn, 22);
+
+  // ---- 4. the cells of this CTA's tiles (and, KV head 0, the outputs)
+  const int nsel = (int)ld_dsmem_u32(dsmem_addr(&fx->nsel, 0));
+  int count = (int)ld_dsmem_u32(dsmem_addr(&fx->count, 0));
+  const int tiles_total = (int)ceil_div(cells_pitch, kTile);
+  const int my_tiles = (int)rank < tiles_total ? (tiles_total - (int)rank + (int)NC - 1) / (int)NC : 0;
+  int32_t* crow = sa.cells + (int64_t)t * cells_pitch;
+  for (int idx = tid; idx < my_tiles * kTile; idx += kThreads) {
+    const int i = ((int)rank + (idx >> 7) * (int)NC) * kTile + (idx & (kTile - 1));
+    int cell = -1;
+    if (i < nsel * r) {
+      const int slot = (int)ld_dsmem_u32(dsmem_addr(&fx->list[i / r], 0));
+      const bool sok = slot >= 0 && slot < ia.n_slots;
+      if (!sok) atomicOr(err, kErrSlot);
+      cell = flag_cell(sok ? ia.blk_cells[(int64_t)slot * r + i % r] : -1, ia.n_cells, err);
+    } else if (i < count) {
+      cell = flag_cell((int)ld_dsmem_u32(dsmem_addr(&fx->tail_cells[i - nsel * r], 0)), ia.n_cells, err);
+    }
+    fx->mycells[idx] = cell;
+    if (g == 0 && i < cells_pitch) crow[i] = cell;
+  }
+  if (g == 0 && rank == 0 && tid == 0) {
+    sa.count[t] = count;
+    if (sg.tail_missing) atomicOr(err, kErrBlockList);
+  }
+  __syncthreads();
+  if (fx->last) {
+    uint4* h4 = reinterpret_cast<uint4*>(gh);
+    for (int i = tid; i < kHistBins / 4; i += kThreads) h4[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (tid == 0) *readers_of(sa.ws, t) = 0u;
+    __threadfence();
+  }
+  QSA_TS(attn, 23);
+  count = count < 0 ? 0 : (count > cells_pitch ? cells_pitch : count);
+  return count;
+}
+
 // kPipe: the launch gives CTAs several tiles each; the pipelined tile loops
 // (fp16: cp.async groups into shared memory; q8_0: the next tile's rows in
 // registers) are compiled only into this variant, so the one-tile decode
 // variant keeps its code small (it runs from a cold instruction cache).
-template <bool kQ8, bool kPipe>
+// kSel: the clusters first select and expand the token's blocks
+// (select_in_cluster) and read the cells from shared memory; otherwise the
+// cell list comes from global memory (written by qsa_index_topk).
+template <bool kQ8, bool kPipe, bool kSel>
 __global__ void __launch_bounds__(kThreads, 1)
-k_attn_tc(const AttnArgs a, unsigned* err) {
+k_attn_tc(const AttnArgs a, const SelArgs sa, unsigned* err) {
   QSA_TS_SCOPE_LAST(attn, 28);
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
@@ -156,8 +633,21 @@ k_attn_tc(const AttnArgs a, unsigned* err) {
   const int G = a.n_kv_heads, Hq = G * kGqa;
   // scores live in the log2 domain: s * attn_scale * log2(e), exponentials by exp2f
   const float scale2 = a.attn_scale * 1.4426950408889634f;
+  SelFix* fx = reinterpret_cast<SelFix*>(base + kOffFix);
+  SelScratch* sx = reinterpret_cast<SelScratch*>(base + kOffK);
 
   QSA_TS(attn, 0);
+  SelGeom sg{};
+  if constexpr (kSel) {
+    // the selection's geometry (inputs only); its counters are set before the
+    // first half of a cluster barrier whose second half precedes any push
+    sg = sel_geometry(sa.ia, t, rank, NC, err);
+    if (tid == 0) {
+      fx->ncand = 0u;
+      fx->ncent = 0u;
+    }
+    cluster_arrive();
+  }
   // ---- prologue (inputs not produced by the preceding index kernels)
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(base_s + kOffTmem),
@@ -188,17 +678,35 @@ k_attn_tc(const AttnArgs a, unsigned* err) {
   tc_fence_after();
   const uint32_t tmem = *stmem;
 
-  // ---- the cell list is written by the index kernels
+  // ---- the cell list is written by the index kernels (kSel: the scores
+  // and histogram are)
   QSA_TS(attn, 1);
   grid_dep_wait();
-  grid_dep_launch();
+  if constexpr (!kSel) grid_dep_launch();
   QSA_TS(attn, 2);
   const int32_t* crow = a.cells + (int64_t)t * a.cells_pitch;
-  // the first tile's cells and the count load together
+  // cell id at position i of the token's list, for positions in this CTA's tiles
+  auto list_cell = [&](int i) -> int {
+    if constexpr (kSel) {
+      return fx->mycells[(((i >> 7) - (int)rank) / (int)NC) * kTile + (i & (kTile - 1))];
+    } else {
+      return crow[i];
+    }
+  };
   int cfirst = -1;
-  if (tid < kTile && (int)rank * kTile + tid < a.cells_pitch) cfirst = crow[(int)rank * kTile + tid];
-  int cnt = a.count[t];
-  cnt = cnt < 0 ? 0 : (cnt > a.cells_pitch ? a.cells_pitch : cnt);
+  int cnt = 0;
+  if constexpr (kSel) {
+    cnt = select_in_cluster(sa, sg, a.cells_pitch, t, g, G, rank, NC, fx, sx, err);
+    if (tid < kTile) cfirst = fx->mycells[tid];
+    // the scores and the histogram are no longer read: the successor may start
+    __syncthreads();
+    grid_dep_launch();
+  } else {
+    // the first tile's cells and the count load together
+    if (tid < kTile && (int)rank * kTile + tid < a.cells_pitch) cfirst = crow[(int)rank * kTile + tid];
+    cnt = a.count[t];
+    cnt = cnt < 0 ? 0 : (cnt > a.cells_pitch ? a.cells_pitch : cnt);
+  }
   const int n_tiles = (cnt + kTile - 1) / kTile;
 
   float run_m[kGqa], run_l[kGqa], acc[2][kGqa];
@@ -230,7 +738,7 @@ k_attn_tc(const AttnArgs a, unsigned* err) {
     const int tx = tid - 128;
     int c = -1;
     if (tx < ovf_n) {
-      c = crow[(n_tiles - 1) * kTile + tx];
+      c = list_cell((n_tiles - 1) * kTile + tx);
       if (c < 0 || c >= a.n_cells) {
         atomicOr(err, kErrCell);
         c = -1;
@@ -355,7 +863,7 @@ k_attn_tc(const AttnArgs a, unsigned* err) {
         const int c0 = tile * kTile, nvt = min(kTile, cnt - c0);
         int c = -1;
         if (tx < nvt) {
-          c = (tile == (int)rank) ? cfirst : crow[c0 + tx];
+          c = (tile == (int)rank) ? cfirst : list_cell(c0 + tx);
           if (c < 0 || c >= a.n_cells) {
             atomicOr(err, kErrCell);
             c = -1;
@@ -474,7 +982,7 @@ k_attn_tc(const AttnArgs a, unsigned* err) {
   };
   auto q8_raw = [&](int tile) {
     const int i = tile * kTile + qrow;
-    return (tile < loop_tiles && i < cnt) ? crow[i] : 0;
+    return (tile < loop_tiles && i < cnt) ? list_cell(i) : 0;
   };
   if constexpr (kQ8 && kPipe) {
     qc = q8_cell((int)rank, q8_raw((int)rank));
@@ -493,7 +1001,7 @@ k_attn_tc(const AttnArgs a, unsigned* err) {
     if (tid < kTile) {
       int c = -1;
       if (tid < nv) {
-        c = (tile == (int)rank) ? cfirst : crow[c0 + tid];
+        c = (tile == (int)rank) ? cfirst : list_cell(c0 + tid);
         if (c < 0 || c >= a.n_cells) {
           atomicOr(err, kErrCell);
           c = -1;
@@ -709,21 +1217,31 @@ k_attn_tc(const AttnArgs a, unsigned* err) {
   QSA_TS(attn, 26);
   {
     // output (head h, dim d0 + e) = sum_p w_p o_p / sum_p w_p l_p with
-    // w_p = exp2(m_p - max_p m_p), one output per thread
+    // w_p = exp2(m_p - max_p m_p).  First the normalised weight of each
+    // (partial p, head h), one per thread of warps 0-3 with a head's partials
+    // in 16 consecutive lanes; then one output per thread.
+    float* wgt = reinterpret_cast<float*>(base + kOffQ);   // the Q tile is no longer read
+    if (tid < 16 * kGqa) {
+      const int h = tid >> 4, p = tid & 15;
+      const float mp = p < (int)NC ? sml[p * 16 + h] : -INFINITY;
+      const float lp = p < (int)NC ? sml[p * 16 + 8 + h] : 0.f;
+      float mx = mp;
+#pragma unroll
+      for (int o = 8; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+      const float w = (mp == -INFINITY) ? 0.f : exp2f(mp - mx);
+      float den = w * lp;
+#pragma unroll
+      for (int o = 8; o >= 1; o >>= 1) den += __shfl_xor_sync(kFull, den, o);
+      wgt[p * kGqa + h] = den > 0.f ? w / den : 0.f;
+    }
+    __syncthreads();
     const int d0 = (int)rank * dpc;
     for (int i = tid; i < kGqa * dpc; i += kThreads) {
       const int h = i / dpc, e = i % dpc, d = d0 + e;
       if (d >= kHeadDim) continue;
-      float mx = -INFINITY;
-      for (int p = 0; p < (int)NC; ++p) mx = fmaxf(mx, sml[p * 16 + h]);
-      float num = 0.f, den = 0.f;
-      for (int p = 0; p < (int)NC; ++p) {
-        const float mp = sml[p * 16 + h];
-        const float w = (mp == -INFINITY) ? 0.f : exp2f(mp - mx);
-        den = fmaf(w, sml[p * 16 + 8 + h], den);
-        num = fmaf(w, so[(p * kGqa + h) * dpc + e], num);
-      }
-      a.out[((int64_t)t * Hq + g * kGqa + h) * kHeadDim + d] = den > 0.f ? num / den : 0.f;
+      float o = 0.f;
+      for (int p = 0; p < (int)NC; ++p) o = fmaf(wgt[p * kGqa + h], so[(p * kGqa + h) * dpc + e], o);
+      a.out[((int64_t)t * Hq + g * kGqa + h) * kHeadDim + d] = o;
     }
   }
   QSA_TS(attn, 27);
@@ -739,13 +1257,14 @@ constexpr int kMaxDevices = 64;
 // Cluster size for a launch of `clusters` clusters: 16 CTAs (one per 128-cell
 // tile of the 2051-cell budget) when that many 16-CTA clusters are co-resident,
 // else the largest smaller power of two that fits them.
-template <bool kQ8>
+template <bool kQ8, bool kSel>
 cudaError_t pick_cluster(const AttnArgs& a, int* nc_out) {
   // per device: clusters of 16, 8, 4, 2, 1 that fit at once, measured once
   // under a lock and published by `configured`
   static int max_active[kMaxDevices][5];
   static std::atomic<bool> configured[kMaxDevices];
   static std::mutex mu;
+  constexpr int kSmem = (int)smem_bytes<kSel>();
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -753,20 +1272,20 @@ cudaError_t pick_cluster(const AttnArgs& a, int* nc_out) {
   if (!configured[dev].load(std::memory_order_acquire)) {
     std::lock_guard<std::mutex> lock(mu);
     if (!configured[dev].load(std::memory_order_relaxed)) {
-      e = cudaFuncSetAttribute(k_attn_tc<kQ8, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+      e = cudaFuncSetAttribute(k_attn_tc<kQ8, false, kSel>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
       if (e != cudaSuccess) return e;
-      e = cudaFuncSetAttribute(k_attn_tc<kQ8, false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      e = cudaFuncSetAttribute(k_attn_tc<kQ8, false, kSel>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
       if (e != cudaSuccess) return e;
-      e = cudaFuncSetAttribute(k_attn_tc<kQ8, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+      e = cudaFuncSetAttribute(k_attn_tc<kQ8, true, kSel>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
       if (e != cudaSuccess) return e;
-      e = cudaFuncSetAttribute(k_attn_tc<kQ8, true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      e = cudaFuncSetAttribute(k_attn_tc<kQ8, true, kSel>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
       if (e != cudaSuccess) return e;
       for (int i = 0; i < 5; ++i) {
         const int nc = 16 >> i;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)nc, 1, 1);
         cfg.blockDim = dim3(kThreads, 1, 1);
-        cfg.dynamicSmemBytes = kSmemBytes;
+        cfg.dynamicSmemBytes = (size_t)kSmem;
         cudaLaunchAttribute attr;
         attr.id = cudaLaunchAttributeClusterDimension;
         attr.val.clusterDim.x = (unsigned)nc;
@@ -775,7 +1294,7 @@ cudaError_t pick_cluster(const AttnArgs& a, int* nc_out) {
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, k_attn_tc<kQ8, false>, &cfg) != cudaSuccess) {
+        if (cudaOccupancyMaxActiveClusters(&n, k_attn_tc<kQ8, false, kSel>, &cfg) != cudaSuccess) {
           (void)cudaGetLastError();
           n = 0;
         }
@@ -817,15 +1336,12 @@ cudaError_t pick_cluster(const AttnArgs& a, int* nc_out) {
   return cudaSuccess;
 }
 
-template <bool kQ8>
-cudaError_t launch_tc(const AttnArgs& a, unsigned* err, cudaStream_t stream) {
-  int nc = 1;
-  cudaError_t e = pick_cluster<kQ8>(a, &nc);
-  if (e != cudaSuccess) return e;
+template <bool kQ8, bool kSel>
+cudaError_t launch_tc(const AttnArgs& a, const SelArgs& sa, int nc, unsigned* err, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)nc, (unsigned)a.n_kv_heads, (unsigned)a.n_tokens);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = smem_bytes<kSel>();
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -838,8 +1354,31 @@ cudaError_t launch_tc(const AttnArgs& a, unsigned* err, cudaStream_t stream) {
   cfg.numAttrs = 2;
   // several tiles per CTA: the pipelined variant
   const int tiles = (int)ceil_div(a.cells_pitch, kTile);
-  if (2 * nc <= tiles) return cudaLaunchKernelEx(&cfg, k_attn_tc<kQ8, true>, a, err);
-  return cudaLaunchKernelEx(&cfg, k_attn_tc<kQ8, false>, a, err);
+  if (2 * nc <= tiles) return cudaLaunchKernelEx(&cfg, k_attn_tc<kQ8, true, kSel>, a, sa, err);
+  return cudaLaunchKernelEx(&cfg, k_attn_tc<kQ8, false, kSel>, a, sa, err);
+}
+
+template <bool kQ8>
+cudaError_t launch_plain(const AttnArgs& a, unsigned* err, cudaStream_t stream) {
+  int nc = 1;
+  cudaError_t e = pick_cluster<kQ8, false>(a, &nc);
+  if (e != cudaSuccess) return e;
+  return launch_tc<kQ8, false>(a, SelArgs{}, nc, err, stream);
+}
+
+// The fused launch when its limits hold (*done = false otherwise, nothing
+// launched): at most 65,536 blocks per token, 1,024 chosen blocks, 8 tiles
+// per CTA.
+template <bool kQ8>
+cudaError_t launch_fused(const AttnArgs& a, const SelArgs& sa, unsigned* err, cudaStream_t stream, bool* done) {
+  *done = false;
+  if (sa.ia.max_blocks > kFusedMaxBlocks || sa.ia.n_sel_blocks > kFusedMaxList || sa.ia.r > 8) return cudaSuccess;
+  int nc = 1;
+  cudaError_t e = pick_cluster<kQ8, true>(a, &nc);
+  if (e != cudaSuccess) return e;
+  if (ceil_div(ceil_div(a.cells_pitch, kTile), nc) > kFusedMaxTiles) return cudaSuccess;
+  *done = true;
+  return launch_tc<kQ8, true>(a, sa, nc, err, stream);
 }
 
 }  // namespace
@@ -849,9 +1388,57 @@ size_t attn_workspace_bytes(int, int, int) { return 0; }
 cudaError_t launch_sparse_attn(const AttnArgs& a, void*, unsigned* err, cudaStream_t stream) {
   if (a.n_tokens <= 0) return cudaSuccess;
   prof_before(kKAttn, stream);
-  cudaError_t e = a.kv_q8 ? launch_tc<true>(a, err, stream) : launch_tc<false>(a, err, stream);
+  cudaError_t e = a.kv_q8 ? launch_plain<true>(a, err, stream) : launch_plain<false>(a, err, stream);
   prof_after(kKAttn, stream);
   if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t index_attn_plan(int n_tokens, int n_kv_heads, int kv_q8, int cells_pitch, int64_t max_blocks,
+                            int n_sel_blocks, int r, bool* fused) {
+  *fused = false;
+  if (n_tokens <= 0 || max_blocks > kFusedMaxBlocks || n_sel_blocks > kFusedMaxList || r > 8) return cudaSuccess;
+  AttnArgs a{};
+  a.n_tokens = n_tokens;
+  a.n_kv_heads = n_kv_heads;
+  a.cells_pitch = cells_pitch;
+  int nc = 1;
+  cudaError_t e = kv_q8 ? pick_cluster<true, true>(a, &nc) : pick_cluster<false, true>(a, &nc);
+  if (e != cudaSuccess) return e;
+  *fused = ceil_div(ceil_div(cells_pitch, kTile), nc) <= kFusedMaxTiles;
+  return cudaSuccess;
+}
+
+cudaError_t launch_index_attn(const IndexArgs& ia, const AttnArgs& a, int32_t* cells, int32_t* count, void* ws,
+                              bool in_cluster, unsigned* err, cudaStream_t stream, bool* fused) {
+  *fused = false;
+  if (a.n_tokens <= 0) return cudaSuccess;
+  SelArgs sa{};
+  sa.ia = ia;
+  sa.ia.max_blocks = ia.max_blocks > 0 ? ia.max_blocks : 1;
+  sa.ws = ws;
+  sa.cells = cells;
+  sa.count = count;
+  // the limits of the fused launch are known before anything is launched
+  bool ok = false;
+  if (in_cluster) {
+    cudaError_t e0 = index_attn_plan(a.n_tokens, a.n_kv_heads, a.kv_q8, a.cells_pitch, sa.ia.max_blocks,
+                                     ia.n_sel_blocks, ia.r, &ok);
+    if (e0 != cudaSuccess) return e0;
+  }
+  if (!ok) {
+    cudaError_t e = launch_index_topk(ia, cells, count, ws, err, stream);
+    if (e != cudaSuccess) return e;
+    return launch_sparse_attn(a, nullptr, err, stream);
+  }
+  cudaError_t e = launch_index_scores_topk(ia, ws, err, stream);
+  if (e != cudaSuccess) return e;
+  bool done = false;
+  prof_before(kKFused, stream);
+  e = a.kv_q8 ? launch_fused<true>(a, sa, err, stream, &done) : launch_fused<false>(a, sa, err, stream, &done);
+  prof_after(kKFused, stream);
+  if (e != cudaSuccess) return e;
+  *fused = done;
   return cudaGetLastError();
 }
 

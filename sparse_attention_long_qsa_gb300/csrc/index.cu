@@ -42,6 +42,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "index_util.cuh"
 #include "qsa_internal.cuh"
 #include "tc_util.cuh"
 
@@ -75,119 +76,6 @@ constexpr int kCentralBlocks = kSelMaxWords * 32 / 2;   // tokens up to 65536 bl
 constexpr int kRankMax = 1024;            // threshold-bin keys resolved by direct ranking
 static_assert(kRankMax <= kSelLocalCand, "the cut-off digit's keys reuse the candidate list");
 constexpr int kSelList = 2048;            // chosen blocks a CTA lists before expanding
-
-// Per-token histogram at the front of the workspace.  Zero on first use;
-// every call leaves it zero again.
-constexpr size_t kCtrlBytes = sizeof(unsigned) * kHistBins;
-
-__host__ __device__ __forceinline__ unsigned* hist_of(void* ws, int t) {
-  return reinterpret_cast<unsigned*>(static_cast<char*>(ws) + (size_t)t * kCtrlBytes);
-}
-
-__host__ __device__ __forceinline__ float* scores_of(void* ws, int max_tokens) {
-  return reinterpret_cast<float*>(static_cast<char*>(ws) + round_up((int64_t)max_tokens * kCtrlBytes, 256));
-}
-
-// Per-token geometry, validated against the caller's bounds.
-struct Tok {
-  int64_t off;      // start of the sequence's block list
-  int64_t len;      // its length
-  int64_t nb_full;  // floor((p+1)/r)
-  int nb;           // blocks scored: nb_full clamped to max_blocks and len
-  int p;
-  bool ok;
-};
-
-__device__ __forceinline__ Tok token_geometry(const IndexArgs& a, int t, unsigned* err, bool report) {
-  Tok k{0, 0, 0, 0, -1, false};
-  const int seq = a.tok_seq[t];
-  const int p = a.tok_pos[t];
-  if (seq < 0 || seq >= a.n_seq || p < 0) {
-    if (report) atomicOr(err, kErrToken);
-    return k;
-  }
-  k.off = a.seq_blk_off[seq];
-  k.len = a.seq_blk_off[seq + 1] - k.off;
-  k.p = p;
-  k.nb_full = ((int64_t)p + 1) / a.r;
-  int64_t nb = k.nb_full;
-  if (nb > a.max_blocks) {
-    if (report) atomicOr(err, kErrMaxBlocks);
-    nb = a.max_blocks;
-  }
-  if (nb > k.len) {
-    if (report) atomicOr(err, kErrBlockList);
-    nb = k.len < 0 ? 0 : k.len;
-  }
-  k.nb = (int)nb;
-  k.ok = true;
-  return k;
-}
-
-// Exclusive sum over the threads with a HIGHER index (suffix sum) of a block.
-__device__ __forceinline__ unsigned block_suffix_exclusive(unsigned v, unsigned* s_warp) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  unsigned x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const unsigned y = __shfl_down_sync(kFull, x, o);
-    if (lane + o < 32) x += y;
-  }
-  if (lane == 0) s_warp[warp] = x;
-  __syncthreads();
-  unsigned above = 0;
-  for (int w = warp + 1; w < nw; ++w) above += s_warp[w];
-  __syncthreads();
-  return x - v + above;
-}
-
-// Exclusive prefix sum over the threads with a LOWER index; *total = block sum.
-__device__ __forceinline__ unsigned block_prefix_exclusive(unsigned v, unsigned* s_warp, unsigned* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  unsigned x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const unsigned y = __shfl_up_sync(kFull, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) s_warp[warp] = x;
-  __syncthreads();
-  unsigned below = 0, all = 0;
-  for (int w = 0; w < nw; ++w) {
-    const unsigned s = s_warp[w];
-    if (w < warp) below += s;
-    all += s;
-  }
-  __syncthreads();
-  *total = all;
-  return x - v + below;
-}
-
-__device__ __forceinline__ void cp_async16_ptr(void* sdst, const void* gsrc) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"((uint32_t)__cvta_generic_to_shared(sdst)),
-               "l"(gsrc)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async4(void* sdst, const void* gsrc) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"((uint32_t)__cvta_generic_to_shared(sdst)),
-               "l"(gsrc)
-               : "memory");
-}
-
-// A cell id read from the block table, passed on as read (the attention masks
-// it) with the error bit set when it is out of range.
-__device__ __forceinline__ int flag_cell(int c, int64_t n_cells, unsigned* err) {
-  if (c < 0 || c >= n_cells) atomicOr(err, kErrCell);
-  return c;
-}
-
-// Unique 56-bit selection key of a block inside the threshold bin: the 20
-// low bits of the score key above the bitwise complement of the block index,
-// so a larger key means a larger score, or an equal score at a lower index.
-__device__ __forceinline__ unsigned long long cand_key(uint32_t key, int64_t j) {
-  return ((unsigned long long)(key & 0xFFFFFu) << 36) |
-         ((unsigned long long)(~(uint32_t)j) << 4);
-}
 
 // ----------------------------------------------------------------- k_score
 // Rows are read by groups of 8 lanes: lane `sub` of a group holds dims
@@ -235,7 +123,11 @@ k_score(const IndexArgs a, void* ws, float* __restrict__ scores, int chunk, unsi
   if (kTopk) QSA_TS(index, 0);
   // ---- before the wait: token geometry, query, slot ids (not written by
   // the pool update that precedes this kernel)
-  const Tok tk = token_geometry(a, t, err, blockIdx.x == 0 && tid == 0);
+  __shared__ int64_t s_off[kOffCache + 1];
+  const int seq_t = a.tok_seq[t], pos_t = a.tok_pos[t];
+  const bool offc = preload_offsets(a.seq_blk_off, a.n_seq, s_off);
+  __syncthreads();
+  const Tok tk = token_geometry(a, seq_t, pos_t, offc ? s_off : nullptr, err, blockIdx.x == 0 && tid == 0);
   const int nb = tk.nb;
   float* srow = scores + (int64_t)t * a.max_blocks;
   const int64_t j0 = (int64_t)blockIdx.x * chunk;
@@ -705,7 +597,11 @@ k_select(const IndexArgs a, void* ws, const float* __restrict__ scores,
   // classification, since the block table is written by the append that may
   // still be running when this kernel starts
   QSA_TS(index, 10);
-  const Tok tk = token_geometry(a, t, err, false);
+  __shared__ int64_t s_off[kOffCache + 1];
+  const int seq_t = a.tok_seq[t], pos_t = a.tok_pos[t];
+  const bool offc = preload_offsets(a.seq_blk_off, a.n_seq, s_off);
+  __syncthreads();
+  const Tok tk = token_geometry(a, seq_t, pos_t, offc ? s_off : nullptr, err, false);
   const int nb = tk.nb;
   const int64_t per = round_up(ceil_div(nb > 0 ? nb : 1, (int64_t)NC), 32);
   const int64_t j0 = (int64_t)rank * per;
@@ -720,6 +616,21 @@ k_select(const IndexArgs a, void* ws, const float* __restrict__ scores,
     sm.ncand = 0u;
     sm.ncent = 0u;
   }
+  // this CTA's slot ids (an input): copied into shared memory now, waited for
+  // before they are read; 16-byte copies where the list is aligned
+  const bool slots_cached = per <= kSelSlots;
+  // s_slots[j - j0] = slots[j]; the array starts 0-3 ints into the buffer so
+  // that it shares the block list's alignment modulo 16 bytes
+  int32_t* s_slots = s_dyn + ((reinterpret_cast<uintptr_t>(slots + j0) >> 2) & 3);
+  if (slots_cached && j1 > j0) {
+    const int64_t n = j1 - j0;
+    const int64_t head = min(n, (int64_t)((4 - ((reinterpret_cast<uintptr_t>(slots + j0) >> 2) & 3)) & 3));
+    const int64_t body = (n - head) / 4;
+    if (tid < head) cp_async4(s_slots + tid, slots + j0 + tid);
+    for (int64_t q = tid; q < body; q += kSelThreads) cp_async16_ptr(s_slots + head + 4 * q, slots + j0 + head + 4 * q);
+    for (int64_t i = head + 4 * body + tid; i < n; i += kSelThreads) cp_async4(s_slots + i, slots + j0 + i);
+  }
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
   // first half of a cluster barrier: the counters above are set before any
   // peer writes into this CTA (the matching wait follows the classification)
   cluster_arrive();
@@ -778,16 +689,9 @@ k_select(const IndexArgs a, void* ws, const float* __restrict__ scores,
   }
   const int thr = sm.thr, ncand_all = sm.ncand_all;
   const bool fast = thr < 0 || ncand_all <= kSelLocalCand;
-  // Which path resolves the cut (central: CTA 0 ranks, orders and expands
-  // alone), and the slot ids the expansion will read (copied into shared
-  // memory after the classification, waited for only before the expansion).
+  // Which path resolves the cut (central: CTA 0 ranks every CTA's
+  // threshold-bin keys, orders and expands the chosen blocks alone)
   const bool central = nb <= kCentralBlocks && (thr < 0 || ncand_all <= kRankMax);
-  const bool all_cached = central && rank == 0 && nb <= kSelSlots;   // CTA 0 holds every slot id
-  const bool slots_cached = !central && per <= kSelSlots;
-  const int64_t slot_lo = all_cached ? 0 : j0, slot_hi = all_cached ? nb : j1;
-  // s_slots[j - slot_lo] = slots[j]; the array starts 0-3 ints into the
-  // buffer so that it shares the block list's alignment modulo 16 bytes
-  int32_t* s_slots = s_dyn + ((reinterpret_cast<uintptr_t>(slots + slot_lo) >> 2) & 3);
   if (tid < tail && rank == 0) {
     if (tslot >= 0 && tslot < a.n_slots) {
       cp_async4(&sm.tail_cells[tid], a.blk_cells + (int64_t)tslot * r + tid);
@@ -834,20 +738,9 @@ k_select(const IndexArgs a, void* ws, const float* __restrict__ scores,
   }
   __syncthreads();
   QSA_TS(index, 13);
-  if (all_cached || slots_cached) {
-    // 16-byte copies where the list is 16-byte aligned, single ids at the ends
-    const int64_t n = slot_hi - slot_lo;
-    const int64_t head = min(n, (int64_t)((4 - ((reinterpret_cast<uintptr_t>(slots + slot_lo) >> 2) & 3)) & 3));
-    const int64_t body = (n - head) / 4;
-    if (tid < head) cp_async4(s_slots + tid, slots + slot_lo + tid);
-    for (int64_t q = tid; q < body; q += kSelThreads)
-      cp_async16_ptr(s_slots + head + 4 * q, slots + slot_lo + head + 4 * q);
-    for (int64_t i = head + 4 * body + tid; i < n; i += kSelThreads) cp_async4(s_slots + i, slots + slot_lo + i);
-    asm volatile("cp.async.commit_group;\n" ::: "memory");
-  }
   cluster_wait();
 
-  if (nb <= kCentralBlocks && (thr < 0 || ncand_all <= kRankMax)) {
+  if (central) {
     // ---- central path: every CTA sends its bitmap words and threshold-bin
     // keys into CTA 0's shared memory; CTA 0 ranks the keys, orders and
     // expands the chosen blocks alone.
@@ -959,7 +852,7 @@ k_select(const IndexArgs a, void* ws, const float* __restrict__ scores,
     int32_t* crow = cells + (int64_t)t * a.cells_pitch;
     for (int i = tid; i < nsel; i += kSelThreads) {
       const int j = s_list[i];
-      const int sl = all_cached ? s_slots[j] : slots[j];
+      const int sl = (slots_cached && j < j1) ? s_slots[j] : slots[j];   // CTA 0's own range is cached
       const bool sok = sl >= 0 && sl < a.n_slots;
       if (!sok) atomicOr(err, kErrSlot);
       int cv[8];
@@ -1334,13 +1227,11 @@ cudaError_t launch_index_scores(const IndexArgs& a, float* scores, unsigned* err
                     chunk, err);
 }
 
-cudaError_t launch_index_topk(const IndexArgs& a, int32_t* cells, int32_t* count,
-                              void* ws, unsigned* err, cudaStream_t stream) {
+cudaError_t launch_index_scores_topk(const IndexArgs& a, void* ws, unsigned* err, cudaStream_t stream) {
   if (a.n_tokens <= 0) return cudaSuccess;
   int sms = 0;
   cudaError_t e = index_setup(&sms);
   if (e != cudaSuccess) return e;
-  const size_t slot_bytes = sizeof(int32_t) * (kSelSlots + 4 + kSelList);
   IndexArgs b = a;
   b.max_blocks = a.max_blocks > 0 ? a.max_blocks : 1;
   float* sc = scores_of(ws, a.max_tokens);
@@ -1355,15 +1246,28 @@ cudaError_t launch_index_topk(const IndexArgs& a, int32_t* cells, int32_t* count
     const dim3 gh((unsigned)ceil_div(b.max_blocks, kHistChunk), (unsigned)a.n_tokens);
     e = launch_pdl(k_hist, gh, dim3(256), 0, stream, 1, b, ws, (const float*)sc);
     prof_after(kKHist, stream);
-    if (e != cudaSuccess) return e;
-  } else {
-    const int chunk = score_chunk(a.n_tokens, b.max_blocks, sms);
-    const dim3 g1((unsigned)ceil_div(b.max_blocks, chunk), (unsigned)a.n_tokens);
-    prof_before(kKScore, stream);
-    e = launch_pdl(k_score<true>, g1, dim3(kScoreThreads), kScoreSmem, stream, 1, b, ws, sc, chunk, err);
-    prof_after(kKScore, stream);
-    if (e != cudaSuccess) return e;
+    return e;
   }
+  const int chunk = score_chunk(a.n_tokens, b.max_blocks, sms);
+  const dim3 g1((unsigned)ceil_div(b.max_blocks, chunk), (unsigned)a.n_tokens);
+  prof_before(kKScore, stream);
+  e = launch_pdl(k_score<true>, g1, dim3(kScoreThreads), kScoreSmem, stream, 1, b, ws, sc, chunk, err);
+  prof_after(kKScore, stream);
+  return e;
+}
+
+cudaError_t launch_index_topk(const IndexArgs& a, int32_t* cells, int32_t* count,
+                              void* ws, unsigned* err, cudaStream_t stream) {
+  if (a.n_tokens <= 0) return cudaSuccess;
+  int sms = 0;
+  cudaError_t e = launch_index_scores_topk(a, ws, err, stream);
+  if (e != cudaSuccess) return e;
+  e = index_setup(&sms);
+  if (e != cudaSuccess) return e;
+  const size_t slot_bytes = sizeof(int32_t) * (kSelSlots + 4 + kSelList);
+  IndexArgs b = a;
+  b.max_blocks = a.max_blocks > 0 ? a.max_blocks : 1;
+  float* sc = scores_of(ws, a.max_tokens);
   prof_before(kKFinal, stream);
   const int nc = select_cluster(a.n_tokens, b.max_blocks, sms);
   e = launch_pdl(k_select, dim3((unsigned)nc, (unsigned)a.n_tokens), dim3(kSelThreads), slot_bytes, stream,

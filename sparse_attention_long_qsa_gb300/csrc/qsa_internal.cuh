@@ -102,6 +102,11 @@ __device__ __forceinline__ void st_dsmem_u32(uint32_t addr, unsigned v) {
 __device__ __forceinline__ void st_dsmem_u64(uint32_t addr, unsigned long long v) {
   asm volatile("st.shared::cluster.u64 [%0], %1;\n" ::"r"(addr), "l"(v) : "memory");
 }
+__device__ __forceinline__ unsigned atom_or_dsmem(uint32_t addr, unsigned v) {
+  unsigned old;
+  asm volatile("atom.shared::cluster.or.b32 %0, [%1], %2;\n" : "=r"(old) : "r"(addr), "r"(v) : "memory");
+  return old;
+}
 __device__ __forceinline__ unsigned atom_add_dsmem(uint32_t addr, unsigned v) {
   unsigned old;
   asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;\n" : "=r"(old) : "r"(addr), "r"(v) : "memory");
@@ -199,7 +204,7 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 // ------------------------------------------------------ measurement hook
 // Kernel ids of qsa_profile_kernel (include/qsa.h).
 enum KernelId : int { kKPool = 0, kKScore = 1, kKHist = 2, kKFinal = 3, kKAttn = 4, kKAppend = 5,
-                      kNumKernels = 6 };
+                      kKFused = 6, kNumKernels = 7 };
 struct ProfileHook {
   cudaEvent_t before[kNumKernels];
   cudaEvent_t after[kNumKernels];
@@ -246,10 +251,10 @@ struct IndexArgs {
   int n_recomputed;
 };
 
-// Workspace of qsa_index_topk: a 4096-bin histogram per token (the control
-// words, zero between calls), then the fp32 scores [max_tokens][max_blocks],
-// each part 256-byte aligned.
-constexpr int64_t kIndexCtrlBytes = (int64_t)sizeof(unsigned) * kHistBins;
+// Workspace of qsa_index_topk: per token a 4096-bin histogram and a reader
+// counter (the control words, zero between calls), then the fp32 scores
+// [max_tokens][max_blocks], each part 256-byte aligned.
+constexpr int64_t kIndexCtrlBytes = (int64_t)sizeof(unsigned) * kHistBins + 256;
 __host__ __device__ constexpr int64_t index_workspace_bytes_max(int64_t max_tokens, int64_t max_blocks) {
   return (max_tokens * kIndexCtrlBytes + 255) / 256 * 256 + (max_tokens * max_blocks * 4 + 255) / 256 * 256;
 }
@@ -264,6 +269,9 @@ void index_workspace_zero_range(int n_tokens, int64_t max_blocks, size_t* offset
 cudaError_t launch_index_scores(const IndexArgs& a, float* scores, unsigned* err, cudaStream_t stream);
 cudaError_t launch_index_topk(const IndexArgs& a, int32_t* cells, int32_t* count,
                               void* ws, unsigned* err, cudaStream_t stream);
+// The score kernels of qsa_index_topk alone (scores and threshold histogram
+// in the workspace), for a selection that runs elsewhere.
+cudaError_t launch_index_scores_topk(const IndexArgs& a, void* ws, unsigned* err, cudaStream_t stream);
 
 struct AttnArgs {
   int n_tokens;
@@ -282,6 +290,15 @@ struct AttnArgs {
 
 size_t attn_workspace_bytes(int n_tokens, int n_q_heads, int cells_pitch);
 cudaError_t launch_sparse_attn(const AttnArgs& a, void* ws, unsigned* err, cudaStream_t stream);
+// qsa_index_attn: the qsa_index_topk kernels and the attention kernel, or
+// (in_cluster, when its limits hold: *fused = true) the score kernels and
+// then the selection and the attention in one cluster kernel.
+cudaError_t launch_index_attn(const IndexArgs& ia, const AttnArgs& a, int32_t* cells, int32_t* count, void* ws,
+                              bool in_cluster, unsigned* err, cudaStream_t stream, bool* fused);
+// Whether qsa_index_attn runs the selection inside the attention clusters
+// for this shape (per-device occupancy decides the cluster size).
+cudaError_t index_attn_plan(int n_tokens, int n_kv_heads, int kv_q8, int cells_pitch, int64_t max_blocks,
+                            int n_sel_blocks, int r, bool* fused);
 
 // Append of new cells (append.cu).  The dirty list is built by one CTA:
 // at most kAppendMaxTokens tokens per call.

@@ -6,7 +6,7 @@ runs a step as the C-ABI calls on one stream:
 
     step:       pool_update(dirty) -> index_topk(tokens) -> sparse_attn(tokens)
     full_step:  kv_append(new cells, re-pooling the blocks they dirty) ->
-                index_topk(tokens) -> sparse_attn(tokens)
+                index_attn(tokens)  (index top-k and sparse attention in one call)
 
 It holds no arithmetic of its own.
 """
@@ -83,6 +83,17 @@ class QSALayer:
                        self.cells[:T], self.count[:T], self.ws_index, self.max_tokens,
                        recomputed, stream)
 
+    def index_attn(self, tok_seq, tok_pos, q_idx, w_idx, q, recomputed=None, stream=None, in_cluster=False,
+                   out=None):
+        """index_topk then sparse_attn in one call (qsa_index_attn); out:
+        where the attention output goes (default the layer's buffer; may be a
+        pinned host tensor)."""
+        T = int(tok_pos.numel())
+        qsa.index_attn(self.cfg, q_idx, w_idx, tok_seq, tok_pos, self.pooled, self.blk_cells,
+                       self.seq_blk_off, self.seq_blk_slots, self.max_blocks, q, self.k_cache, self.v_cache,
+                       self.n_cells, self.cells[:T], self.count[:T], self.out[:T] if out is None else out,
+                       self.ws_index, self.max_tokens, recomputed, stream, in_cluster=in_cluster)
+
     def sparse_attn(self, q, n_tokens: int, stream=None):
         T = int(n_tokens)
         qsa.sparse_attn(self.cfg, q, self.k_cache, self.v_cache, self.n_cells, self.cells[:T],
@@ -112,17 +123,20 @@ class QSALayer:
                       self.idx_k, self.blk_cells, self.seq_blk_off, self.seq_blk_slots, d, stream=stream, **extra)
         return d
 
-    def full_step(self, tok_seq, tok_pos, q, q_idx, w_idx, cells, k_new, v_new, idx_new, stream=None, **_):
+    def full_step(self, tok_seq, tok_pos, q, q_idx, w_idx, cells, k_new, v_new, idx_new, stream=None,
+                  in_cluster=False, out=None, **_):
         """The whole layer step from the new tokens on: append of their cells
         (K/V, indexer keys, table, device dirty list) with the pool update of
-        the blocks they dirty in the same launch, index top-k, sparse
-        attention.  Returns the out[:T] view (fp32)."""
+        the blocks they dirty in the same launch, then index top-k and sparse
+        attention in one qsa_index_attn call (in_cluster: the selection inside
+        the attention clusters).  The step's inputs and `out` may be pinned
+        host tensors.  Returns the output (fp32 [T][n_q_heads][head_dim])."""
         # the append re-pooled only the query tokens' own blocks: score work on
         # the other blocks may start before it finishes
         self.kv_append(tok_seq, tok_pos, cells, k_new, v_new, idx_new, stream, pool=True)
-        self.index_topk(tok_seq, tok_pos, q_idx, w_idx, recomputed="query_blocks", stream=stream)
-        self.sparse_attn(q, int(tok_pos.numel()), stream)
-        return self.out[:int(tok_pos.numel())]
+        self.index_attn(tok_seq, tok_pos, q_idx, w_idx, q, recomputed="query_blocks", stream=stream,
+                        in_cluster=in_cluster, out=out)
+        return self.out[:int(tok_pos.numel())] if out is None else out
 
     def set_cells(self, slots, rows):
         """Write block-table rows (the append of new cells), device side."""
@@ -150,7 +164,9 @@ class PackedInputs:
     """A step's input tensors laid out back to back (256-byte aligned) in one
     pinned host buffer and one device buffer, so that moving a step's inputs
     to the device is a single copy.  `views` are the device tensors to pass to
-    the layer's calls; `pack` fills a pinned host buffer from host arrays."""
+    the layer's calls; `pack` fills a pinned host buffer from host arrays and
+    `host_views` gives the tensors of such a buffer, which the calls can also
+    take directly (read in place over the host link)."""
 
     def __init__(self, fields: dict, device="cuda", pin=True):
         self.fields = {}
@@ -177,6 +193,10 @@ class PackedInputs:
                 raise ValueError(f"{k}: expected {shape} ({n} bytes), got {a.shape} ({a.nbytes} bytes)")
             hv[o:o + n] = a.view(np.uint8).reshape(-1)
         return host
+
+    def host_views(self, host):
+        """Tensors of the fields of a pinned host buffer made by `pack`."""
+        return {k: host[o:o + n].view(dtype).view(shape) for k, (o, shape, dtype, n) in self.fields.items()}
 
     def upload(self, host, stream=None):
         """One host-to-device copy of a packed step (asynchronous on `stream`,

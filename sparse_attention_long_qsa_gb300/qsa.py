@@ -21,6 +21,7 @@ QSA_OK = 0
 QSA_KV_F16 = 0
 QSA_KV_Q8_0 = 1
 QSA_HINT_QUERY_BLOCKS = -1
+QSA_INDEX_ATTN_IN_CLUSTER = 1
 STATUS = {0: "QSA_OK", -1: "QSA_ERR_INVALID_ARG", -2: "QSA_ERR_SHAPE", -3: "QSA_ERR_UNSUPPORTED",
           -4: "QSA_ERR_WORKSPACE", -5: "QSA_ERR_CUDA", -6: "QSA_ERR_DEVICE_BOUNDS"}
 
@@ -28,11 +29,11 @@ STATUS = {0: "QSA_OK", -1: "QSA_ERR_INVALID_ARG", -2: "QSA_ERR_SHAPE", -3: "QSA_
 EXPORTS = ("qsa_config_init", "qsa_cells_per_token", "qsa_pool_update", "qsa_index_scores",
            "qsa_index_topk_workspace_size", "qsa_index_topk", "qsa_index_topk_noalloc",
            "qsa_sparse_attn_workspace_size",
-           "qsa_sparse_attn", "qsa_kv_append", "qsa_blocks_dirty", "qsa_debug_check", "qsa_profile_kernel",
-           "qsa_index_topk_kernels", "qsa_status_string")
+           "qsa_sparse_attn", "qsa_index_attn", "qsa_index_attn_kernels", "qsa_kv_append", "qsa_blocks_dirty",
+           "qsa_debug_check", "qsa_profile_kernel", "qsa_index_topk_kernels", "qsa_status_string")
 
 # Kernel ids of qsa_profile_kernel.
-KERNELS = {"pool": 0, "score": 1, "hist": 2, "select": 3, "attn": 4, "append": 5}
+KERNELS = {"pool": 0, "score": 1, "hist": 2, "select": 3, "attn": 4, "append": 5, "select_attn": 6}
 
 
 class QSAError(RuntimeError):
@@ -96,6 +97,11 @@ def _load():
     L.qsa_sparse_attn_workspace_size.restype = _SZ
     L.qsa_sparse_attn.argtypes = [CP, _I32, _P, _P, _P, _I64, _P, _P, _P, _P, _SZ, _P]
     L.qsa_sparse_attn.restype = _I32
+    L.qsa_index_attn.argtypes = [CP, _I32, _I32, _P, _P, _P, _P, _P, _P, _I64, _P, _P, _I32, _I64,
+                                 _P, _P, _P, _I64, _P, _P, _P, _P, _I32, ctypes.c_uint32, _P, _SZ, _P]
+    L.qsa_index_attn.restype = _I32
+    L.qsa_index_attn_kernels.argtypes = [CP, _I32, _I32, _I64, ctypes.c_uint32]
+    L.qsa_index_attn_kernels.restype = ctypes.c_uint32
     L.qsa_kv_append.argtypes = [CP, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _P, _I64, _P, _P, _I32,
                                 _P, _I32, _P, _P, _P, _P]
     L.qsa_kv_append.restype = _I32
@@ -146,7 +152,10 @@ def _stream(stream):
     return stream.cuda_stream
 
 
-def _ptr(t, dtype, name, allow_none=False):
+def _ptr(t, dtype, name, allow_none=False, host_ok=False):
+    """Device address of a CUDA tensor on the current device.  host_ok: a
+    step's own inputs and outputs may instead be page-locked (pinned) host
+    tensors, which the kernels read and write in place over the host link."""
     import torch
     if t is None:
         if allow_none:
@@ -155,8 +164,10 @@ def _ptr(t, dtype, name, allow_none=False):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch tensor")
     if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor (libqsa has no CPU path)")
-    if t.get_device() != torch.cuda.current_device():
+        if not (host_ok and t.is_pinned()):
+            raise ValueError(f"{name} must be a CUDA tensor" + (" or a pinned host tensor" if host_ok else "")
+                             + " (libqsa has no CPU path)")
+    elif t.get_device() != torch.cuda.current_device():
         # the library launches on the current device: another device's
         # memory would be read through an address that is not mapped there
         raise ValueError(f"{name} is on {t.device}, the current device is cuda:{torch.cuda.current_device()}")
@@ -165,6 +176,11 @@ def _ptr(t, dtype, name, allow_none=False):
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     return t.data_ptr()
+
+
+def _io(t, dtype, name):
+    """A step input or output: device memory or pinned host memory."""
+    return _ptr(t, dtype, name, host_ok=True)
 
 
 def cells_per_token(cfg: Config) -> int:
@@ -190,8 +206,8 @@ def index_scores(cfg, q_idx, w_idx, tok_seq, tok_pos, pooled, seq_blk_off, seq_b
     import torch
     T = int(tok_pos.numel())
     st = lib().qsa_index_scores(
-        ctypes.byref(cfg), T, _ptr(q_idx, torch.float32, "q_idx"), _ptr(w_idx, torch.float32, "w_idx"),
-        _ptr(tok_seq, torch.int32, "tok_seq"), _ptr(tok_pos, torch.int32, "tok_pos"),
+        ctypes.byref(cfg), T, _io(q_idx, torch.float32, "q_idx"), _io(w_idx, torch.float32, "w_idx"),
+        _io(tok_seq, torch.int32, "tok_seq"), _io(tok_pos, torch.int32, "tok_pos"),
         _ptr(pooled, torch.float32, "pooled"), int(pooled.shape[0]),
         _ptr(seq_blk_off, torch.int64, "seq_blk_off"), _ptr(seq_blk_slots, torch.int32, "seq_blk_slots"),
         int(seq_blk_off.numel()) - 1, int(max_blocks), _ptr(scores, torch.float32, "scores"),
@@ -219,9 +235,9 @@ def index_topk(cfg, q_idx, w_idx, tok_seq, tok_pos, pooled, blk_cells, seq_blk_o
         rec_ptr = _ptr(recomputed, torch.int32, "recomputed") if recomputed is not None else None
         rec_n = int(recomputed.numel()) if recomputed is not None else 0
     st = lib().qsa_index_topk(
-        ctypes.byref(cfg), T, int(max_tokens), _ptr(q_idx, torch.float32, "q_idx"),
-        _ptr(w_idx, torch.float32, "w_idx"),
-        _ptr(tok_seq, torch.int32, "tok_seq"), _ptr(tok_pos, torch.int32, "tok_pos"),
+        ctypes.byref(cfg), T, int(max_tokens), _io(q_idx, torch.float32, "q_idx"),
+        _io(w_idx, torch.float32, "w_idx"),
+        _io(tok_seq, torch.int32, "tok_seq"), _io(tok_pos, torch.int32, "tok_pos"),
         _ptr(pooled, torch.float32, "pooled"), _ptr(blk_cells, torch.int32, "blk_cells"),
         int(pooled.shape[0]), _ptr(seq_blk_off, torch.int64, "seq_blk_off"),
         _ptr(seq_blk_slots, torch.int32, "seq_blk_slots"), int(seq_blk_off.numel()) - 1,
@@ -229,6 +245,42 @@ def index_topk(cfg, q_idx, w_idx, tok_seq, tok_pos, pooled, blk_cells, seq_blk_o
         _ptr(count, torch.int32, "count"), rec_ptr, rec_n, _ptr(workspace, torch.uint8, "workspace"),
         int(workspace.numel()), _stream(stream))
     _check(st, "qsa_index_topk")
+
+
+def index_attn(cfg, q_idx, w_idx, tok_seq, tok_pos, pooled, blk_cells, seq_blk_offs, seq_blk_slots,
+               max_blocks: int, q, k_cache, v_cache, n_cells: int, cells, count, out, workspace,
+               max_tokens: int, recomputed=None, stream=None, in_cluster: bool = False):
+    """qsa_index_topk then qsa_sparse_attn in one call (same workspace and
+    hint as index_topk); fills cells, count and out.  in_cluster: the
+    selection runs inside the attention clusters where the call's limits
+    allow (QSA_INDEX_ATTN_IN_CLUSTER)."""
+    import torch
+    T = int(tok_pos.numel())
+    if isinstance(recomputed, str) and recomputed == "query_blocks":
+        rec_ptr, rec_n = None, QSA_HINT_QUERY_BLOCKS
+    else:
+        rec_ptr = _ptr(recomputed, torch.int32, "recomputed") if recomputed is not None else None
+        rec_n = int(recomputed.numel()) if recomputed is not None else 0
+    st = lib().qsa_index_attn(
+        ctypes.byref(cfg), T, int(max_tokens), _io(q_idx, torch.float32, "q_idx"),
+        _io(w_idx, torch.float32, "w_idx"),
+        _io(tok_seq, torch.int32, "tok_seq"), _io(tok_pos, torch.int32, "tok_pos"),
+        _ptr(pooled, torch.float32, "pooled"), _ptr(blk_cells, torch.int32, "blk_cells"),
+        int(pooled.shape[0]), _ptr(seq_blk_offs, torch.int64, "seq_blk_off"),
+        _ptr(seq_blk_slots, torch.int32, "seq_blk_slots"), int(seq_blk_offs.numel()) - 1,
+        int(max_blocks), _io(q, torch.float16, "q"), _ptr(k_cache, None, "k_cache"),
+        _ptr(v_cache, None, "v_cache"), int(n_cells), _ptr(cells, torch.int32, "cells"),
+        _ptr(count, torch.int32, "count"), _io(out, torch.float32, "out"), rec_ptr, rec_n,
+        QSA_INDEX_ATTN_IN_CLUSTER if in_cluster else 0,
+        _ptr(workspace, torch.uint8, "workspace"), int(workspace.numel()), _stream(stream))
+    _check(st, "qsa_index_attn")
+
+
+def index_attn_kernels(cfg, n_tokens: int, n_seq: int, max_blocks: int, in_cluster: bool = False) -> list:
+    """Names of the kernels one index_attn call launches on the current device."""
+    m = int(lib().qsa_index_attn_kernels(ctypes.byref(cfg), int(n_tokens), int(n_seq), int(max_blocks),
+                                         QSA_INDEX_ATTN_IN_CLUSTER if in_cluster else 0))
+    return [k for k, v in KERNELS.items() if (m >> v) & 1]
 
 
 def sparse_attn_workspace_size(cfg, n_tokens: int) -> int:
@@ -241,9 +293,9 @@ def sparse_attn(cfg, q, k_cache, v_cache, n_cells: int, cells, count, out, works
     ws_ptr = _ptr(workspace, torch.uint8, "workspace") if workspace is not None and workspace.numel() else None
     ws_len = int(workspace.numel()) if workspace is not None else 0
     st = lib().qsa_sparse_attn(
-        ctypes.byref(cfg), T, _ptr(q, torch.float16, "q"), _ptr(k_cache, None, "k_cache"),
+        ctypes.byref(cfg), T, _io(q, torch.float16, "q"), _ptr(k_cache, None, "k_cache"),
         _ptr(v_cache, None, "v_cache"), int(n_cells), _ptr(cells, torch.int32, "cells"),
-        _ptr(count, torch.int32, "count"), _ptr(out, torch.float32, "out"),
+        _ptr(count, torch.int32, "count"), _io(out, torch.float32, "out"),
         ws_ptr, ws_len, _stream(stream))
     _check(st, "qsa_sparse_attn")
 
@@ -260,10 +312,10 @@ def kv_append(cfg, tok_seq, tok_pos, cells, k_new, v_new, idx_new, k_cache, v_ca
                      _ptr(pooled, torch.float32, "pooled"))
     n_cells = int(idx_k.shape[0])
     st = lib().qsa_kv_append(
-        ctypes.byref(cfg), int(tok_pos.numel()), _ptr(tok_seq, torch.int32, "tok_seq"),
-        _ptr(tok_pos, torch.int32, "tok_pos"), _ptr(cells, torch.int32, "cells"),
-        _ptr(k_new, torch.float16, "k_new"), _ptr(v_new, torch.float16, "v_new"),
-        _ptr(idx_new, torch.float16, "idx_new"), _ptr(k_cache, None, "k_cache"), _ptr(v_cache, None, "v_cache"),
+        ctypes.byref(cfg), int(tok_pos.numel()), _io(tok_seq, torch.int32, "tok_seq"),
+        _io(tok_pos, torch.int32, "tok_pos"), _io(cells, torch.int32, "cells"),
+        _io(k_new, torch.float16, "k_new"), _io(v_new, torch.float16, "v_new"),
+        _io(idx_new, torch.float16, "idx_new"), _ptr(k_cache, None, "k_cache"), _ptr(v_cache, None, "v_cache"),
         _ptr(idx_k, torch.float16, "idx_k"), n_cells, _ptr(blk_cells, torch.int32, "blk_cells"),
         int(blk_cells.shape[0]), _ptr(seq_blk_off, torch.int64, "seq_blk_off"),
         _ptr(seq_blk_slots, torch.int32, "seq_blk_slots"), int(seq_blk_off.numel()) - 1,

@@ -92,8 +92,13 @@ class Runner:
     """A workload on the GPU, stepped through the C ABI, with the oracle
     state kept alongside for comparison."""
 
-    def __init__(self, wl, warm_check_slots=None):
+    def __init__(self, wl, warm_check_slots=None, mode="calls"):
+        """mode "calls": pool update, index top-k, attention (three calls);
+        "index_attn": pool update, then index top-k and attention in one
+        qsa_index_attn call; "in_cluster": the same with the selection inside
+        the attention clusters."""
         self.wl = wl
+        self.mode = mode
         self.layer = QSALayer.from_workload(wl, 0)
         self.layer.warm(torch.from_numpy(wl.prompt_dirty()).cuda())
         self.step_idx = 0
@@ -108,7 +113,13 @@ class Runner:
             L.set_cells(slots, rows)
         st = wl.steps[i]
         inp = step_inputs(st)
-        out = L.step(**inp)
+        if self.mode in ("index_attn", "in_cluster"):
+            L.pool_update(inp["dirty"])
+            L.index_attn(inp["tok_seq"], inp["tok_pos"], inp["q_idx"], inp["w_idx"], inp["q"],
+                         recomputed=inp["dirty"], in_cluster=self.mode == "in_cluster")
+            out = L.out[:len(st.tok_pos)]
+        else:
+            out = L.step(**inp)
         torch.cuda.synchronize()
         T = len(st.tok_pos)
         return dict(out=to_np(out), cells=to_np(L.cells[:T]), count=to_np(L.count[:T]),
