@@ -47,7 +47,13 @@ METRIC = "QSA-layer decode tokens/s at 50k/250k ctx (1 and 5 seqs); HBM GB/s vs 
 # sources whose hash is stored beside it.  The line reports the number only
 # while the kernel's sources still hash to that value (null otherwise, and for
 # a workload or kernel without an entry).
-NCU_TRAFFIC = {}
+NCU_CMD_250K = ("ncu --set full --clock-control none -k regex:<kernel> -s 6 -c 1 python bench.py --config 250k_q8 "
+                "--steps 8 --warmup 3 --secondary none --target none --no-cpu --no-compare --flush-mb 256")
+NCU_TRAFFIC = {
+    ("250k_q8", "score"): {"bytes": 33_289_984, "source": "0e8e020ab527cc7f", "capture": NCU_CMD_250K},
+    ("250k_q8", "select"): {"bytes": 647_168, "source": "12a017b968c7226f", "capture": NCU_CMD_250K},
+    ("250k_q8", "attn"): {"bytes": 2_314_240, "source": "1338b592cb9ad74a", "capture": NCU_CMD_250K},
+}
 KERNEL_SOURCES = {
     "append": ("append.cu", "pool_row.cuh", "qsa_internal.cuh"),
     "pool": ("pool.cu", "pool_row.cuh", "qsa_internal.cuh"),
@@ -631,7 +637,7 @@ def run_native(args, rank, world, local):
     # the 250k q8_0 decode (the long-context target) on a complete line of its
     # own: end to end, CPU baseline, roofline
     target = None
-    if args.target and args.target != args.config and rank == 0:
+    if args.target not in ("", "none", args.config) and rank == 0:
         rt = measure_config(args.target, min(args.steps, 256), args.warmup, dev, path=args.path)
         cpu_t = None if args.no_cpu else cpu_line(rt["wl"], args.target, args.cpu_seconds)
         target = workload_line(rt, args.target, hbm, peak_src, cpu_t)
