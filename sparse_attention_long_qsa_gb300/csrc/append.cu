@@ -12,8 +12,9 @@
 // away from zero, all in fp32.
 //
 // One warp per (token, row): rows 0..G-1 are the K heads, G..2G-1 the V
-// heads, 2G the indexer key together with the table entry.  An extra last CTA
-// builds the dirty list: the distinct slots, ascending, padded with -1.
+// heads, 2G the indexer key together with the table entry; that warp of each
+// block's first new token then re-pools the block.  An extra last CTA builds
+// the dirty list: the distinct slots, ascending, padded with -1.
 // Everything is read and encoded before the grid-dependency wait (the new
 // rows are inputs, not outputs of the preceding kernel); only the stores wait.
 #include "pool_row.cuh"
@@ -124,8 +125,6 @@ k_append(const AppendArgs a, const Turns turns, unsigned* err) {
   if (dirty_cta) {
     // ---- the dirty list (n_new <= kAppendMaxTokens, 4 tokens per thread)
     __shared__ int s_slot[kAppendMaxTokens];
-    __shared__ unsigned char s_ib[kAppendMaxTokens];
-    __shared__ int s_dslot[kAppendMaxTokens];
     __shared__ unsigned s_warp[kAppWarps];
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
@@ -133,7 +132,6 @@ k_append(const AppendArgs a, const Turns turns, unsigned* err) {
       if (u >= a.n_new) break;
       int ib = 0;
       s_slot[u] = token_slot(a, mine[k], s_off, &ib, err, false);
-      s_ib[u] = (unsigned char)ib;
     }
     __syncthreads();
     // token t leads its slot if no earlier token has it; leaders are ranked
@@ -172,56 +170,8 @@ k_append(const AppendArgs a, const Turns turns, unsigned* err) {
     QSA_TS_IF(append, 2, tid == 0);
 #pragma unroll
     for (int k = 0; k < kAppendMaxTokens / kAppThreads; ++k)
-      if (rank[k] >= 0 && rank[k] < a.n_dirty) {
-        a.dirty[rank[k]] = lead_slot[k];
-        s_dslot[rank[k]] = lead_slot[k];
-      }
+      if (rank[k] >= 0 && rank[k] < a.n_dirty) a.dirty[rank[k]] = lead_slot[k];
     for (int i = (int)n_lead + tid; i < a.n_dirty; i += kAppThreads) a.dirty[i] = -1;
-    if (a.pooled == nullptr) return;
-    __syncthreads();
-    // ---- re-pool the dirtied blocks, one warp per block (as qsa_pool_update
-    // would after this launch): members from the table, except the positions
-    // this launch appends, whose cells and keys come from the inputs (other
-    // warps of this launch are writing them)
-    const int nl = min((int)n_lead, a.n_dirty);
-    for (int e = warp; e < nl; e += kAppWarps) {
-      const int slot = s_dslot[e];
-      int m = -1, tn = -1;
-      if (lane < a.r) {
-        m = a.blk_cells[(int64_t)slot * a.r + lane];
-        for (int t = 0; t < a.n_new; ++t)
-          if (s_slot[t] == slot && s_ib[t] == lane) {
-            m = a.cell[t];
-            tn = t;
-          }
-      }
-      int cell[kMaxR], tnew[kMaxR];
-#pragma unroll
-      for (int i = 0; i < kMaxR; ++i) {
-        cell[i] = __shfl_sync(kFull, m, i);
-        tnew[i] = __shfl_sync(kFull, tn, i);
-        if (i >= a.r) cell[i] = -1;
-      }
-      const int blk = a.slot_block_idx[slot];
-      float2 lo[kMaxR], hi[kMaxR];
-      bool present[kMaxR];
-#pragma unroll
-      for (int i = 0; i < kMaxR; ++i) {
-        const bool ok = cell[i] >= 0 && cell[i] < a.n_cells;
-        if (cell[i] >= a.n_cells && lane == 0) atomicOr(err, kErrCell);
-        const __half* src = tnew[i] >= 0 ? a.idx_new + (int64_t)tnew[i] * kIdxDim
-                                         : a.idx_k + (int64_t)(ok ? cell[i] : 0) * kIdxDim;
-        const __half2* row = reinterpret_cast<const __half2*>(src);
-        lo[i] = ok ? __half22float2(row[lane]) : make_float2(0.f, 0.f);
-        hi[i] = ok ? __half22float2(row[32 + lane]) : make_float2(0.f, 0.f);
-        present[i] = ok;
-      }
-      float2 olo, ohi;
-      pool_rows_warp(lo, hi, present, blk, a.r, a.norm_w, turns, a.eps, &olo, &ohi);
-      float* out = a.pooled + (int64_t)slot * kIdxDim;
-      reinterpret_cast<float2*>(out)[lane] = olo;
-      reinterpret_cast<float2*>(out)[32 + lane] = ohi;
-    }
     return;
   }
 
@@ -288,6 +238,65 @@ k_append(const AppendArgs a, const Turns turns, unsigned* err) {
   if (!ok) return;
   if (lane < 16) reinterpret_cast<uint4*>(a.idx_k + c * kIdxDim)[lane] = raw;
   if (lane == 0) a.blk_cells[(int64_t)slot * a.r + ib] = (int32_t)c;
+  if (a.pooled == nullptr) return;
+
+  // ---- re-pool this token's block (as qsa_pool_update would after this
+  // launch) if this is the block's first new token: the warps of all tokens
+  // re-pool their blocks in parallel.  Members come from the table, except
+  // the positions this launch appends, whose cells and keys come from the
+  // inputs (other warps of this launch are writing them).  One pass over the
+  // new tokens, 32 at a time, finds both.
+  const int r = a.r;
+  const int64_t jb = (int64_t)mine[0].p / r;
+  int tn = -1;            // lane i < r: the new token at position jb * r + i
+  bool earlier = false;   // a token before this one falls in the same block
+  for (int u0 = 0; u0 < a.n_new; u0 += 32) {
+    const int u = u0 + lane;
+    bool hit = false;
+    int pos_in = 0;
+    if (u < a.n_new) {
+      const int su = a.tok_seq[u], pu = a.tok_pos[u];
+      hit = su == mine[0].s && pu >= 0 && (int64_t)pu / r == jb;
+      pos_in = pu - (int)(jb * r);
+    }
+    earlier |= __any_sync(kFull, hit && u < t);
+    unsigned m = __ballot_sync(kFull, hit);
+    while (m) {
+      const int src = __ffs(m) - 1;
+      m &= m - 1u;
+      const int at = __shfl_sync(kFull, pos_in, src);
+      if (lane == at) tn = u0 + src;
+    }
+  }
+  if (earlier) return;
+  int mcell = -1;
+  if (lane < r) mcell = tn >= 0 ? a.cell[tn] : a.blk_cells[(int64_t)slot * r + lane];
+  int cell[kMaxR], tnew[kMaxR];
+#pragma unroll
+  for (int i = 0; i < kMaxR; ++i) {
+    cell[i] = __shfl_sync(kFull, mcell, i);
+    tnew[i] = __shfl_sync(kFull, tn, i);
+    if (i >= r) cell[i] = -1;
+  }
+  const int blk = a.slot_block_idx[slot];
+  float2 lo[kMaxR], hi[kMaxR];
+  bool present[kMaxR];
+#pragma unroll
+  for (int i = 0; i < kMaxR; ++i) {
+    const bool pok = cell[i] >= 0 && cell[i] < a.n_cells;
+    if (cell[i] >= a.n_cells && lane == 0) atomicOr(err, kErrCell);
+    const __half* src = (i < r && tnew[i] >= 0) ? a.idx_new + (int64_t)tnew[i] * kIdxDim
+                                                : a.idx_k + (int64_t)(pok ? cell[i] : 0) * kIdxDim;
+    const __half2* row = reinterpret_cast<const __half2*>(src);
+    lo[i] = pok ? __half22float2(row[lane]) : make_float2(0.f, 0.f);
+    hi[i] = pok ? __half22float2(row[32 + lane]) : make_float2(0.f, 0.f);
+    present[i] = pok;
+  }
+  float2 olo, ohi;
+  pool_rows_warp(lo, hi, present, blk, r, a.norm_w, turns, a.eps, &olo, &ohi);
+  float* out = a.pooled + (int64_t)slot * kIdxDim;
+  reinterpret_cast<float2*>(out)[lane] = olo;
+  reinterpret_cast<float2*>(out)[32 + lane] = ohi;
 }
 
 }  // namespace

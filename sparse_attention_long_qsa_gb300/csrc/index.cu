@@ -296,63 +296,98 @@ k_score(const IndexArgs a, void* ws, float* __restrict__ scores, int chunk, unsi
 
 // ------------------------------------------------------------- k_score_tc
 // Token-tiled scores on the tensor cores: D[row][4u + h] = pooled[row] .
-// q_idx[t0 + u][h] for M = 128 rows x N = 4 NT (NT tokens x 4 heads) x K =
-// 128 dims, tcgen05 kind::tf32 with each fp32 operand split in two, x = t(x)
-// + l(x), t(x) = x with its low 13 mantissa bits cleared (a TF32 value) and
-// l(x) = x - t(x) rounded to TF32:  D = t(A) t(B) + t(A) l(B) + l(A) t(B),
+// q_idx[t0 + u][h] for M = 128 block rows x N = 128 (32 tokens x 4 heads) x
+// K = 128 dims, tcgen05 kind::tf32 with each fp32 operand split in two,
+// x = t(x) + l(x), t(x) = x with its low 13 mantissa bits cleared (a TF32
+// value) and l(x) = x - t(x) rounded to TF32:
+//   D = t(A) t(B) + t(A) l(B) + l(A) t(B),
 // every product exact in fp32, accumulated in fp32 in tensor memory.  The
 // omitted l(A) l(B) and the rounding of l(.) are below 2^-21 of each product,
-// under the rounding of an fp32 FMA chain over 128 terms.  A is gathered by
-// slot with cp.async into a 128B-swizzled K-major tile, KC dims at a time,
-// and split in place; B (the query tile) is split once per CTA.  The
-// epilogue turns the 4 head dots of a (row, token) into its score as k_score
-// does, warps 0-3 for the first half of the tokens, warps 4-7 for the second.
-template <int NT, int KC>
-struct TcShape {
-  static constexpr int N = NT * 4;
-  static constexpr uint32_t kBBytes = (uint32_t)N * 512u;        // t(B) or l(B): N rows x 128 fp32
-  static constexpr uint32_t kABytes = 128u * KC * 4u;            // t(A) or l(A): 128 rows x KC fp32
-  static constexpr uint32_t kOffBt = 0, kOffBl = kBBytes;
-  static constexpr uint32_t kOffAt = 2 * kBBytes, kOffAl = 2 * kBBytes + kABytes;
-  static constexpr uint32_t kOffBar = 2 * kBBytes + 2 * kABytes;
-  static constexpr uint32_t kOffTmem = kOffBar + 8;
-  static constexpr uint32_t kOffSlot = kOffBar + 16;             // int32 [128]
-  static constexpr size_t kSmem = kOffSlot + 128 * 4 + 1024;     // + alignment slack
-  static constexpr uint32_t kTmemCols = N < 32 ? 32u : (uint32_t)N;
-  // kind::tf32: fp32 accumulate, A and B TF32, both K-major, N, M = 128
-  static constexpr uint32_t kIdesc = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) |
-                                     ((128u >> 4) << 24);
-  static_assert(NT % 8 == 0 && N <= 256 && N % 16 == 0, "token tile");
-  static_assert(KC % 32 == 0 && 128 % KC == 0, "dim chunk");
-};
+// under the rounding of an fp32 FMA chain over 128 terms.
+//
+// The split query tile is stored as one 256-row operand [t(B); l(B)], so one
+// MMA with N = 256 gives t(A) t(B) (columns 0-127) and t(A) l(B) (columns
+// 128-255) and a second with N = 128 adds l(A) t(B) to columns 0-127: t(A) is
+// read once per K step.  One CTA per SM, 288 threads in three roles that meet
+// only at mbarriers (every wait bounded):
+//   warps 0-3  gather: thread p takes row p of the tile, 32 dims (one
+//              128-byte line) per chunk, with cp.async into a 3-stage ring,
+//              two chunks ahead, and splits its own line in place into t(A)
+//              and l(A) once it lands;
+//   warp 8     issues the MMAs of a chunk when its stage is full and frees
+//              the stage (tcgen05.commit) when they complete; tensor memory
+//              holds two accumulators so a row tile's MMAs run while the
+//              previous tile is read out;
+//   warps 4-7  epilogue: thread e reads row e of the accumulator, sums the
+//              two halves, and writes the scores of the tile's tokens.
+constexpr int kTcTok = 32;                       // tokens per tile
+constexpr int kTcN = 4 * kTcTok;                 // B rows of t(B) (and of l(B))
+constexpr int kTcKC = 32;                        // dims per chunk: one 128-byte swizzle atom of fp32
+constexpr int kTcChunks = kIdxDim / kTcKC;       // 4
+constexpr int kTcStages = 3;
+constexpr int kTcGather = 128;                   // warps 0-3
+constexpr int kTcEpi = 128;                      // warps 4-7
+constexpr int kTcThreads = kTcGather + kTcEpi + 32;
+constexpr int kTcMaxSeq = kTcTok;                // distinct sequences in a tile
+constexpr uint32_t kTcOffB = 0;                                // [t(B); l(B)]: 256 rows x 128 fp32
+constexpr uint32_t kTcBBytes = 2u * kTcN * 512u;               // 128 KB
+constexpr uint32_t kTcOffA = kTcOffB + kTcBBytes;              // stages: t(A) 16 KB then l(A) 16 KB
+constexpr uint32_t kTcAHalf = 128u * kTcKC * 4u;
+constexpr uint32_t kTcStageBytes = 2u * kTcAHalf;
+constexpr uint32_t kTcOffBar = kTcOffA + kTcStages * kTcStageBytes;
+constexpr uint32_t kTcNumBars = 2 * kTcStages + 4;             // full, empty per stage; acc full, acc empty x 2
+constexpr uint32_t kTcOffTmem = kTcOffBar + 8 * kTcNumBars;
+constexpr size_t kTcSmem = kTcOffTmem + 16 + 1024;             // + alignment slack
+constexpr uint32_t kTcTmemCols = 512;                          // two accumulators of 256 columns
+// kind::tf32: fp32 accumulate, A and B TF32, both K-major, M = 128
+constexpr uint32_t kTcIdesc256 = (1u << 4) | (2u << 7) | (2u << 10) | ((256u >> 3) << 17) | ((128u >> 4) << 24);
+constexpr uint32_t kTcIdesc128 = (1u << 4) | (2u << 7) | (2u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+static_assert(kTcSmem + 1024 <= 227u * 1024u, "token-tiled scorer shared memory");
 
 __device__ __forceinline__ float tf32_trunc(float x) { return __uint_as_float(__float_as_uint(x) & 0xffffe000u); }
 // x rounded to the nearest TF32 value (ties away from zero)
 __device__ __forceinline__ float tf32_round(float x) {
   return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u);
 }
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
 
-template <int NT, int KC, bool kTopk>
-__global__ void __launch_bounds__(256, 1)
+template <bool kTopk>
+__global__ void __launch_bounds__(kTcThreads, 1)
 k_score_tc(const IndexArgs a, float* __restrict__ scores, unsigned* err) {
-  using S = TcShape<NT, KC>;
   extern __shared__ unsigned char tc_smem_raw[];
   const uint32_t raw_s = smem_u32(tc_smem_raw);
   const uint32_t base_s = (raw_s + 1023u) & ~1023u;
   unsigned char* base = tc_smem_raw + (base_s - raw_s);
-  int32_t* s_slot = reinterpret_cast<int32_t*>(base + S::kOffSlot);
-  const uint32_t bar = base_s + S::kOffBar;
-  __shared__ int s_seq[NT], s_nb[NT];
-  __shared__ int64_t s_off[NT];
-  __shared__ float s_w[NT][kIdxHeads];
+  __shared__ int s_seq[kTcTok], s_nb[kTcTok];
+  __shared__ int64_t s_off[kTcTok];
+  __shared__ float s_w[kTcTok][kIdxHeads];
+  // the tile's distinct sequences: token mask, blocks, list offset, and the
+  // prefix of this CTA's row tiles over them
+  __shared__ unsigned s_dmask[kTcMaxSeq];
+  __shared__ int s_dnb[kTcMaxSeq], s_dpre[kTcMaxSeq + 1];
+  __shared__ int64_t s_doff[kTcMaxSeq];
+  __shared__ int s_nd;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int t0 = blockIdx.y * NT;
+  const int t0 = blockIdx.y * kTcTok;
+  const uint32_t bar_full = base_s + kTcOffBar, bar_empty = bar_full + 8 * kTcStages;
+  const uint32_t bar_accf = bar_empty + 8 * kTcStages, bar_acce = bar_accf + 16;
 
-  // ---- before the wait: tensor memory, barrier, tokens, query tile
-  if (warp == 0) tmem_alloc(base_s + S::kOffTmem, S::kTmemCols);
-  if (tid == 0) mbar_init(bar, 1);
-  if (tid < NT) {
+  // ---- before the wait: tensor memory, barriers, tokens, the split query tile
+  if (warp == 0) tmem_alloc(base_s + kTcOffTmem, kTcTmemCols);
+  if (tid == 0) {
+    for (int q = 0; q < kTcStages; ++q) {
+      mbar_init(bar_full + 8 * q, kTcGather);
+      mbar_init(bar_empty + 8 * q, 1);
+    }
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(bar_accf + 8 * q, 1);
+      mbar_init(bar_acce + 8 * q, kTcEpi);
+    }
+  }
+  if (tid < kTcTok) {
     const int t = t0 + tid;
     int seq = -1, nb = 0;
     int64_t off = 0;
@@ -370,7 +405,7 @@ k_score_tc(const IndexArgs a, float* __restrict__ scores, unsigned* err) {
 #pragma unroll
     for (int h = 0; h < kIdxHeads; ++h) s_w[tid][h] = t < a.n_tokens ? a.w_idx[(int64_t)t * kIdxHeads + h] : 0.f;
   }
-  for (int i = tid; i < S::N * (kIdxDim / 4); i += 256) {
+  for (int i = tid; i < kTcN * (kIdxDim / 4); i += kTcThreads) {
     const int n = i / (kIdxDim / 4), c16 = i % (kIdxDim / 4);
     const int t = t0 + (n >> 2);
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -379,137 +414,192 @@ k_score_tc(const IndexArgs a, float* __restrict__ scores, unsigned* err) {
     const float4 vt = make_float4(tf32_trunc(v.x), tf32_trunc(v.y), tf32_trunc(v.z), tf32_trunc(v.w));
     const float4 vl = make_float4(tf32_round(v.x - vt.x), tf32_round(v.y - vt.y), tf32_round(v.z - vt.z),
                                   tf32_round(v.w - vt.w));
-    const uint32_t o = sw128((uint32_t)S::N, (uint32_t)n, (uint32_t)c16);
-    *reinterpret_cast<float4*>(base + S::kOffBt + o) = vt;
-    *reinterpret_cast<float4*>(base + S::kOffBl + o) = vl;
+    *reinterpret_cast<float4*>(base + kTcOffB + sw128(2u * kTcN, (uint32_t)n, (uint32_t)c16)) = vt;
+    *reinterpret_cast<float4*>(base + kTcOffB + sw128(2u * kTcN, (uint32_t)(kTcN + n), (uint32_t)c16)) = vl;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    // distinct sequences in order of first token; this CTA's row tiles of
+    // each are rt = blockIdx.x, blockIdx.x + gridDim.x, ...
+    unsigned done = 0;
+    for (int v = 0; v < kTcTok; ++v)
+      if (s_seq[v] < 0) done |= 1u << v;
+    int nd = 0, pre = 0;
+    while (done != 0xffffffffu) {
+      const int first = __ffs(~done) - 1;
+      const int seq = s_seq[first];
+      unsigned mask = 0;
+      int nbmax = 0;
+      for (int v = 0; v < kTcTok; ++v)
+        if (s_seq[v] == seq) {
+          mask |= 1u << v;
+          nbmax = max(nbmax, s_nb[v]);
+        }
+      done |= mask;
+      const int tiles = (nbmax + 127) / 128;
+      s_dmask[nd] = mask;
+      s_dnb[nd] = nbmax;
+      s_doff[nd] = s_off[first];
+      s_dpre[nd] = pre;
+      pre += tiles > (int)blockIdx.x ? (tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+      ++nd;
+    }
+    s_dpre[nd] = pre;
+    s_nd = nd;
   }
   fence_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *reinterpret_cast<const uint32_t*>(base + S::kOffTmem);
+  const uint32_t tmem = *reinterpret_cast<const uint32_t*>(base + kTcOffTmem);
+  const int nd = s_nd;
+  const int n_items = s_dpre[nd];
+  // item k of this CTA: (distinct sequence, row tile)
+  auto item_at = [&](int k, int* d, int* rt) {
+    int x = 0;
+    while (x + 1 < nd && s_dpre[x + 1] <= k) ++x;
+    *d = x;
+    *rt = (int)blockIdx.x + (k - s_dpre[x]) * (int)gridDim.x;
+  };
 
   // ---- pooled rows are written by the preceding pool update / append
   grid_dep_wait();
   grid_dep_launch();
 
-  uint32_t phase = 0;
   bool timed_out = false;
-  const int row = tid >> 1, half = tid & 1;             // gather: half a row chunk per thread
-  constexpr int kMine = KC / 8;                         // 16-byte pieces per thread per chunk
-  const int erow = 32 * (warp & 3) + lane;              // epilogue: TMEM lane = row of the tile
-  const int ehalf = warp >> 2;                          // epilogue: tokens [ehalf * NT/2, +NT/2)
-  unsigned done = 0;
-  for (int v = 0; v < NT; ++v)
-    if (s_seq[v] < 0) done |= 1u << v;
-  const unsigned all = (1u << NT) - 1u;
-  while (done != all) {
-    const int first = __ffs(~done) - 1;
-    const int seq = s_seq[first];
-    unsigned mask = 0;
-    int nbmax = 0;
-    for (int v = 0; v < NT; ++v)
-      if (s_seq[v] == seq) {
-        mask |= 1u << v;
-        nbmax = max(nbmax, s_nb[v]);
-      }
-    done |= mask;
-    const int64_t off = s_off[first];
-    const int64_t tiles = ceil_div((int64_t)nbmax, 128);
-    for (int64_t rt = blockIdx.x; rt < tiles; rt += gridDim.x) {
-      const int64_t j0 = rt * 128;
-      if (tid < 128) {
-        int sl = -1;
-        if (j0 + tid < nbmax) {
-          sl = a.seq_blk_slots[off + j0 + tid];
-          if (sl < 0 || sl >= a.n_slots) {
-            atomicOr(err, kErrSlot);
-            sl = -1;
-          }
+  const int n_chunks = n_items * kTcChunks;
+  if (warp < 4) {
+    // ---- gather and split: thread p owns row p of every tile.  Chunk q is
+    // split as soon as its line lands and handed to the MMA; only then is
+    // the gather of chunk q + 2 issued into the stage chunk q - 1 used, so
+    // the MMAs of chunk q run while q + 1 is split and q + 2 is in flight.
+    const int p = tid;
+    auto row_slot = [&](int k) {
+      int d, rt;
+      item_at(k, &d, &rt);
+      const int64_t j = (int64_t)rt * 128 + p;
+      int sl = -1;
+      if (j < s_dnb[d]) {
+        sl = a.seq_blk_slots[s_doff[d] + j];
+        if (sl < 0 || sl >= a.n_slots) {
+          atomicOr(err, kErrSlot);
+          sl = -1;
         }
-        s_slot[tid] = sl;
       }
-      tc_fence_before();
-      __syncthreads();
+      return sl;
+    };
+    // the slot of row p in the item being gathered, and in the next one
+    // (loaded one item ahead, so the gather never waits on it)
+    int sl_cur = -1, sl_next = n_items > 0 ? row_slot(0) : -1;
+    auto gather = [&](int q) {
+      const int k = q / kTcChunks, c = q % kTcChunks, st = q % kTcStages, use = q / kTcStages;
+      if (!mbar_wait(bar_empty + 8 * st, (uint32_t)((use & 1) ^ 1))) timed_out = true;
+      if (c == 0) {
+        sl_cur = sl_next;
+        sl_next = k + 1 < n_items ? row_slot(k + 1) : -1;
+      }
+      const float* src = a.pooled + (int64_t)(sl_cur < 0 ? 0 : sl_cur) * kIdxDim + c * kTcKC;
+      const uint32_t dst = base_s + kTcOffA + (uint32_t)st * kTcStageBytes;
+#pragma unroll
+      for (int m = 0; m < kTcKC / 4; ++m) cp_async16(dst + sw128(128u, (uint32_t)p, (uint32_t)m), src + 4 * m, sl_cur >= 0);
+      asm volatile("cp.async.commit_group;\n" ::: "memory");
+    };
+    for (int q = 0; q < kTcStages - 1 && q < n_chunks; ++q) gather(q);
+    for (int q = 0; q < n_chunks; ++q) {
+      if (q + 1 < n_chunks) {
+        asm volatile("cp.async.wait_group 1;\n" ::: "memory");   // chunk q landed, q + 1 may be in flight
+      } else {
+        asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+      }
+      // this thread's line of chunk q: split it in place
+      const int st = q % kTcStages;
+      unsigned char* at = base + kTcOffA + (uint32_t)st * kTcStageBytes;
+#pragma unroll
+      for (int m = 0; m < kTcKC / 4; ++m) {
+        const uint32_t o = sw128(128u, (uint32_t)p, (uint32_t)m);
+        const float4 x = *reinterpret_cast<const float4*>(at + o);
+        const float4 xt = make_float4(tf32_trunc(x.x), tf32_trunc(x.y), tf32_trunc(x.z), tf32_trunc(x.w));
+        const float4 xl = make_float4(tf32_round(x.x - xt.x), tf32_round(x.y - xt.y), tf32_round(x.z - xt.z),
+                                      tf32_round(x.w - xt.w));
+        *reinterpret_cast<float4*>(at + o) = xt;
+        *reinterpret_cast<float4*>(at + kTcAHalf + o) = xl;
+      }
+      fence_async_smem();
+      mbar_arrive(bar_full + 8 * st);
+      if (q + kTcStages - 1 < n_chunks) gather(q + kTcStages - 1);
+    }
+  } else if (warp == 8) {
+    // ---- the MMAs, issued by one thread
+    if (lane == 0) {
+      for (int q = 0; q < n_chunks; ++q) {
+        const int k = q / kTcChunks, c = q % kTcChunks, st = q % kTcStages, use = q / kTcStages;
+        const int b = k & 1;
+        if (c == 0 && !mbar_wait(bar_acce + 8 * b, (uint32_t)(((k >> 1) & 1) ^ 1))) timed_out = true;
+        if (!mbar_wait(bar_full + 8 * st, (uint32_t)(use & 1))) timed_out = true;
+        tc_fence_after();
+        const uint32_t a_t = base_s + kTcOffA + (uint32_t)st * kTcStageBytes;
+        const uint32_t d = tmem + (uint32_t)b * 256u;
+#pragma unroll
+        for (int kk = 0; kk < kTcKC / 8; ++kk) {
+          const int kg = c * (kTcKC / 8) + kk;            // K step of 8 dims over the whole row
+          const uint64_t at = smem_desc(a_t + (uint32_t)kk * 32u, 16, 1024);
+          const uint64_t al = smem_desc(a_t + kTcAHalf + (uint32_t)kk * 32u, 16, 1024);
+          const uint64_t bd = smem_desc(base_s + kTcOffB + (uint32_t)(kg >> 2) * (2u * kTcN * 128u) +
+                                            (uint32_t)(kg & 3) * 32u, 16, 1024);
+          mma_tf32(d, at, bd, kTcIdesc256, (c | kk) ? 1u : 0u);   // t(A) [t(B); l(B)]
+          mma_tf32(d, al, bd, kTcIdesc128, 1u);                   // + l(A) t(B)
+        }
+        mma_commit(bar_empty + 8 * st);
+        if (c == kTcChunks - 1) mma_commit(bar_accf + 8 * b);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---- epilogue: thread e reads row e of the accumulator
+    const int e = tid - kTcGather;
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    for (int k = 0; k < n_items; ++k) {
+      int d, rt;
+      item_at(k, &d, &rt);
+      const int64_t j = (int64_t)rt * 128 + e;
+      const unsigned mask = s_dmask[d];
+      // the row's slot (its validity), loaded before the accumulator is ready
+      bool rok = false;
+      if (j < s_dnb[d]) {
+        const int sl = a.seq_blk_slots[s_doff[d] + j];
+        rok = sl >= 0 && sl < a.n_slots;
+      }
+      const int b = k & 1;
+      if (!mbar_wait(bar_accf + 8 * b, (uint32_t)((k >> 1) & 1))) timed_out = true;
       tc_fence_after();
-      const int sl = s_slot[row];
-      const float* src = a.pooled + (int64_t)(sl < 0 ? 0 : sl) * kIdxDim;
-      for (int c = 0; c < kIdxDim / KC; ++c) {
-        // raw rows, dims [c KC, c KC + KC), into t(A); zeros for rows without a slot
 #pragma unroll
-        for (int m = 0; m < kMine; ++m) {
-          const int q = half * kMine + m;
-          cp_async16(base_s + S::kOffAt + sw128(128u, (uint32_t)row, (uint32_t)q), src + c * KC + q * 4, sl >= 0);
-        }
-        asm volatile("cp.async.wait_all;\n" ::: "memory");
-        // split my pieces in place: t(A) truncated, l(A) rounded
-#pragma unroll
-        for (int m = 0; m < kMine; ++m) {
-          const int q = half * kMine + m;
-          const uint32_t o = sw128(128u, (uint32_t)row, (uint32_t)q);
-          const float4 x = *reinterpret_cast<const float4*>(base + S::kOffAt + o);
-          const float4 xt = make_float4(tf32_trunc(x.x), tf32_trunc(x.y), tf32_trunc(x.z), tf32_trunc(x.w));
-          const float4 xl = make_float4(tf32_round(x.x - xt.x), tf32_round(x.y - xt.y), tf32_round(x.z - xt.z),
-                                        tf32_round(x.w - xt.w));
-          *reinterpret_cast<float4*>(base + S::kOffAt + o) = xt;
-          *reinterpret_cast<float4*>(base + S::kOffAl + o) = xl;
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        if (tid == 0) {
-#pragma unroll
-          for (int kk = 0; kk < KC / 8; ++kk) {
-            const int kg = c * (KC / 8) + kk;     // K step of 8 dims over the whole row
-            const uint32_t ka = (uint32_t)(kk >> 2) * (128u * 128u) + (uint32_t)(kk & 3) * 32u;
-            const uint32_t kb = (uint32_t)(kg >> 2) * ((uint32_t)S::N * 128u) + (uint32_t)(kg & 3) * 32u;
-            const uint64_t at = smem_desc(base_s + S::kOffAt + ka, 16, 1024);
-            const uint64_t al = smem_desc(base_s + S::kOffAl + ka, 16, 1024);
-            const uint64_t bt = smem_desc(base_s + S::kOffBt + kb, 16, 1024);
-            const uint64_t bl = smem_desc(base_s + S::kOffBl + kb, 16, 1024);
-            mma_tf32(tmem, at, bt, S::kIdesc, kg > 0 ? 1u : 0u);
-            mma_tf32(tmem, at, bl, S::kIdesc, 1u);
-            mma_tf32(tmem, al, bt, S::kIdesc, 1u);
-          }
-          mma_commit(bar);
-        }
-        if (!mbar_wait(bar, phase)) timed_out = true;
-        phase ^= 1;
-        tc_fence_after();
-      }
-      // ---- epilogue: row erow, tokens of this warp's half
-      {
-        constexpr int kHalfCols = NT * 2;                 // NT/2 tokens x 4 heads
-        uint32_t r[kHalfCols];
-#pragma unroll
-        for (int g = 0; g < kHalfCols / 16; ++g)
-          tmem_ld16_nowait(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(ehalf * kHalfCols + 16 * g),
-                           r + 16 * g);
+      for (int gq = 0; gq < kTcN / 16; ++gq) {
+        uint32_t r0[16], r1[16];
+        tmem_ld16_nowait(tmem + lane_base + (uint32_t)b * 256u + (uint32_t)(16 * gq), r0);
+        tmem_ld16_nowait(tmem + lane_base + (uint32_t)b * 256u + 128u + (uint32_t)(16 * gq), r1);
         tmem_wait_ld();
-        const int64_t j = j0 + erow;
-        const bool rok = s_slot[erow] >= 0;
 #pragma unroll
-        for (int uu = 0; uu < NT / 2; ++uu) {
-          const int u = ehalf * (NT / 2) + uu;
+        for (int uu = 0; uu < 4; ++uu) {
+          const int u = gq * 4 + uu;
           if (((mask >> u) & 1u) && j < s_nb[u]) {
             float v[kIdxHeads];
 #pragma unroll
-            for (int h = 0; h < kIdxHeads; ++h) v[h] = s_w[u][h] * fmaxf(__uint_as_float(r[uu * 4 + h]), 0.f);
+            for (int h = 0; h < kIdxHeads; ++h)
+              v[h] = s_w[u][h] * fmaxf(__uint_as_float(r0[uu * 4 + h]) + __uint_as_float(r1[uu * 4 + h]), 0.f);
             scores[(int64_t)(t0 + u) * a.max_blocks + j] = rok ? (v[0] + v[1]) + (v[2] + v[3]) : -INFINITY;
           }
         }
       }
       tc_fence_before();
-      __syncthreads();   // TMEM read and slots used before the next tile
-      tc_fence_after();
+      mbar_arrive(bar_acce + 8 * b);
     }
   }
   if (!kTopk) {
     // -inf for the blocks of this CTA's row tiles a token does not see
+    __syncthreads();
     const int64_t all_tiles = ceil_div(a.max_blocks, 128);
     for (int64_t rt = blockIdx.x; rt < all_tiles; rt += gridDim.x)
-      for (int i = tid; i < NT * 128; i += 256) {
+      for (int i = tid; i < kTcTok * 128; i += kTcThreads) {
         const int v = i / 128;
         const int64_t j = rt * 128 + i % 128;
         const int t = t0 + v;
@@ -520,7 +610,7 @@ k_score_tc(const IndexArgs a, float* __restrict__ scores, unsigned* err) {
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 0) tmem_dealloc(tmem, S::kTmemCols);
+  if (warp == 0) tmem_dealloc(tmem, kTcTmemCols);
 }
 
 // ------------------------------------------------------------------ k_hist
@@ -1172,11 +1262,9 @@ cudaError_t index_setup(int* sms) {
     e = cudaFuncSetAttribute(k_select, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)(sizeof(int32_t) * (kSelSlots + 4 + kSelList)));
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k_score_tc<16, 32, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)TcShape<16, 32>::kSmem);
+    e = cudaFuncSetAttribute(k_score_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k_score_tc<16, 32, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)TcShape<16, 32>::kSmem);
+    e = cudaFuncSetAttribute(k_score_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
     if (e != cudaSuccess) return e;
     if (n <= 0) return cudaErrorInvalidDevice;
     sm_count[dev].store(n, std::memory_order_release);
@@ -1185,15 +1273,15 @@ cudaError_t index_setup(int* sms) {
   return cudaSuccess;
 }
 
-// Launches the token-tiled scores on the tensor cores: 16 tokens per CTA, 32
-// dims per gather, 2 CTAs per SM, the row tiles dealt to about 2 CTAs per SM.
+// Launches the token-tiled scores on the tensor cores: 32 tokens per CTA, one
+// CTA per SM, the row tiles of each token tile dealt to sms / token tiles CTAs.
 template <bool kTopk>
 cudaError_t launch_tiled(const IndexArgs& a, float* scores, unsigned* err, cudaStream_t stream, int sms) {
   const int64_t row_tiles = ceil_div(a.max_blocks, 128);
-  const int64_t tt = ceil_div(a.n_tokens, 16);
-  const int64_t x = std::min<int64_t>(row_tiles, std::max<int64_t>(1, 2 * (int64_t)sms / tt));
-  return launch_pdl(k_score_tc<16, 32, kTopk>, dim3((unsigned)std::max<int64_t>(x, 1), (unsigned)tt), dim3(256),
-                    TcShape<16, 32>::kSmem, stream, 1, a, scores, err);
+  const int64_t tt = ceil_div(a.n_tokens, kTcTok);
+  const int64_t x = std::min<int64_t>(row_tiles, std::max<int64_t>(1, (int64_t)sms / tt));
+  return launch_pdl(k_score_tc<kTopk>, dim3((unsigned)std::max<int64_t>(x, 1), (unsigned)tt), dim3(kTcThreads),
+                    kTcSmem, stream, 1, a, scores, err);
 }
 
 }  // namespace
