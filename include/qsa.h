@@ -374,7 +374,7 @@ qsa_status qsa_profile_kernel(int32_t kernel, void* before, void* after);
 
 /* Which kernels (bit k = kernel id k above) one qsa_index_topk call of
  * n_tokens tokens over n_seq sequences launches.  Scoring is token-tiled
- * (each pooled row read once per tile of 16 tokens of one sequence and
+ * (each pooled row read once per tile of 32 tokens of one sequence and
  * scored on the tensor cores, kernel 1, then kernel 2 builds the threshold
  * histogram) when n_tokens > 8 and n_tokens >= 2 * n_seq; otherwise one pass
  * per token builds the histogram as it scores.  qsa_index_scores follows the same

@@ -21,7 +21,7 @@
 //             the top 12 bits of the order-preserving score key.
 //   k_score_tc / k_hist  replace k_score when the call's tokens share
 //             sequences (a verify batch, a prefill ubatch): each pooled row
-//             is read once per tile of 16 tokens and scored on the
+//             is read once per tile of 32 tokens and scored on the
 //             tensor cores (split-TF32, fp32-accurate), then k_hist builds the
 //             histogram from the written scores.
 //   k_select  one thread-block cluster per token (8 CTAs for a few tokens,
