@@ -60,8 +60,8 @@ KERNEL_SOURCES = {
     "score": ("index.cu", "index_util.cuh", "tc_util.cuh", "qsa_internal.cuh"),
     "hist": ("index.cu", "index_util.cuh", "qsa_internal.cuh"),
     "select": ("index.cu", "index_util.cuh", "qsa_internal.cuh"),
-    "attn": ("attn.cu", "index_util.cuh", "tc_util.cuh", "qsa_internal.cuh"),
-    "select_attn": ("attn.cu", "index_util.cuh", "tc_util.cuh", "qsa_internal.cuh"),
+    "attn": ("attn.cu", "attn_util.cuh", "index_util.cuh", "tc_util.cuh", "qsa_internal.cuh"),
+    "select_attn": ("attn.cu", "attn_util.cuh", "index_util.cuh", "tc_util.cuh", "qsa_internal.cuh"),
 }
 FLUSH_BYTES = [1 << 30]   # L2 flush buffer (--flush-mb)
 FLUSH_READ_BYTES = 256 << 20   # read after the flush write (> the 129 MB L2)
@@ -76,6 +76,10 @@ DESCR = {
     "prefill": "prefill ubatch, 512 tokens appended to a 250,000-cell fp16 prompt, 128 dirty blocks",
     "verify5_250k_q8": "verify batch, 1 seq, 250,000-cell q8_0 K/V prompt + 5 consecutive query tokens/step, "
                        "same heads, top_k=2048",
+    "prefill_corr": "prefill ubatch as `prefill`, the tokens' indexer queries correlated (rho 0.98 with a shared "
+                    "component, shared indexer weights), so consecutive tokens choose overlapping blocks",
+    "verify5_250k_q8_corr": "verify batch as `verify5_250k_q8`, the tokens' indexer queries correlated (rho 0.98 "
+                            "with a shared component, shared indexer weights)",
 }
 
 
@@ -350,7 +354,7 @@ class _ExternalEvents:
             raise RuntimeError(f"cudaEventRecordWithFlags failed: {st}")
 
 
-def measure_config(name, K, W, dev, *, path="full", e2e=True, clocks=None, in_cluster=False):
+def measure_config(name, K, W, dev, *, path="full", e2e=True, clocks=None, in_cluster=False, union=False):
     """Time K decode steps of workload `name` on the device.  The K timed
     steps are captured as ONE CUDA graph: per step an L2 flush (write, then
     read; outside the step's events), a start event node, the step, an end event node.  Path
@@ -359,7 +363,9 @@ def measure_config(name, K, W, dev, *, path="full", e2e=True, clocks=None, in_cl
     blocks), qsa_index_topk, qsa_sparse_attn.  Path "calls": qsa_pool_update,
     qsa_index_topk, qsa_sparse_attn, the block table appended by a torch index
     write outside the step's events and the dirty list from the host.
-    The graph is replayed once; the step time is end - start of each step."""
+    The graph is replayed once; the step time is end - start of each step.
+    union (path "full"): token pairs attend over the union of their lists
+    (QSA_INDEX_ATTN_UNION)."""
     import torch
     from qsa_workload import make_workload
     from sparse_attention_long_qsa_gb300 import qsa
@@ -387,7 +393,7 @@ def measure_config(name, K, W, dev, *, path="full", e2e=True, clocks=None, in_cl
     # the attention clusters where its limits hold)
     if full:
         kernels = ["append"] + qsa.index_attn_kernels(L.cfg, toks[0], wl.n_seq, L.max_blocks,
-                                                      in_cluster=in_cluster)
+                                                      in_cluster=in_cluster, union=union)
     else:
         kernels = ["pool"] + qsa.index_topk_kernels(toks[0], wl.n_seq) + ["attn"]
     for a in alg:
@@ -399,7 +405,7 @@ def measure_config(name, K, W, dev, *, path="full", e2e=True, clocks=None, in_cl
             a.pop("hist")
         if "select_attn" in kernels:
             a["select_attn"] = a.pop("select") + a.pop("attn")
-    step_fn = (lambda **kw: L.full_step(**kw, in_cluster=in_cluster)) if full else L.step
+    step_fn = (lambda **kw: L.full_step(**kw, in_cluster=in_cluster, union=union)) if full else L.step
     xev = _ExternalEvents()
 
     def do_append(i):
@@ -646,11 +652,17 @@ def run_native(args, rank, world, local):
 
     secondary = {}
     if args.secondary and rank == 0:
-        for name in args.secondary.split(","):
-            if name in (args.config, args.target, "", "none"):
+        for item in args.secondary.split(","):
+            # "name" or "name:union" (the pairs' union attention)
+            name, _, mode = item.partition(":")
+            if item in (args.config, args.target, "", "none"):
                 continue
-            r2 = measure_config(name, min(args.steps, 128), args.warmup, dev, path=args.path, e2e=False)
-            secondary[name] = workload_line(r2, name, hbm, peak_src)
+            r2 = measure_config(name, min(args.steps, 128), args.warmup, dev, path=args.path, e2e=False,
+                                union=mode == "union")
+            secondary[item] = workload_line(r2, name, hbm, peak_src)
+            if mode == "union":
+                secondary[item]["roofline"].update(traffic=None,
+                                                   traffic_source="no ncu capture of the union attention")
             del r2
 
     cpu = None
@@ -700,7 +712,8 @@ def main():
     ap.add_argument("--target", default="250k_q8",
                     help="workload given a complete line of its own under `target` (rank 0; '' for none)")
     ap.add_argument("--secondary", default="250k_f16,5x250k_q8",
-                    help="comma list of further workloads timed on rank 0 ('none': no others)")
+                    help="comma list of further workloads timed on rank 0 ('none': no others); "
+                         "'name:union' times a workload with the token pairs' union attention")
     ap.add_argument("--path", default="full", choices=["full", "calls"],
                     help="full: append (with the pool update) + index + attention (the layer's whole step); "
                          "calls: the last three, the table appended outside the timed region")

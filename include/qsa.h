@@ -293,6 +293,27 @@ qsa_status qsa_sparse_attn(const qsa_config* cfg, int32_t n_tokens,
                            qsa_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * S5+S6 for token pairs  qsa_sparse_attn_union  (issue #28734, goodbadwolf's
+ * comment on the merged sparse path: the union kernel that multi-token
+ * batches run, tokens x heads over the union of their selected cells with a
+ * mask per token)
+ * Same arguments, layouts, outputs and errors as qsa_sparse_attn.  Tokens 2i
+ * and 2i + 1 (any two tokens; they share work only when their lists share
+ * cells, i.e. tokens of one sequence) are attended together: one cluster per
+ * (pair, KV head) builds the union of the two cell lists in shared memory
+ * (a cell on both lists is gathered once), the MMAs carry both tokens' 8 query
+ * heads in their 16 columns, and each column's softmax sees only its token's
+ * cells.  An odd last token is attended alone.  Each output equals
+ * qsa_sparse_attn's up to the rounding of the split merge (within 1e-6
+ * relative), for lists in which no cell repeats.  cells_pitch (top_k + r - 1)
+ * must be at most 4104, else QSA_ERR_UNSUPPORTED.  Needs no workspace. */
+qsa_status qsa_sparse_attn_union(const qsa_config* cfg, int32_t n_tokens,
+                                 const void* q, const void* k_cache, const void* v_cache,
+                                 int64_t n_cells, const int32_t* cells, const int32_t* count,
+                                 float* out, void* workspace, size_t ws_bytes,
+                                 qsa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * S2+S3+S4+S5+S6  qsa_index_attn  (issue #28734, fix summary, lever3, lever1
  * and sparse256: block-granular top-k, then attention over only the chosen
  * K/V set)
@@ -314,10 +335,15 @@ qsa_status qsa_sparse_attn(const qsa_config* cfg, int32_t n_tokens,
  * output equals the two calls' up to the rounding of the split merge.  On a
  * GB300 this mode is slower than flags = 0 (its one large kernel waits longer
  * for its instructions and for free SMs), so it is not the default.
+ * flags = QSA_INDEX_ATTN_UNION: the attention of qsa_sparse_attn_union (token
+ * pairs over the union of their lists) after the index kernels.
  * qsa_index_attn_kernels says which kernels a call runs.
  * Errors: as qsa_index_topk and qsa_sparse_attn (all pointers required);
- * QSA_ERR_INVALID_ARG for an unknown flag. */
+ * QSA_ERR_INVALID_ARG for an unknown flag or both flags;
+ * QSA_ERR_UNSUPPORTED for QSA_INDEX_ATTN_UNION where qsa_sparse_attn_union
+ * would return it. */
 #define QSA_INDEX_ATTN_IN_CLUSTER 1u
+#define QSA_INDEX_ATTN_UNION 2u
 qsa_status qsa_index_attn(const qsa_config* cfg, int32_t n_tokens, int32_t max_tokens,
                           const float* q_idx, const float* w_idx,
                           const int32_t* tok_seq, const int32_t* tok_pos,
@@ -332,7 +358,8 @@ qsa_status qsa_index_attn(const qsa_config* cfg, int32_t n_tokens, int32_t max_t
 /* Which kernels (bit k = kernel id k of qsa_profile_kernel) one
  * qsa_index_attn call with these flags launches on the current device: the
  * scores (1, plus 2 when token-tiled), then 3 and 4, or 6 (selection inside
- * the attention clusters).  0 for an invalid configuration or no tokens. */
+ * the attention clusters; with QSA_INDEX_ATTN_UNION kernel 4 is the union
+ * attention).  0 for an invalid configuration, flags or no tokens. */
 uint32_t qsa_index_attn_kernels(const qsa_config* cfg, int32_t n_tokens, int32_t n_seq, int64_t max_blocks,
                                 uint32_t flags);
 

@@ -21,7 +21,8 @@ from typing import List, Optional
 
 import numpy as np
 
-CONFIG_NAMES = ("tiny", "50k", "250k_q8", "250k_f16", "5x250k_q8", "prefill", "verify5_250k_q8")
+CONFIG_NAMES = ("tiny", "50k", "250k_q8", "250k_f16", "5x250k_q8", "prefill", "verify5_250k_q8",
+                "prefill_corr", "verify5_250k_q8_corr")
 
 
 def default_cfg(**over) -> dict:
@@ -192,6 +193,10 @@ PRESETS = {
     "prefill": (1, 250_000, 1, 512, "f16"),
     # speculative verify batch: 5 consecutive query tokens of one sequence per step
     "verify5_250k_q8": (1, 250_000, 128, 5, "q8_0"),
+    # the same two batches with the indexer queries of a sequence's tokens
+    # correlated (idx_corr below), so consecutive tokens choose overlapping blocks
+    "prefill_corr": (1, 250_000, 1, 512, "f16", 0.98),
+    "verify5_250k_q8_corr": (1, 250_000, 128, 5, "q8_0", 0.98),
 }
 
 
@@ -199,7 +204,8 @@ def make_workload(name: str = "custom", *, n_seq: Optional[int] = None,
                   prompt_len=None, n_steps: Optional[int] = None,
                   tokens_per_step: Optional[int] = None,
                   kv_type: Optional[str] = None, seed: int = 0,
-                  shuffled: bool = False, cfg: Optional[dict] = None) -> Workload:
+                  shuffled: bool = False, cfg: Optional[dict] = None,
+                  idx_corr: Optional[float] = None) -> Workload:
     """Build a workload.  Named presets: tiny, 50k, 250k_q8, 5x250k_q8, prefill, verify5_250k_q8.
 
     Decode (tokens_per_step == 1): every step appends one position to each
@@ -211,7 +217,13 @@ def make_workload(name: str = "custom", *, n_seq: Optional[int] = None,
     Cells: prompts occupy contiguous cell ranges (sequence-major), decode cells
     are appended interleaved across sequences; shuffled=True permutes all cells
     and all slots.  Slots: prompt blocks sequence-major, later blocks in order
-    of first appearance."""
+    of first appearance.
+
+    idx_corr = rho > 0: within a step, the tokens of one sequence share their
+    indexer weights w_idx (the sequence's first token's draw) and their
+    indexer queries are sqrt(1 - rho^2) z_t + rho z_seq with z_t, z_seq
+    N(0,1), drawn after the independent draws (rho = 0 leaves every array
+    as it was)."""
     if name in PRESETS:
         p = PRESETS[name]
         n_seq = p[0] if n_seq is None else n_seq
@@ -219,6 +231,10 @@ def make_workload(name: str = "custom", *, n_seq: Optional[int] = None,
         n_steps = p[2] if n_steps is None else n_steps
         tokens_per_step = p[3] if tokens_per_step is None else tokens_per_step
         kv_type = p[4] if kv_type is None else kv_type
+        if idx_corr is None and len(p) > 5:
+            idx_corr = p[5]
+    idx_corr = 0.0 if idx_corr is None else float(idx_corr)
+    assert 0.0 <= idx_corr < 1.0
     n_seq = 1 if n_seq is None else n_seq
     n_steps = 1 if n_steps is None else n_steps
     tokens_per_step = 1 if tokens_per_step is None else tokens_per_step
@@ -323,6 +339,12 @@ def make_workload(name: str = "custom", *, n_seq: Optional[int] = None,
         q = rng.standard_normal((T, Hq, D), dtype=np.float32).astype(np.float16)
         q_idx = rng.standard_normal((T, HI, DI), dtype=np.float32)
         w_idx = rng.random((T, HI), dtype=np.float32)
+        if idx_corr > 0.0:
+            z_seq = rng.standard_normal((n_seq, HI, DI), dtype=np.float32)
+            q_idx = (np.float32(np.sqrt(1.0 - idx_corr ** 2)) * q_idx +
+                     np.float32(idx_corr) * z_seq[tok_seq]).astype(np.float32)
+            first = np.searchsorted(tok_seq, tok_seq)   # tokens are ordered by sequence
+            w_idx = w_idx[first]
         dslots = sorted({int(seq_slots[s][int(p) // r]) for s in range(n_seq) for p in step_pos[i][s]})
         dirty = _pad_pow2(np.array(dslots, dtype=np.int32), 4)
         at = np.searchsorted(new_cells, step_cells[i])

@@ -180,10 +180,12 @@ size_t qsa_sparse_attn_workspace_size(const qsa_config* cfg, int32_t n_tokens) {
   return attn_workspace_bytes(n_tokens, cfg->n_q_heads, cfg->top_k + cfg->compress_ratio - 1);
 }
 
-qsa_status qsa_sparse_attn(const qsa_config* cfg, int32_t n_tokens, const void* q,
-                           const void* k_cache, const void* v_cache, int64_t n_cells,
-                           const int32_t* cells, const int32_t* count, float* out,
-                           void* workspace, size_t ws_bytes, qsa_stream_t stream) {
+namespace {
+
+// Checks of qsa_sparse_attn's arguments (shared by its union form); fills `a`.
+qsa_status attn_args(const qsa_config* cfg, int32_t n_tokens, const void* q, const void* k_cache,
+                     const void* v_cache, int64_t n_cells, const int32_t* cells, const int32_t* count, float* out,
+                     void* workspace, size_t ws_bytes, AttnArgs* a) {
   qsa_status st = check_cfg(cfg);
   if (st != QSA_OK) return st;
   if (n_tokens < 0 || n_cells < 0) return QSA_ERR_INVALID_ARG;
@@ -196,22 +198,49 @@ qsa_status qsa_sparse_attn(const qsa_config* cfg, int32_t n_tokens, const void* 
   const size_t need = qsa_sparse_attn_workspace_size(cfg, n_tokens);
   if (need > 0 && (workspace == nullptr || !aligned(workspace, 256) || ws_bytes < need))
     return QSA_ERR_WORKSPACE;
+  a->n_tokens = n_tokens;
+  a->n_kv_heads = cfg->n_kv_heads;
+  a->kv_q8 = cfg->kv_type == QSA_KV_Q8_0;
+  a->q = static_cast<const __half*>(q);
+  a->k_cache = k_cache;
+  a->v_cache = v_cache;
+  a->n_cells = n_cells;
+  a->cells = cells;
+  a->cells_pitch = cfg->top_k + cfg->compress_ratio - 1;
+  a->count = count;
+  a->out = out;
+  a->attn_scale = cfg->attn_scale;
+  return QSA_OK;
+}
+
+}  // namespace
+
+qsa_status qsa_sparse_attn(const qsa_config* cfg, int32_t n_tokens, const void* q,
+                           const void* k_cache, const void* v_cache, int64_t n_cells,
+                           const int32_t* cells, const int32_t* count, float* out,
+                           void* workspace, size_t ws_bytes, qsa_stream_t stream) {
   AttnArgs a{};
-  a.n_tokens = n_tokens;
-  a.n_kv_heads = cfg->n_kv_heads;
-  a.kv_q8 = cfg->kv_type == QSA_KV_Q8_0;
-  a.q = static_cast<const __half*>(q);
-  a.k_cache = k_cache;
-  a.v_cache = v_cache;
-  a.n_cells = n_cells;
-  a.cells = cells;
-  a.cells_pitch = cfg->top_k + cfg->compress_ratio - 1;
-  a.count = count;
-  a.out = out;
-  a.attn_scale = cfg->attn_scale;
+  const qsa_status st = attn_args(cfg, n_tokens, q, k_cache, v_cache, n_cells, cells, count, out, workspace,
+                                  ws_bytes, &a);
+  if (st != QSA_OK || n_tokens == 0) return st;
   unsigned* err = error_word();
   if (err == nullptr) return QSA_ERR_CUDA;
   return from_cuda(launch_sparse_attn(a, workspace, err, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+qsa_status qsa_sparse_attn_union(const qsa_config* cfg, int32_t n_tokens, const void* q,
+                                 const void* k_cache, const void* v_cache, int64_t n_cells,
+                                 const int32_t* cells, const int32_t* count, float* out,
+                                 void* workspace, size_t ws_bytes, qsa_stream_t stream) {
+  AttnArgs a{};
+  const qsa_status st = attn_args(cfg, n_tokens, q, k_cache, v_cache, n_cells, cells, count, out, workspace,
+                                  ws_bytes, &a);
+  if (st != QSA_OK) return st;
+  if (cfg->top_k + cfg->compress_ratio - 1 > union_attn_max_pitch()) return QSA_ERR_UNSUPPORTED;
+  if (n_tokens == 0) return QSA_OK;
+  unsigned* err = error_word();
+  if (err == nullptr) return QSA_ERR_CUDA;
+  return from_cuda(launch_sparse_attn_union(a, err, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 qsa_status qsa_index_attn(const qsa_config* cfg, int32_t n_tokens, int32_t max_tokens, const float* q_idx,
@@ -226,7 +255,10 @@ qsa_status qsa_index_attn(const qsa_config* cfg, int32_t n_tokens, int32_t max_t
   qsa_status st = fill_index_args(cfg, n_tokens, max_tokens, q_idx, w_idx, tok_seq, tok_pos, pooled, n_slots,
                                   seq_blk_off, seq_blk_slots, n_seq, max_blocks, &ia);
   if (st != QSA_OK) return st;
-  if (n_cells < 0 || (flags & ~(uint32_t)QSA_INDEX_ATTN_IN_CLUSTER) != 0u) return QSA_ERR_INVALID_ARG;
+  constexpr uint32_t kFlags = QSA_INDEX_ATTN_IN_CLUSTER | QSA_INDEX_ATTN_UNION;
+  if (n_cells < 0 || (flags & ~kFlags) != 0u || flags == kFlags) return QSA_ERR_INVALID_ARG;
+  const bool by_union = (flags & QSA_INDEX_ATTN_UNION) != 0u;
+  if (by_union && cfg->top_k + cfg->compress_ratio - 1 > union_attn_max_pitch()) return QSA_ERR_UNSUPPORTED;
   if (n_cells > kMaxI32) return QSA_ERR_UNSUPPORTED;
   if (n_tokens == 0) return QSA_OK;
   if (!blk_cells || !cells || !count || !q || !k_cache || !v_cache || !out) return QSA_ERR_INVALID_ARG;
@@ -256,14 +288,24 @@ qsa_status qsa_index_attn(const qsa_config* cfg, int32_t n_tokens, int32_t max_t
   a.attn_scale = cfg->attn_scale;
   unsigned* err = error_word();
   if (err == nullptr) return QSA_ERR_CUDA;
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (by_union) {
+    cudaError_t e = launch_index_topk(ia, cells, count, workspace, err, cs);
+    if (e == cudaSuccess) e = launch_sparse_attn_union(a, err, cs);
+    return from_cuda(e);
+  }
   bool fused = false;
   return from_cuda(launch_index_attn(ia, a, cells, count, workspace, (flags & QSA_INDEX_ATTN_IN_CLUSTER) != 0u,
-                                     err, reinterpret_cast<cudaStream_t>(stream), &fused));
+                                     err, cs, &fused));
 }
 
 uint32_t qsa_index_attn_kernels(const qsa_config* cfg, int32_t n_tokens, int32_t n_seq, int64_t max_blocks,
                                 uint32_t flags) {
   if (check_cfg(cfg) != QSA_OK || n_tokens <= 0) return 0u;
+  constexpr uint32_t kFlags = QSA_INDEX_ATTN_IN_CLUSTER | QSA_INDEX_ATTN_UNION;
+  if ((flags & ~kFlags) != 0u || flags == kFlags) return 0u;
+  if ((flags & QSA_INDEX_ATTN_UNION) != 0u && cfg->top_k + cfg->compress_ratio - 1 > qsa::union_attn_max_pitch())
+    return 0u;
   bool fused = false;
   if ((flags & QSA_INDEX_ATTN_IN_CLUSTER) != 0u && qsa::index_attn_plan(n_tokens, cfg->n_kv_heads, cfg->kv_type == QSA_KV_Q8_0,
                            cfg->top_k + cfg->compress_ratio - 1, max_blocks > 0 ? max_blocks : 1,

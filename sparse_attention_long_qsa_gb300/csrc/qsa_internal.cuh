@@ -290,6 +290,10 @@ struct AttnArgs {
 
 size_t attn_workspace_bytes(int n_tokens, int n_q_heads, int cells_pitch);
 cudaError_t launch_sparse_attn(const AttnArgs& a, void* ws, unsigned* err, cudaStream_t stream);
+// Attention of token pairs (2i, 2i + 1) over the union of their lists
+// (attn_union.cu); cells_pitch <= union_attn_max_pitch().
+cudaError_t launch_sparse_attn_union(const AttnArgs& a, unsigned* err, cudaStream_t stream);
+int union_attn_max_pitch();
 // qsa_index_attn: the qsa_index_topk kernels and the attention kernel, or
 // (in_cluster, when its limits hold: *fused = true) the score kernels and
 // then the selection and the attention in one cluster kernel.

@@ -84,20 +84,21 @@ class QSALayer:
                        recomputed, stream)
 
     def index_attn(self, tok_seq, tok_pos, q_idx, w_idx, q, recomputed=None, stream=None, in_cluster=False,
-                   out=None):
+                   out=None, union=False):
         """index_topk then sparse_attn in one call (qsa_index_attn); out:
         where the attention output goes (default the layer's buffer; may be a
-        pinned host tensor)."""
+        pinned host tensor); union: token pairs attend over the union of
+        their lists."""
         T = int(tok_pos.numel())
         qsa.index_attn(self.cfg, q_idx, w_idx, tok_seq, tok_pos, self.pooled, self.blk_cells,
                        self.seq_blk_off, self.seq_blk_slots, self.max_blocks, q, self.k_cache, self.v_cache,
                        self.n_cells, self.cells[:T], self.count[:T], self.out[:T] if out is None else out,
-                       self.ws_index, self.max_tokens, recomputed, stream, in_cluster=in_cluster)
+                       self.ws_index, self.max_tokens, recomputed, stream, in_cluster=in_cluster, union=union)
 
-    def sparse_attn(self, q, n_tokens: int, stream=None):
+    def sparse_attn(self, q, n_tokens: int, stream=None, union=False):
         T = int(n_tokens)
         qsa.sparse_attn(self.cfg, q, self.k_cache, self.v_cache, self.n_cells, self.cells[:T],
-                        self.count[:T], self.out[:T], self.ws_attn, stream)
+                        self.count[:T], self.out[:T], self.ws_attn, stream, union=union)
 
     def step(self, tok_seq, tok_pos, q, q_idx, w_idx, dirty, stream=None):
         """One QSA step for T tokens; returns the out[:T] view (fp32)."""
@@ -124,18 +125,19 @@ class QSALayer:
         return d
 
     def full_step(self, tok_seq, tok_pos, q, q_idx, w_idx, cells, k_new, v_new, idx_new, stream=None,
-                  in_cluster=False, out=None, **_):
+                  in_cluster=False, out=None, union=False, **_):
         """The whole layer step from the new tokens on: append of their cells
         (K/V, indexer keys, table, device dirty list) with the pool update of
         the blocks they dirty in the same launch, then index top-k and sparse
         attention in one qsa_index_attn call (in_cluster: the selection inside
-        the attention clusters).  The step's inputs and `out` may be pinned
+        the attention clusters; union: token pairs over the union of their
+        lists).  The step's inputs and `out` may be pinned
         host tensors.  Returns the output (fp32 [T][n_q_heads][head_dim])."""
         # the append re-pooled only the query tokens' own blocks: score work on
         # the other blocks may start before it finishes
         self.kv_append(tok_seq, tok_pos, cells, k_new, v_new, idx_new, stream, pool=True)
         self.index_attn(tok_seq, tok_pos, q_idx, w_idx, q, recomputed="query_blocks", stream=stream,
-                        in_cluster=in_cluster, out=out)
+                        in_cluster=in_cluster, out=out, union=union)
         return self.out[:int(tok_pos.numel())] if out is None else out
 
     def set_cells(self, slots, rows):

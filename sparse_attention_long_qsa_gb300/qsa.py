@@ -22,6 +22,7 @@ QSA_KV_F16 = 0
 QSA_KV_Q8_0 = 1
 QSA_HINT_QUERY_BLOCKS = -1
 QSA_INDEX_ATTN_IN_CLUSTER = 1
+QSA_INDEX_ATTN_UNION = 2
 STATUS = {0: "QSA_OK", -1: "QSA_ERR_INVALID_ARG", -2: "QSA_ERR_SHAPE", -3: "QSA_ERR_UNSUPPORTED",
           -4: "QSA_ERR_WORKSPACE", -5: "QSA_ERR_CUDA", -6: "QSA_ERR_DEVICE_BOUNDS"}
 
@@ -29,7 +30,7 @@ STATUS = {0: "QSA_OK", -1: "QSA_ERR_INVALID_ARG", -2: "QSA_ERR_SHAPE", -3: "QSA_
 EXPORTS = ("qsa_config_init", "qsa_cells_per_token", "qsa_pool_update", "qsa_index_scores",
            "qsa_index_topk_workspace_size", "qsa_index_topk", "qsa_index_topk_noalloc",
            "qsa_sparse_attn_workspace_size",
-           "qsa_sparse_attn", "qsa_index_attn", "qsa_index_attn_kernels", "qsa_kv_append", "qsa_blocks_dirty",
+           "qsa_sparse_attn", "qsa_sparse_attn_union", "qsa_index_attn", "qsa_index_attn_kernels", "qsa_kv_append", "qsa_blocks_dirty",
            "qsa_debug_check", "qsa_profile_kernel", "qsa_index_topk_kernels", "qsa_status_string")
 
 # Kernel ids of qsa_profile_kernel.
@@ -97,6 +98,8 @@ def _load():
     L.qsa_sparse_attn_workspace_size.restype = _SZ
     L.qsa_sparse_attn.argtypes = [CP, _I32, _P, _P, _P, _I64, _P, _P, _P, _P, _SZ, _P]
     L.qsa_sparse_attn.restype = _I32
+    L.qsa_sparse_attn_union.argtypes = [CP, _I32, _P, _P, _P, _I64, _P, _P, _P, _P, _SZ, _P]
+    L.qsa_sparse_attn_union.restype = _I32
     L.qsa_index_attn.argtypes = [CP, _I32, _I32, _P, _P, _P, _P, _P, _P, _I64, _P, _P, _I32, _I64,
                                  _P, _P, _P, _I64, _P, _P, _P, _P, _I32, ctypes.c_uint32, _P, _SZ, _P]
     L.qsa_index_attn.restype = _I32
@@ -249,11 +252,13 @@ def index_topk(cfg, q_idx, w_idx, tok_seq, tok_pos, pooled, blk_cells, seq_blk_o
 
 def index_attn(cfg, q_idx, w_idx, tok_seq, tok_pos, pooled, blk_cells, seq_blk_offs, seq_blk_slots,
                max_blocks: int, q, k_cache, v_cache, n_cells: int, cells, count, out, workspace,
-               max_tokens: int, recomputed=None, stream=None, in_cluster: bool = False):
+               max_tokens: int, recomputed=None, stream=None, in_cluster: bool = False,
+               union: bool = False):
     """qsa_index_topk then qsa_sparse_attn in one call (same workspace and
     hint as index_topk); fills cells, count and out.  in_cluster: the
     selection runs inside the attention clusters where the call's limits
-    allow (QSA_INDEX_ATTN_IN_CLUSTER)."""
+    allow (QSA_INDEX_ATTN_IN_CLUSTER); union: token pairs attend over the
+    union of their lists (QSA_INDEX_ATTN_UNION)."""
     import torch
     T = int(tok_pos.numel())
     if isinstance(recomputed, str) and recomputed == "query_blocks":
@@ -271,15 +276,20 @@ def index_attn(cfg, q_idx, w_idx, tok_seq, tok_pos, pooled, blk_cells, seq_blk_o
         int(max_blocks), _io(q, torch.float16, "q"), _ptr(k_cache, None, "k_cache"),
         _ptr(v_cache, None, "v_cache"), int(n_cells), _ptr(cells, torch.int32, "cells"),
         _ptr(count, torch.int32, "count"), _io(out, torch.float32, "out"), rec_ptr, rec_n,
-        QSA_INDEX_ATTN_IN_CLUSTER if in_cluster else 0,
+        _attn_flags(in_cluster, union),
         _ptr(workspace, torch.uint8, "workspace"), int(workspace.numel()), _stream(stream))
     _check(st, "qsa_index_attn")
 
 
-def index_attn_kernels(cfg, n_tokens: int, n_seq: int, max_blocks: int, in_cluster: bool = False) -> list:
+def _attn_flags(in_cluster: bool, union: bool) -> int:
+    return (QSA_INDEX_ATTN_IN_CLUSTER if in_cluster else 0) | (QSA_INDEX_ATTN_UNION if union else 0)
+
+
+def index_attn_kernels(cfg, n_tokens: int, n_seq: int, max_blocks: int, in_cluster: bool = False,
+                       union: bool = False) -> list:
     """Names of the kernels one index_attn call launches on the current device."""
     m = int(lib().qsa_index_attn_kernels(ctypes.byref(cfg), int(n_tokens), int(n_seq), int(max_blocks),
-                                         QSA_INDEX_ATTN_IN_CLUSTER if in_cluster else 0))
+                                         _attn_flags(in_cluster, union)))
     return [k for k, v in KERNELS.items() if (m >> v) & 1]
 
 
@@ -287,17 +297,21 @@ def sparse_attn_workspace_size(cfg, n_tokens: int) -> int:
     return int(lib().qsa_sparse_attn_workspace_size(ctypes.byref(cfg), int(n_tokens)))
 
 
-def sparse_attn(cfg, q, k_cache, v_cache, n_cells: int, cells, count, out, workspace=None, stream=None):
+def sparse_attn(cfg, q, k_cache, v_cache, n_cells: int, cells, count, out, workspace=None, stream=None,
+                union: bool = False):
+    """qsa_sparse_attn (union: qsa_sparse_attn_union, token pairs over the
+    union of their lists)."""
     import torch
     T = int(count.numel())
     ws_ptr = _ptr(workspace, torch.uint8, "workspace") if workspace is not None and workspace.numel() else None
     ws_len = int(workspace.numel()) if workspace is not None else 0
-    st = lib().qsa_sparse_attn(
+    name = "qsa_sparse_attn_union" if union else "qsa_sparse_attn"
+    st = getattr(lib(), name)(
         ctypes.byref(cfg), T, _io(q, torch.float16, "q"), _ptr(k_cache, None, "k_cache"),
         _ptr(v_cache, None, "v_cache"), int(n_cells), _ptr(cells, torch.int32, "cells"),
         _ptr(count, torch.int32, "count"), _io(out, torch.float32, "out"),
         ws_ptr, ws_len, _stream(stream))
-    _check(st, "qsa_sparse_attn")
+    _check(st, name)
 
 
 def kv_append(cfg, tok_seq, tok_pos, cells, k_new, v_new, idx_new, k_cache, v_cache, idx_k, blk_cells,

@@ -96,7 +96,8 @@ class Runner:
         """mode "calls": pool update, index top-k, attention (three calls);
         "index_attn": pool update, then index top-k and attention in one
         qsa_index_attn call; "in_cluster": the same with the selection inside
-        the attention clusters."""
+        the attention clusters; "union": the same with token pairs attended
+        over the union of their lists."""
         self.wl = wl
         self.mode = mode
         self.layer = QSALayer.from_workload(wl, 0)
@@ -113,10 +114,11 @@ class Runner:
             L.set_cells(slots, rows)
         st = wl.steps[i]
         inp = step_inputs(st)
-        if self.mode in ("index_attn", "in_cluster"):
+        if self.mode in ("index_attn", "in_cluster", "union"):
             L.pool_update(inp["dirty"])
             L.index_attn(inp["tok_seq"], inp["tok_pos"], inp["q_idx"], inp["w_idx"], inp["q"],
-                         recomputed=inp["dirty"], in_cluster=self.mode == "in_cluster")
+                         recomputed=inp["dirty"], in_cluster=self.mode == "in_cluster",
+                         union=self.mode == "union")
             out = L.out[:len(st.tok_pos)]
         else:
             out = L.step(**inp)

@@ -95,6 +95,27 @@ def test_null_and_workspace_checks(L):
     assert L.qsa_status_string(-4) == b"workspace null, misaligned or too small"
 
 
+def test_union_attention_host_checks(L):
+    """qsa_sparse_attn_union takes qsa_sparse_attn's checks, and refuses lists
+    longer than its shared-memory union holds (top_k 8192) before any launch;
+    qsa_index_attn refuses both attention flags at once."""
+    fake = ctypes.c_void_p(0x10000)
+    c = qsa.config()
+    bad = [ctypes.byref(c), 5, fake, ctypes.c_void_p(0x10002), fake, 1000, fake, fake, fake]
+    assert L.qsa_sparse_attn_union(*bad, None, 0, None) == -1
+    big = qsa.config(top_k=8192)
+    assert L.qsa_sparse_attn_union(ctypes.byref(big), 5, fake, fake, fake, 1000, fake, fake, fake,
+                                   None, 0, None) == -3
+    assert L.qsa_sparse_attn_union(ctypes.byref(big), 0, None, None, None, 0, None, None, None,
+                                   None, 0, None) == -3
+    need = L.qsa_index_topk_workspace_size(ctypes.byref(c), 5, 1000)
+    args = [ctypes.byref(c), 5, 5] + [fake] * 6 + [100, fake, fake, 1, 1000, fake, fake, fake, 1000,
+                                                   fake, fake, fake, None, 0]
+    assert L.qsa_index_attn(*args, 3, fake, need, None) == -1
+    assert L.qsa_index_attn(*args, 4, fake, need, None) == -1
+    assert L.qsa_index_attn_kernels(ctypes.byref(c), 5, 1, 1000, 3) == 0
+
+
 def test_blocks_dirty_host_helper(L):
     rng = np.random.default_rng(0)
     old = rng.integers(-1, 1000, (300, 4)).astype(np.int32)
