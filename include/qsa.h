@@ -303,9 +303,11 @@ qsa_status qsa_sparse_attn(const qsa_config* cfg, int32_t n_tokens,
  * (pair, KV head) builds the union of the two cell lists in shared memory
  * (a cell on both lists is gathered once), the MMAs carry both tokens' 8 query
  * heads in their 16 columns, and each column's softmax sees only its token's
- * cells.  An odd last token is attended alone.  Each output equals
- * qsa_sparse_attn's up to the rounding of the split merge (within 1e-6
- * relative), for lists in which no cell repeats.  cells_pitch (top_k + r - 1)
+ * cells.  An odd last token is attended alone.  Each output is the same
+ * attention as qsa_sparse_attn's, for lists in which no cell repeats; the
+ * tiles hold other cells, so the fp16 rounding of the probabilities and the
+ * order of the sums differ (both within 2e-3 max-relative of the exact
+ * result for fp16 K/V, 5e-3 for q8_0).  cells_pitch (top_k + r - 1)
  * must be at most 4104, else QSA_ERR_UNSUPPORTED.  Needs no workspace. */
 qsa_status qsa_sparse_attn_union(const qsa_config* cfg, int32_t n_tokens,
                                  const void* q, const void* k_cache, const void* v_cache,

@@ -30,11 +30,12 @@
 // o) per head in registers.  The partials of the 16 (token, head) columns are
 // merged over the cluster through distributed shared memory.
 //
-// Each token's output equals the per-token kernel's over the same list up to
-// the rounding of the split merge, provided no cell repeats within a token's
-// list (a repeated cell is attended once per occurrence by the per-token
-// kernel; here token 1's occurrences of a cell that token 0 also lists
-// collapse into one).  Waits on the MMA completion barrier are bounded.
+// Each token gets the attention the per-token kernel computes over its list,
+// provided no cell repeats within a token's list (a repeated cell is attended
+// once per occurrence by the per-token kernel; here token 1's occurrences of
+// a cell that token 0 also lists collapse into one); the tiles hold other
+// cells, so the fp16 rounding of P and the order of the sums differ.  Waits
+// on the MMA completion barrier are bounded.
 #include <atomic>
 #include <mutex>
 
