@@ -105,8 +105,13 @@ def ncu_traffic(workload: str, kernel: str):
                         f"({e['capture']}; sources {e['source']})")
 
 
-L2_NOTE = ("GPU arm: L2 flushed before every step (a 1 GiB write, then a 256 MiB read of its head so that "
-           "no dirty line is left), outside the step's events")
+L2_NOTE = ("GPU arm, headline and e2e: the timed layer-steps run back to back over copies of the layer's "
+           "state (each one more layer of the model: its own caches, keys, block table and pooled keys), "
+           "enough that the other copies' steps move more than 3x the 129 MB L2 between two steps of one "
+           "copy (inputs larger than L2, no flush); per-kernel times: L2 flushed before every step (a 1 GiB "
+           "write, then a 256 MiB read of its head), outside the step's events")
+L2_BYTES = 129 * 10 ** 6
+CHAIN_MEM_BYTES = 48 << 30   # device memory the layer copies may take
 
 
 def bench_config(name: str, tokens_per_step: int) -> dict:
@@ -548,6 +553,121 @@ def measure_config(name, K, W, dev, *, path="full", e2e=True, clocks=None, in_cl
     return res
 
 
+def clone_layer(L):
+    """Another layer of the same model: a copy of the layer's state (caches,
+    indexer keys, block table, pooled keys, outputs, workspaces); the
+    sequences' block lists and the norm weight are shared."""
+    import copy
+    C = copy.copy(L)
+    for k in ("idx_k", "k_cache", "v_cache", "blk_cells", "pooled", "cells", "count", "out", "ws_index",
+              "ws_attn"):
+        setattr(C, k, getattr(L, k).clone())
+    C._dirty = None
+    return C
+
+
+def measure_chain(name, K, W, dev, *, e2e=True, clocks=None, union=False):
+    """Headline timing of the whole layer step (qsa_kv_append re-pooling the
+    blocks it dirties, then qsa_index_attn): K layer-steps back to back in
+    one CUDA graph, events only at its two ends, replayed once.  Layer-step n
+    is token (n // n_layers) of the workload on layer copy n % n_layers, the
+    copies being enough that the other copies' steps move more than 3x the L2
+    between two steps of one copy (so no flush is needed and none is timed).
+    A 4-byte fill between layer-steps ends the launch overlap: each step's
+    first kernel starts after the previous step's last one has completed, as
+    after the other ops of a model.  With e2e, each step's inputs are read in
+    place from pinned host memory and its output is stored there."""
+    import torch
+    from qsa_workload import make_workload
+    from sparse_attention_long_qsa_gb300.layer import PackedInputs, QSALayer, step_inputs
+
+    wl = make_workload(name, seed=0)
+    n_tok = len(wl.steps)
+    L0 = QSALayer.from_workload(wl, 0, device=dev)
+    L0.warm(torch.from_numpy(wl.prompt_dirty()).to(dev))
+    step_bytes = float(np.mean([sum(algorithmic_bytes(wl, i).values()) for i in range(n_tok)]))
+    state_bytes = sum(getattr(L0, k).numel() * getattr(L0, k).element_size()
+                      for k in ("idx_k", "k_cache", "v_cache", "blk_cells", "pooled", "cells", "count", "out",
+                                "ws_index", "ws_attn"))
+    n_layers = max(2, int(np.ceil(3 * L2_BYTES / step_bytes)) + 1)
+    n_layers = max(2, min(n_layers, 64, int(CHAIN_MEM_BYTES // max(state_bytes, 1))))
+    layers = [L0] + [clone_layer(L0) for _ in range(n_layers - 1)]
+    inputs = [step_inputs(st, device=dev, new_cells=True) for st in wl.steps]
+    toks = [len(st.tok_pos) for st in wl.steps]
+    sep = torch.zeros(1, dtype=torch.int32, device=dev)
+    xev = _ExternalEvents()
+    io_keys = ("tok_seq", "tok_pos", "q", "q_idx", "w_idx", "cells", "k_new", "v_new", "idx_new")
+    host = None
+    if e2e:
+        staging = PackedInputs({k: (tuple(inputs[0][k].shape), inputs[0][k].dtype) for k in io_keys}, device=dev)
+        host = []
+        for i, st in enumerate(wl.steps):
+            h = {"in": staging.pack({k: getattr(st, k) for k in io_keys})}
+            h["views"] = staging.host_views(h["in"])
+            h["out"] = torch.empty((toks[i], wl.cfg["n_q_heads"], wl.cfg["head_dim"]),
+                                   dtype=torch.float32).pin_memory()
+            host.append(h)
+
+    def step(n, with_io=False):
+        i, l = (n // n_layers) % n_tok, n % n_layers
+        if with_io:
+            layers[l].full_step(**{**inputs[i], **host[i]["views"]}, out=host[i]["out"], union=union)
+        else:
+            layers[l].full_step(**inputs[i], union=union)
+        sep.zero_()
+        return toks[i]
+
+    for n in range(W):
+        step(n)
+    torch.cuda.synchronize()
+
+    def timed(with_io):
+        """Median over replays of the K-step graph (one replay, then ~1 s of
+        replays with the clocks sampled, or 3 with host I/O)."""
+        e0, e1 = xev.new(), xev.new()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        tokens = 0
+        with torch.cuda.graph(g):
+            xev.record(e0)
+            for n in range(W, W + K):
+                tokens += step(n, with_io)
+            xev.record(e1)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        reps = [e0.elapsed_time(e1)]
+        n_rep = 2 if with_io else min(200, max(3, int(np.ceil(1000.0 / max(reps[0], 1e-3)))))
+        if clocks and not with_io:
+            clocks.start()
+        for _ in range(n_rep):
+            g.replay()
+            torch.cuda.synchronize()
+            reps.append(e0.elapsed_time(e1))
+        ck = clocks.stop() if clocks and not with_io else None
+        del g
+        return float(np.median(reps)), tokens, ck, len(reps)
+
+    ms, tokens, ck, n_rep = timed(False)
+    res = dict(value=tokens / (ms / 1e3), ms_per_step=ms / K, tokens=tokens, n_layers=n_layers,
+               state_bytes=state_bytes, step_bytes=step_bytes, clocks=ck, replays=n_rep)
+    if e2e:
+        ms2, tokens2, _, _ = timed(True)
+        h2d = float(sum(n for (_, _, _, n) in staging.fields.values()))
+        d2h = float(np.mean([host[i]["out"].numel() * 4 for i in range(n_tok)]))
+        res["e2e"] = {"value": tokens2 / (ms2 / 1e3), "unit": "tokens/s",
+                      "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                      "how": "the same back-to-back layer-steps with each step's inputs in pinned host memory, "
+                             "read in place by the kernels over NVLink-C2C, and its output stored by the "
+                             "attention kernel into pinned host memory"}
+    st, flags = __import__("sparse_attention_long_qsa_gb300.qsa", fromlist=["qsa"]).debug_check()
+    if st != 0:
+        raise RuntimeError(f"device error word set during the bench: {flags:#x}")
+    del layers, L0, inputs
+    torch.cuda.empty_cache()
+    return res
+
+
 def replica_value(local_ms: float, tokens: int, world: int, dist=None, device="cpu"):
     """Whole-job tokens/s of `world` replicas that each processed `tokens` in
     their own `local_ms`: all replicas' tokens over the slowest replica's
@@ -560,13 +680,18 @@ def replica_value(local_ms: float, tokens: int, world: int, dist=None, device="c
     return world * tokens / (local_ms / 1e3), local_ms
 
 
-def launch_note(res, path):
+def launch_note(res, path, ch=None):
+    kern = f"{res['launches_per_step']} kernels ({', '.join(res['kernels'])}) chained by programmatic dependent launch"
+    if ch is not None:
+        return ("the K timed layer-steps captured back to back as one CUDA graph with an event node at each "
+                "end: per layer-step qsa_kv_append (re-pooling the blocks it dirties) + "
+                f"qsa_index_attn = {kern}, then a 4-byte fill that ends the launch overlap; {chain_note(ch)} "
+                "(gpu_launches counts one replay)")
     return ("the K timed steps captured as one CUDA graph (per step: L2 flush, start event, "
             + ("qsa_kv_append (re-pooling the blocks it dirties) + qsa_index_attn"
                if path == "full" else
                "table append outside the events, qsa_pool_update + qsa_index_topk + qsa_sparse_attn")
-            + f" = {res['launches_per_step']} kernels ({', '.join(res['kernels'])})"
-            + " chained by programmatic dependent launch, end event), replayed once")
+            + f" = {kern}, end event), replayed once")
 
 
 def roofline_of(res, name, hbm, peak_src):
@@ -582,19 +707,41 @@ def roofline_of(res, name, hbm, peak_src):
             "traffic": traffic, "traffic_source": tsrc}
 
 
-def workload_line(res, name, hbm, peak_src, cpu=None):
-    """Per-workload results: throughput, end to end, roofline, kernel times."""
-    return {
-        "workload": DESCR[name], "value": res["value"], "unit": "tokens/s",
-        "ms_per_step": res["ms_per_step"],
-        "step_us_p50": res["step_us_p50"], "step_us_p90": res["step_us_p90"],
-        "e2e": res.get("e2e"), "cpu_baseline": cpu,
+def event_line(res):
+    """The event-bracketed timing of measure_config (each step between its own
+    event nodes after an L2 flush)."""
+    return {"value": res["value"], "ms_per_step": res["ms_per_step"], "step_us_p50": res["step_us_p50"],
+            "step_us_p90": res["step_us_p90"],
+            "how": "each step between two event nodes of the graph, the L2 flushed before it (the event nodes "
+                   "and the first launch after them add ~6 us per step)"}
+
+
+def chain_note(ch):
+    return (f"{ch['n_layers']} layer copies of {ch['state_bytes'] / 1e6:.0f} MB, "
+            f"{ch['step_bytes'] / 1e6:.1f} MB of algorithmic bytes per layer-step; median of "
+            f"{ch['replays']} replays of the K-step graph")
+
+
+def workload_line(res, name, hbm, peak_src, cpu=None, chain=None):
+    """Per-workload results: throughput (back-to-back layer-steps when `chain`
+    is given, else event-bracketed), end to end, roofline, kernel times."""
+    top = chain if chain is not None else res
+    line = {
+        "workload": DESCR[name], "value": top["value"], "unit": "tokens/s",
+        "ms_per_step": top["ms_per_step"],
+        "e2e": top.get("e2e"), "cpu_baseline": cpu,
         "roofline": roofline_of(res, name, hbm, peak_src),
         "kernels_us": {k: round(v, 3) for k, v in res["kern_us"].items()},
         "kernels_gbs": {k: round(v, 1) for k, v in res["kern_gbs"].items()},
         "step_bytes": res["step_bytes"],
-        "step_gbs": res["step_bytes"] / (res["ms_per_step"] * 1e-3) / 1e9,
+        "step_gbs": res["step_bytes"] / (top["ms_per_step"] * 1e-3) / 1e9,
     }
+    if chain is not None:
+        line["chain"] = chain_note(chain)
+        line["event_bracketed"] = event_line(res)
+    else:
+        line["step_us_p50"], line["step_us_p90"] = res["step_us_p50"], res["step_us_p90"]
+    return line
 
 
 def cpu_line(wl, name, seconds):
@@ -622,31 +769,47 @@ def run_native(args, rank, world, local):
     peak_src = "of measured" if peaks else "of fallback"
 
     clocks = Clocks(local)
+    chained = args.path == "full"
+    # per-kernel breakdown, roofline kernel and event-bracketed steps (rank 0
+    # only when chained: the headline comes from the chain)
+    res = None
+    if rank == 0 or not chained:
+        res = measure_config(args.config, args.steps, args.warmup, dev, path=args.path,
+                             clocks=None if chained else clocks, e2e=not chained)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    res = measure_config(args.config, args.steps, args.warmup, dev, path=args.path, clocks=clocks)
+    ch = measure_chain(args.config, args.steps, args.warmup, dev, clocks=clocks) if chained else None
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    value, max_ms = replica_value(res["ms_per_step"] * args.steps, res["tokens"], world, dist, dev)
+    top = ch if chained else res
+    value, max_ms = replica_value(top["ms_per_step"] * args.steps, top["tokens"], world, dist, dev)
 
-    other = "calls" if args.path == "full" else "full"
-    paths = {args.path: {"value": res["value"], "ms_per_step": res["ms_per_step"],
-                         "launches_per_step": res["launches_per_step"]}}
+    paths = None
+    if rank == 0:
+        paths = {args.path: {"value": top["value"], "ms_per_step": top["ms_per_step"],
+                             "launches_per_step": res["launches_per_step"],
+                             "timing": "back-to-back layer-steps" if chained else "event-bracketed"}}
+        if chained:
+            paths[args.path]["event_bracketed"] = {"value": res["value"], "ms_per_step": res["ms_per_step"]}
     if rank == 0 and args.compare:
+        other = "calls" if args.path == "full" else "full"
         ro = measure_config(args.config, args.steps, args.warmup, dev, path=other, e2e=False)
         paths[other] = {"value": ro["value"], "ms_per_step": ro["ms_per_step"],
                         "launches_per_step": ro["launches_per_step"],
+                        "timing": "event-bracketed",
                         "kernels_us": {k: round(v, 3) for k, v in ro["kern_us"].items()}}
 
     # the 250k q8_0 decode (the long-context target) on a complete line of its
     # own: end to end, CPU baseline, roofline
     target = None
     if args.target not in ("", "none", args.config) and rank == 0:
-        rt = measure_config(args.target, min(args.steps, 256), args.warmup, dev, path=args.path)
+        rt = measure_config(args.target, min(args.steps, 256), args.warmup, dev, path=args.path,
+                            e2e=not chained)
+        ct = measure_chain(args.target, min(args.steps, 256), args.warmup, dev) if chained else None
         cpu_t = None if args.no_cpu else cpu_line(rt["wl"], args.target, args.cpu_seconds)
-        target = workload_line(rt, args.target, hbm, peak_src, cpu_t)
+        target = workload_line(rt, args.target, hbm, peak_src, cpu_t, chain=ct)
         target["config"] = bench_config(args.target, len(rt["wl"].steps[0].tok_pos))
         del rt
 
@@ -659,7 +822,9 @@ def run_native(args, rank, world, local):
                 continue
             r2 = measure_config(name, min(args.steps, 128), args.warmup, dev, path=args.path, e2e=False,
                                 union=mode == "union")
-            secondary[item] = workload_line(r2, name, hbm, peak_src)
+            c2 = (measure_chain(name, min(args.steps, 128), args.warmup, dev, e2e=False, union=mode == "union")
+                  if chained else None)
+            secondary[item] = workload_line(r2, name, hbm, peak_src, chain=c2)
             if mode == "union":
                 secondary[item]["roofline"].update(traffic=None,
                                                    traffic_source="no ncu capture of the union attention")
@@ -673,7 +838,7 @@ def run_native(args, rank, world, local):
             dist.destroy_process_group()
         return
     wl = res["wl"]
-    main_line = workload_line(res, args.config, hbm, peak_src, cpu)
+    main_line = workload_line(res, args.config, hbm, peak_src, cpu, chain=ch)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_ms / args.steps,
@@ -681,22 +846,26 @@ def run_native(args, rank, world, local):
         "dtype": "f16" if wl.cfg["kv_type"] == "f16" else "q8_0",
         "data": "synthetic (seeded N(0,1) K/V/keys, U(0,1) weights)",
         "config": bench_config(args.config, len(wl.steps[0].tok_pos)),
-        "launch": {"path": args.path, "steps": launch_note(res, args.path),
+        "launch": {"path": args.path, "steps": launch_note(res, args.path, ch),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": main_line["roofline"],
-        "step_us_p50": res["step_us_p50"], "step_us_p90": res["step_us_p90"],
         "kernels_us": main_line["kernels_us"],
         "kernels_gbs": main_line["kernels_gbs"],
         "step_bytes": res["step_bytes"],
         "step_gbs": main_line["step_gbs"],
         "cpu_baseline": cpu,
-        "e2e": res.get("e2e"),
+        "e2e": top.get("e2e"),
         "gpu_launches": res["launches_per_step"] * args.steps,
         "paths": paths,
-        "clocks": res["clocks"],
+        "clocks": top["clocks"],
         "target": target,
         "secondary": secondary or None,
     }
+    if chained:
+        line["chain"] = main_line["chain"]
+        line["event_bracketed"] = main_line["event_bracketed"]
+    else:
+        line["step_us_p50"], line["step_us_p90"] = res["step_us_p50"], res["step_us_p90"]
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
