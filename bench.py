@@ -47,12 +47,13 @@ METRIC = "QSA-layer decode tokens/s at 50k/250k ctx (1 and 5 seqs); HBM GB/s vs 
 # sources whose hash is stored beside it.  The line reports the number only
 # while the kernel's sources still hash to that value (null otherwise, and for
 # a workload or kernel without an entry).
-NCU_CMD_250K = ("ncu --set full --clock-control none -k regex:<kernel> -s 6 -c 1 python bench.py --config 250k_q8 "
-                "--steps 8 --warmup 3 --secondary none --target none --no-cpu --no-compare --flush-mb 256")
+NCU_CMD = ("ncu --set full --clock-control none -k regex:<kernel> -s 6 -c 1 python bench.py --config {cfg} "
+           "--path calls --steps 8 --warmup 3 --secondary none --target none --no-cpu --no-compare --flush-mb 256")
 NCU_TRAFFIC = {
-    ("250k_q8", "score"): {"bytes": 33_289_984, "source": "0e8e020ab527cc7f", "capture": NCU_CMD_250K},
-    ("250k_q8", "select"): {"bytes": 647_168, "source": "12a017b968c7226f", "capture": NCU_CMD_250K},
-    ("250k_q8", "attn"): {"bytes": 2_314_240, "source": "1338b592cb9ad74a", "capture": NCU_CMD_250K},
+    ("250k_q8", "score"): {"bytes": 33_290_240, "source": "967c8d48cd66bd64", "capture": NCU_CMD.format(cfg="250k_q8")},
+    ("250k_q8", "select"): {"bytes": 646_144, "source": "f478f462fa5df093", "capture": NCU_CMD.format(cfg="250k_q8")},
+    ("250k_q8", "attn"): {"bytes": 2_314_240, "source": "294f516b769e2876", "capture": NCU_CMD.format(cfg="250k_q8")},
+    ("50k", "attn"): {"bytes": 4_279_040, "source": "294f516b769e2876", "capture": NCU_CMD.format(cfg="50k")},
 }
 KERNEL_SOURCES = {
     "append": ("append.cu", "pool_row.cuh", "qsa_internal.cuh"),
@@ -775,11 +776,11 @@ def run_native(args, rank, world, local):
     res = None
     if rank == 0 or not chained:
         res = measure_config(args.config, args.steps, args.warmup, dev, path=args.path,
-                             clocks=None if chained else clocks, e2e=not chained)
+                             clocks=None if chained else clocks, e2e=not chained, union=args.union)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    ch = measure_chain(args.config, args.steps, args.warmup, dev, clocks=clocks) if chained else None
+    ch = measure_chain(args.config, args.steps, args.warmup, dev, clocks=clocks, union=args.union) if chained else None
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
@@ -886,6 +887,8 @@ def main():
     ap.add_argument("--path", default="full", choices=["full", "calls"],
                     help="full: append (with the pool update) + index + attention (the layer's whole step); "
                          "calls: the last three, the table appended outside the timed region")
+    ap.add_argument("--union", action="store_true",
+                    help="path full: token pairs attend over the union of their lists (QSA_INDEX_ATTN_UNION)")
     ap.add_argument("--no-compare", dest="compare", action="store_false",
                     help="do not also time the other path")
     ap.add_argument("--no-cpu", action="store_true")
