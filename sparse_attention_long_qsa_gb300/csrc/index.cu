@@ -24,8 +24,8 @@
 //             is read once per tile of 32 tokens and scored on the
 //             tensor cores (split-TF32, fp32-accurate), then k_hist builds the
 //             histogram from the written scores.
-//   k_select  one thread-block cluster per token (8 CTAs for a few tokens,
-//             down to 1 for many: select_cluster).  Every CTA reads the
+//   k_select  one thread-block cluster per token (16 CTAs for one to four
+//             tokens, 8 for a few more, down to 1 for many: select_cluster).  Every CTA reads the
 //             histogram and finds the bin holding the B-th largest score.
 //             Each CTA then takes a range of blocks: blocks above that bin go
 //             straight into its shared selection bitmap (warp ballots), blocks
@@ -67,7 +67,7 @@ constexpr int kMaxHint = 32;              // recomputed-slot hints checked per C
 
 constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
-constexpr int kSelCluster = 8;
+constexpr int kSelCluster = 16;
 constexpr int kSelMaxWords = 4096;        // bitmap words per CTA: 131072 blocks
 constexpr int kSelLocalCand = 2048;       // candidate keys held per CTA
 constexpr int kSelBatch = 16;             // score words a warp loads before using any
@@ -1219,12 +1219,18 @@ int score_chunk(int T, int64_t max_blocks, int sms) {
 // CTAs per selection cluster.  One k_select CTA fills an SM (512 threads,
 // ~118 KB of shared memory).  A CTA costs about 5 us of its own (histogram,
 // barriers, ordering, expansion) plus ~3 us per 62,500 blocks it classifies,
-// so few tokens take 8-CTA clusters (one wave either way) and many tokens
+// so few tokens take large clusters (one wave either way) and many tokens
 // take small clusters (fewer waves); a CTA holds at most kSelMaxWords words.
+// 16-CTA clusters are taken only while the call's selection CTAs leave half
+// of the SMs free: the attention CTAs launched behind the selection (one per
+// SM) then become resident while it runs (measured: a 1-token step 0.3 us
+// faster at 50k and 0.7 us at 250k than with 8-CTA clusters, a 5-token step
+// 1 us slower).
 int select_cluster(int T, int64_t max_blocks, int sms) {
-  int best_nc = kSelCluster;
+  int best_nc = 8;
   double best = -1.0;
   for (int nc = kSelCluster; nc >= 1; nc >>= 1) {
+    if (nc > 8 && (int64_t)T * nc > (int64_t)sms / 2) continue;
     if (ceil_div(max_blocks, (int64_t)nc) > (int64_t)kSelMaxWords * 32) break;
     const double waves = (double)ceil_div((int64_t)T * nc, (int64_t)(sms > 0 ? sms : 1));
     const double cost = waves * (5.0 + 3.0 * (double)max_blocks / 62500.0 / nc);
@@ -1262,6 +1268,8 @@ cudaError_t index_setup(int* sms) {
     e = cudaFuncSetAttribute(k_select, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)(sizeof(int32_t) * (kSelSlots + 4 + kSelList)));
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_select, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(k_score_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(k_score_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
@@ -1291,7 +1299,8 @@ cudaError_t launch_tiled(const IndexArgs& a, float* scores, unsigned* err, cudaS
 // serves the repeats.
 bool index_tiled(int n_tokens, int n_seq) { return n_tokens > 8 && n_tokens >= 2 * n_seq; }
 
-int64_t index_max_blocks_limit() { return (int64_t)kSelCluster * kSelMaxWords * 32; }
+// what an 8-CTA cluster holds (16-CTA clusters serve only calls of few tokens)
+int64_t index_max_blocks_limit() { return (int64_t)8 * kSelMaxWords * 32; }
 
 size_t index_workspace_bytes(int max_tokens, int64_t max_blocks) {
   static_assert(kCtrlBytes == (size_t)kIndexCtrlBytes, "workspace layout");
