@@ -305,44 +305,48 @@ k_score(const IndexArgs a, void* ws, float* __restrict__ scores, int chunk, unsi
 // omitted l(A) l(B) and the rounding of l(.) are below 2^-21 of each product,
 // under the rounding of an fp32 FMA chain over 128 terms.
 //
-// The split query tile is stored as one 256-row operand [t(B); l(B)], so one
-// MMA with N = 256 gives t(A) t(B) (columns 0-127) and t(A) l(B) (columns
-// 128-255) and a second with N = 128 adds l(A) t(B) to columns 0-127: t(A) is
-// read once per K step.  One CTA per SM, 288 threads in three roles that meet
-// only at mbarriers (every wait bounded):
+// The split query tile [t(B); l(B)] (256 rows) stays in shared memory; the
+// split rows go to tensor memory, so per 8-dim K step three MMAs with
+// N = 128 and A read from tensor memory accumulate t(A) t(B), t(A) l(B) and
+// l(A) t(B) into the same columns, and the MMAs read only B from shared
+// memory.  One CTA
+// per SM, 288 threads in three roles that meet only at mbarriers (every wait
+// bounded):
 //   warps 0-3  gather: thread p takes row p of the tile, 32 dims (one
-//              128-byte line) per chunk, with cp.async into a 3-stage ring,
-//              two chunks ahead, and splits its own line in place into t(A)
-//              and l(A) once it lands;
+//              128-byte line) per chunk, loaded into registers three chunks
+//              ahead, split into t(A) and l(A) and stored into its lane of
+//              one of four tensor-memory stages;
 //   warp 8     issues the MMAs of a chunk when its stage is full and frees
 //              the stage (tcgen05.commit) when they complete; tensor memory
 //              holds two accumulators so a row tile's MMAs run while the
 //              previous tile is read out;
-//   warps 4-7  epilogue: thread e reads row e of the accumulator, sums the
-//              two halves, and writes the scores of the tile's tokens.
+//   warps 4-7  epilogue: thread e reads row e of the accumulator and writes
+//              the scores of the tile's tokens.
 constexpr int kTcTok = 32;                       // tokens per tile
 constexpr int kTcN = 4 * kTcTok;                 // B rows of t(B) (and of l(B))
 constexpr int kTcKC = 32;                        // dims per chunk: one 128-byte swizzle atom of fp32
 constexpr int kTcChunks = kIdxDim / kTcKC;       // 4
-constexpr int kTcStages = 3;
+constexpr int kTcStages = 4;                     // tensor-memory stages of the split rows
+constexpr int kTcAhead = 3;                      // chunks of a row in registers ahead of their store
 constexpr int kTcGather = 128;                   // warps 0-3
 constexpr int kTcEpi = 128;                      // warps 4-7
 constexpr int kTcThreads = kTcGather + kTcEpi + 32;
 constexpr int kTcMaxSeq = kTcTok;                // distinct sequences in a tile
 constexpr uint32_t kTcOffB = 0;                                // [t(B); l(B)]: 256 rows x 128 fp32
 constexpr uint32_t kTcBBytes = 2u * kTcN * 512u;               // 128 KB
-constexpr uint32_t kTcOffA = kTcOffB + kTcBBytes;              // stages: t(A) 16 KB then l(A) 16 KB
-constexpr uint32_t kTcAHalf = 128u * kTcKC * 4u;
-constexpr uint32_t kTcStageBytes = 2u * kTcAHalf;
-constexpr uint32_t kTcOffBar = kTcOffA + kTcStages * kTcStageBytes;
+constexpr uint32_t kTcOffBar = kTcOffB + kTcBBytes;
 constexpr uint32_t kTcNumBars = 2 * kTcStages + 4;             // full, empty per stage; acc full, acc empty x 2
 constexpr uint32_t kTcOffTmem = kTcOffBar + 8 * kTcNumBars;
 constexpr size_t kTcSmem = kTcOffTmem + 16 + 1024;             // + alignment slack
-constexpr uint32_t kTcTmemCols = 512;                          // two accumulators of 256 columns
-// kind::tf32: fp32 accumulate, A and B TF32, both K-major, M = 128
-constexpr uint32_t kTcIdesc256 = (1u << 4) | (2u << 7) | (2u << 10) | ((256u >> 3) << 17) | ((128u >> 4) << 24);
+// tensor memory: accumulators in columns [0, 128) and [128, 256); stage q's
+// t(A) in [256 + 64 q, 256 + 64 q + 32), its l(A) in the next 32 columns
+constexpr uint32_t kTcTmemCols = 512;
+constexpr uint32_t kTcTmemA = 256;
+// kind::tf32: fp32 accumulate, A and B TF32, both K-major, M = 128, N = 128
 constexpr uint32_t kTcIdesc128 = (1u << 4) | (2u << 7) | (2u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
 static_assert(kTcSmem + 1024 <= 227u * 1024u, "token-tiled scorer shared memory");
+static_assert(kTcTmemA + 64u * kTcStages <= kTcTmemCols, "token-tiled scorer tensor memory");
+static_assert(kTcStages == kTcChunks, "a row tile's chunks map onto the stages one to one");
 
 __device__ __forceinline__ float tf32_trunc(float x) { return __uint_as_float(__float_as_uint(x) & 0xffffe000u); }
 // x rounded to the nearest TF32 value (ties away from zero)
@@ -469,11 +473,15 @@ k_score_tc(const IndexArgs a, float* __restrict__ scores, unsigned* err) {
   bool timed_out = false;
   const int n_chunks = n_items * kTcChunks;
   if (warp < 4) {
-    // ---- gather and split: thread p owns row p of every tile.  Chunk q is
-    // split as soon as its line lands and handed to the MMA; only then is
-    // the gather of chunk q + 2 issued into the stage chunk q - 1 used, so
-    // the MMAs of chunk q run while q + 1 is split and q + 2 is in flight.
+    // ---- gather and split: thread p owns row p of every tile.  Chunk q's
+    // line is loaded three chunks ahead into registers; once its stage is
+    // free it is split and stored into the thread's lane of the stage, and
+    // the load of chunk q + 3 takes its registers.  (Staging the lines
+    // through a 5-deep cp.async ring in shared memory instead was measured
+    // slower: 224 against 184 us for the 512-token ubatch.)
     const int p = tid;
+    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    const bool pooled32 = (reinterpret_cast<uintptr_t>(a.pooled) & 31u) == 0;   // else 16-byte loads
     auto row_slot = [&](int k) {
       int d, rt;
       item_at(k, &d, &rt);
@@ -488,45 +496,74 @@ k_score_tc(const IndexArgs a, float* __restrict__ scores, unsigned* err) {
       }
       return sl;
     };
-    // the slot of row p in the item being gathered, and in the next one
-    // (loaded one item ahead, so the gather never waits on it)
+    // the slot of row p in the item whose chunks are being loaded, and in
+    // the next one (loaded one item ahead, so no load waits on it)
     int sl_cur = -1, sl_next = n_items > 0 ? row_slot(0) : -1;
-    auto gather = [&](int q) {
-      const int k = q / kTcChunks, c = q % kTcChunks, st = q % kTcStages, use = q / kTcStages;
-      if (!mbar_wait(bar_empty + 8 * st, (uint32_t)((use & 1) ^ 1))) timed_out = true;
+    auto load = [&](int q, float4 (&r)[8]) {
+      const int k = q / kTcChunks, c = q % kTcChunks;
       if (c == 0) {
         sl_cur = sl_next;
         sl_next = k + 1 < n_items ? row_slot(k + 1) : -1;
       }
-      const float* src = a.pooled + (int64_t)(sl_cur < 0 ? 0 : sl_cur) * kIdxDim + c * kTcKC;
-      const uint32_t dst = base_s + kTcOffA + (uint32_t)st * kTcStageBytes;
+      if (sl_cur >= 0 && pooled32) {
+        // 32-byte loads: one L1 sector per load
+        const float* src = a.pooled + (int64_t)sl_cur * kIdxDim + c * kTcKC;
 #pragma unroll
-      for (int m = 0; m < kTcKC / 4; ++m) cp_async16(dst + sw128(128u, (uint32_t)p, (uint32_t)m), src + 4 * m, sl_cur >= 0);
-      asm volatile("cp.async.commit_group;\n" ::: "memory");
-    };
-    for (int q = 0; q < kTcStages - 1 && q < n_chunks; ++q) gather(q);
-    for (int q = 0; q < n_chunks; ++q) {
-      if (q + 1 < n_chunks) {
-        asm volatile("cp.async.wait_group 1;\n" ::: "memory");   // chunk q landed, q + 1 may be in flight
+        for (int m = 0; m < kTcKC / 8; ++m)
+          asm volatile("ld.global.nc.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+                       : "=f"(r[2 * m].x), "=f"(r[2 * m].y), "=f"(r[2 * m].z), "=f"(r[2 * m].w),
+                         "=f"(r[2 * m + 1].x), "=f"(r[2 * m + 1].y), "=f"(r[2 * m + 1].z), "=f"(r[2 * m + 1].w)
+                       : "l"(src + 8 * m));
+      } else if (sl_cur >= 0) {
+        const float4* src = reinterpret_cast<const float4*>(a.pooled + (int64_t)sl_cur * kIdxDim + c * kTcKC);
+#pragma unroll
+        for (int m = 0; m < kTcKC / 4; ++m) r[m] = __ldg(src + m);
       } else {
-        asm volatile("cp.async.wait_group 0;\n" ::: "memory");
-      }
-      // this thread's line of chunk q: split it in place
-      const int st = q % kTcStages;
-      unsigned char* at = base + kTcOffA + (uint32_t)st * kTcStageBytes;
 #pragma unroll
-      for (int m = 0; m < kTcKC / 4; ++m) {
-        const uint32_t o = sw128(128u, (uint32_t)p, (uint32_t)m);
-        const float4 x = *reinterpret_cast<const float4*>(at + o);
-        const float4 xt = make_float4(tf32_trunc(x.x), tf32_trunc(x.y), tf32_trunc(x.z), tf32_trunc(x.w));
-        const float4 xl = make_float4(tf32_round(x.x - xt.x), tf32_round(x.y - xt.y), tf32_round(x.z - xt.z),
-                                      tf32_round(x.w - xt.w));
-        *reinterpret_cast<float4*>(at + o) = xt;
-        *reinterpret_cast<float4*>(at + kTcAHalf + o) = xl;
+        for (int m = 0; m < kTcKC / 4; ++m) r[m] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      fence_async_smem();
+    };
+    auto store = [&](int q, float4 (&r)[8]) {
+      const int st = q % kTcStages, use = q / kTcStages;
+      if (!mbar_wait(bar_empty + 8 * st, (uint32_t)((use & 1) ^ 1))) timed_out = true;
+      tc_fence_after();
+      const uint32_t col = tmem + lane_base + kTcTmemA + 64u * (uint32_t)st;
+      {
+        uint32_t v[kTcKC];   // t(A)
+#pragma unroll
+        for (int m = 0; m < kTcKC / 4; ++m) {
+          v[4 * m] = __float_as_uint(tf32_trunc(r[m].x));
+          v[4 * m + 1] = __float_as_uint(tf32_trunc(r[m].y));
+          v[4 * m + 2] = __float_as_uint(tf32_trunc(r[m].z));
+          v[4 * m + 3] = __float_as_uint(tf32_trunc(r[m].w));
+        }
+        tmem_st32(col, v);
+      }
+      {
+        uint32_t v[kTcKC];   // l(A)
+#pragma unroll
+        for (int m = 0; m < kTcKC / 4; ++m) {
+          v[4 * m] = __float_as_uint(tf32_round(r[m].x - tf32_trunc(r[m].x)));
+          v[4 * m + 1] = __float_as_uint(tf32_round(r[m].y - tf32_trunc(r[m].y)));
+          v[4 * m + 2] = __float_as_uint(tf32_round(r[m].z - tf32_trunc(r[m].z)));
+          v[4 * m + 3] = __float_as_uint(tf32_round(r[m].w - tf32_trunc(r[m].w)));
+        }
+        tmem_st32(col + 32u, v);
+      }
+      tmem_wait_st();
+      tc_fence_before();
       mbar_arrive(bar_full + 8 * st);
-      if (q + kTcStages - 1 < n_chunks) gather(q + kTcStages - 1);
+      if (q + kTcAhead < n_chunks) load(q + kTcAhead, r);
+    };
+    float4 r0[8], r1[8], r2[8];
+    static_assert(kTcAhead == 3, "three register buffers");
+    if (0 < n_chunks) load(0, r0);
+    if (1 < n_chunks) load(1, r1);
+    if (2 < n_chunks) load(2, r2);
+    for (int q = 0; q < n_chunks; q += 3) {
+      store(q, r0);
+      if (q + 1 < n_chunks) store(q + 1, r1);
+      if (q + 2 < n_chunks) store(q + 2, r2);
     }
   } else if (warp == 8) {
     // ---- the MMAs, issued by one thread
@@ -537,17 +574,17 @@ k_score_tc(const IndexArgs a, float* __restrict__ scores, unsigned* err) {
         if (c == 0 && !mbar_wait(bar_acce + 8 * b, (uint32_t)(((k >> 1) & 1) ^ 1))) timed_out = true;
         if (!mbar_wait(bar_full + 8 * st, (uint32_t)(use & 1))) timed_out = true;
         tc_fence_after();
-        const uint32_t a_t = base_s + kTcOffA + (uint32_t)st * kTcStageBytes;
-        const uint32_t d = tmem + (uint32_t)b * 256u;
+        const uint32_t a_t = tmem + kTcTmemA + 64u * (uint32_t)st;
+        const uint32_t d = tmem + (uint32_t)b * 128u;
 #pragma unroll
         for (int kk = 0; kk < kTcKC / 8; ++kk) {
           const int kg = c * (kTcKC / 8) + kk;            // K step of 8 dims over the whole row
-          const uint64_t at = smem_desc(a_t + (uint32_t)kk * 32u, 16, 1024);
-          const uint64_t al = smem_desc(a_t + kTcAHalf + (uint32_t)kk * 32u, 16, 1024);
-          const uint64_t bd = smem_desc(base_s + kTcOffB + (uint32_t)(kg >> 2) * (2u * kTcN * 128u) +
-                                            (uint32_t)(kg & 3) * 32u, 16, 1024);
-          mma_tf32(d, at, bd, kTcIdesc256, (c | kk) ? 1u : 0u);   // t(A) [t(B); l(B)]
-          mma_tf32(d, al, bd, kTcIdesc128, 1u);                   // + l(A) t(B)
+          const uint32_t bo = base_s + kTcOffB + (uint32_t)(kg >> 2) * (2u * kTcN * 128u) + (uint32_t)(kg & 3) * 32u;
+          const uint64_t bt = smem_desc(bo, 16, 1024);                     // t(B): rows 0-127
+          const uint64_t bl = smem_desc(bo + (uint32_t)kTcN * 128u, 16, 1024);   // l(B): rows 128-255
+          mma_tf32_ts(d, a_t + 8u * kk, bt, kTcIdesc128, (c | kk) ? 1u : 0u);   // t(A) t(B)
+          mma_tf32_ts(d, a_t + 8u * kk, bl, kTcIdesc128, 1u);                   // + t(A) l(B)
+          mma_tf32_ts(d, a_t + 32u + 8u * kk, bt, kTcIdesc128, 1u);             // + l(A) t(B)
         }
         mma_commit(bar_empty + 8 * st);
         if (c == kTcChunks - 1) mma_commit(bar_accf + 8 * b);
@@ -573,19 +610,19 @@ k_score_tc(const IndexArgs a, float* __restrict__ scores, unsigned* err) {
       if (!mbar_wait(bar_accf + 8 * b, (uint32_t)((k >> 1) & 1))) timed_out = true;
       tc_fence_after();
 #pragma unroll
-      for (int gq = 0; gq < kTcN / 16; ++gq) {
+      for (int gq = 0; gq < kTcN / 32; ++gq) {
         uint32_t r0[16], r1[16];
-        tmem_ld16_nowait(tmem + lane_base + (uint32_t)b * 256u + (uint32_t)(16 * gq), r0);
-        tmem_ld16_nowait(tmem + lane_base + (uint32_t)b * 256u + 128u + (uint32_t)(16 * gq), r1);
+        tmem_ld16_nowait(tmem + lane_base + (uint32_t)b * 128u + (uint32_t)(32 * gq), r0);
+        tmem_ld16_nowait(tmem + lane_base + (uint32_t)b * 128u + (uint32_t)(32 * gq + 16), r1);
         tmem_wait_ld();
 #pragma unroll
-        for (int uu = 0; uu < 4; ++uu) {
-          const int u = gq * 4 + uu;
+        for (int uu = 0; uu < 8; ++uu) {
+          const int u = gq * 8 + uu;
           if (((mask >> u) & 1u) && j < s_nb[u]) {
+            const uint32_t* rr = uu < 4 ? r0 + 4 * uu : r1 + 4 * (uu - 4);
             float v[kIdxHeads];
 #pragma unroll
-            for (int h = 0; h < kIdxHeads; ++h)
-              v[h] = s_w[u][h] * fmaxf(__uint_as_float(r0[uu * 4 + h]) + __uint_as_float(r1[uu * 4 + h]), 0.f);
+            for (int h = 0; h < kIdxHeads; ++h) v[h] = s_w[u][h] * fmaxf(__uint_as_float(rr[h]), 0.f);
             scores[(int64_t)(t0 + u) * a.max_blocks + j] = rok ? (v[0] + v[1]) + (v[2] + v[3]) : -INFINITY;
           }
         }
