@@ -567,7 +567,7 @@ def clone_layer(L):
     return C
 
 
-def measure_chain(name, K, W, dev, *, e2e=True, clocks=None, union=False):
+def measure_chain(name, K, W, dev, *, e2e=True, clocks=None, union=False, in_cluster=False):
     """Headline timing of the whole layer step (qsa_kv_append re-pooling the
     blocks it dirties, then qsa_index_attn): K layer-steps back to back in
     one CUDA graph, events only at its two ends, replayed once.  Layer-step n
@@ -612,9 +612,10 @@ def measure_chain(name, K, W, dev, *, e2e=True, clocks=None, union=False):
     def step(n, with_io=False):
         i, l = (n // n_layers) % n_tok, n % n_layers
         if with_io:
-            layers[l].full_step(**{**inputs[i], **host[i]["views"]}, out=host[i]["out"], union=union)
+            layers[l].full_step(**{**inputs[i], **host[i]["views"]}, out=host[i]["out"], union=union,
+                                in_cluster=in_cluster)
         else:
-            layers[l].full_step(**inputs[i], union=union)
+            layers[l].full_step(**inputs[i], union=union, in_cluster=in_cluster)
         sep.zero_()
         return toks[i]
 
@@ -776,11 +777,13 @@ def run_native(args, rank, world, local):
     res = None
     if rank == 0 or not chained:
         res = measure_config(args.config, args.steps, args.warmup, dev, path=args.path,
-                             clocks=None if chained else clocks, e2e=not chained, union=args.union)
+                             clocks=None if chained else clocks, e2e=not chained, union=args.union,
+                             in_cluster=args.in_cluster)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    ch = measure_chain(args.config, args.steps, args.warmup, dev, clocks=clocks, union=args.union) if chained else None
+    ch = (measure_chain(args.config, args.steps, args.warmup, dev, clocks=clocks, union=args.union,
+                        in_cluster=args.in_cluster) if chained else None)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
@@ -887,6 +890,8 @@ def main():
     ap.add_argument("--path", default="full", choices=["full", "calls"],
                     help="full: append (with the pool update) + index + attention (the layer's whole step); "
                          "calls: the last three, the table appended outside the timed region")
+    ap.add_argument("--in-cluster", action="store_true",
+                    help="path full: the selection inside the attention clusters (QSA_INDEX_ATTN_IN_CLUSTER)")
     ap.add_argument("--union", action="store_true",
                     help="path full: token pairs attend over the union of their lists (QSA_INDEX_ATTN_UNION)")
     ap.add_argument("--no-compare", dest="compare", action="store_false",
