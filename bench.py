@@ -567,6 +567,14 @@ def clone_layer(L):
     return C
 
 
+def chain_layers(step_bytes: float, state_bytes: float) -> int:
+    """Layer copies for back-to-back timing: enough that the other copies'
+    steps move more than 3x the L2 between two steps of one copy, at least
+    2, at most 64 and at most what CHAIN_MEM_BYTES holds."""
+    n = max(2, int(np.ceil(3 * L2_BYTES / max(step_bytes, 1.0))) + 1)
+    return max(2, min(n, 64, int(CHAIN_MEM_BYTES // max(state_bytes, 1))))
+
+
 def measure_chain(name, K, W, dev, *, e2e=True, clocks=None, union=False, in_cluster=False):
     """Headline timing of the whole layer step (qsa_kv_append re-pooling the
     blocks it dirties, then qsa_index_attn): K layer-steps back to back in
@@ -590,8 +598,7 @@ def measure_chain(name, K, W, dev, *, e2e=True, clocks=None, union=False, in_clu
     state_bytes = sum(getattr(L0, k).numel() * getattr(L0, k).element_size()
                       for k in ("idx_k", "k_cache", "v_cache", "blk_cells", "pooled", "cells", "count", "out",
                                 "ws_index", "ws_attn"))
-    n_layers = max(2, int(np.ceil(3 * L2_BYTES / step_bytes)) + 1)
-    n_layers = max(2, min(n_layers, 64, int(CHAIN_MEM_BYTES // max(state_bytes, 1))))
+    n_layers = chain_layers(step_bytes, state_bytes)
     layers = [L0] + [clone_layer(L0) for _ in range(n_layers - 1)]
     inputs = [step_inputs(st, device=dev, new_cells=True) for st in wl.steps]
     toks = [len(st.tok_pos) for st in wl.steps]
