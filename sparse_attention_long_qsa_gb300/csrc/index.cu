@@ -656,6 +656,7 @@ k_score_tc(const IndexArgs a, float* __restrict__ scores, unsigned* err) {
 // them in shared memory and adds only the bins it touched to the token's
 // histogram.
 constexpr int kHistChunk = 8192;
+static_assert(kHistChunk % 1024 == 0, "whole 16-byte loads per thread");
 
 __global__ void __launch_bounds__(256)
 k_hist(const IndexArgs a, void* ws, const float* __restrict__ scores) {
@@ -672,9 +673,35 @@ k_hist(const IndexArgs a, void* ws, const float* __restrict__ scores) {
   grid_dep_wait();
   grid_dep_launch();
   const float* srow = scores + (int64_t)t * a.max_blocks;
-  for (int64_t j = j0 + tid; j < j1; j += 256) {
-    const unsigned bin = score_key(__ldcg(srow + j)) >> (32 - kHistBits);
+  auto add = [&](float x) {
+    const unsigned bin = score_key(x) >> (32 - kHistBits);
     if (atomicAdd(&s_hist[bin], 1u) == 0u) s_touched[atomicAdd(&s_ntouched, 1u)] = (unsigned short)bin;
+  };
+  const float* cs = srow + j0;
+  const int n = j1 > j0 ? (int)(j1 - j0) : 0;
+  if ((reinterpret_cast<uintptr_t>(cs) & 15u) == 0) {
+    // every load of the chunk in flight before the first atomic: 16-byte
+    // loads, kHistChunk / 1024 per thread
+    constexpr int kV = kHistChunk / 4 / 256;
+    const int n4 = n >> 2;
+    float4 v[kV];
+#pragma unroll
+    for (int k = 0; k < kV; ++k) {
+      const int q = tid + 256 * k;
+      v[k] = q < n4 ? __ldcg(reinterpret_cast<const float4*>(cs) + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < kV; ++k) {
+      if (tid + 256 * k < n4) {
+        add(v[k].x);
+        add(v[k].y);
+        add(v[k].z);
+        add(v[k].w);
+      }
+    }
+    for (int j = 4 * n4 + tid; j < n; j += 256) add(__ldcg(cs + j));
+  } else {
+    for (int j = tid; j < n; j += 256) add(__ldcg(cs + j));
   }
   __syncthreads();
   unsigned* gh = hist_of(ws, t);
