@@ -117,8 +117,24 @@ constexpr uint32_t kOffFix = (kOffXC + kOvf * 4 + 15u) & ~15u;
 constexpr uint32_t kSmemBytesSel = kOffFix + (uint32_t)sizeof(SelFix) + 1024;
 static_assert(kSmemBytesSel <= 227u * 1024u, "shared memory of the fused variant");
 
+// fp16 with several tiles per CTA (the pipelined variant, no overflow
+// cells): a third 64 KB row stage over the overflow buffers, two more cell
+// lists and the stages' full and empty barriers.
+constexpr uint32_t kOffX3 = (kOffTmem + 8 + 1023u) & ~1023u;
+constexpr uint32_t kOffCell2 = kOffX3 + kTile * 512;
+constexpr uint32_t kOffCell3 = kOffCell2 + kTile * 4;
+constexpr uint32_t kOffPipeBar = kOffCell3 + kTile * 4;   // u64 full[3], empty[3]
+constexpr uint32_t kSmemBytesPipe16 = kOffPipeBar + 6 * 8 + 1024;
+static_assert(kSmemBytesPipe16 <= 227u * 1024u, "shared memory of the pipelined fp16 variant");
+
 template <bool kSel>
 constexpr uint32_t smem_bytes() { return kSel ? kSmemBytesSel : kSmemBytes; }
+template <bool kQ8, bool kPipe, bool kSel>
+constexpr uint32_t smem_bytes_of() { return (!kQ8 && kPipe && !kSel) ? kSmemBytesPipe16 : smem_bytes<kSel>(); }
+
+__device__ __forceinline__ void arrive_cta(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
 
 // Instruction descriptor, kind::f16: fp32 accumulate, fp16 A and B,
 // M = 128, N = 16; A K-major (QK) or MN-major (PV), B K-major.
@@ -698,14 +714,17 @@ k_attn_tc(const AttnArgs a, const SelArgs sa, unsigned* err) {
   // 4-7 gather and attend the overflow cells from the start
   const bool split = !kQ8 && my_ovf && loop_tiles <= (int)NC;   // this CTA runs one MMA tile
 
-  // Per-tile steps of warps 0-3 (tile: for the phase stamps only)
+  // Per-tile steps of warps 0-3 (tile: for the phase stamps only); uK and
+  // uV are the shared-memory tiles the MMAs read (they rotate over three
+  // stages in the pipelined fp16 variant)
+  uint32_t uK = sK, uV = sV;
   float tmax[kGqa], pe[kGqa];
   auto qk_mma = [&](int tile) {
     // 2. S[cell][head] = K . Q^T
     if (tid == 0) {
 #pragma unroll
       for (int kk = 0; kk < 16; ++kk) {
-        const uint64_t ad = smem_desc(sK + (kk >> 2) * (kTile * 128) + (kk & 3) * 32, 16, 1024);
+        const uint64_t ad = smem_desc(uK + (kk >> 2) * (kTile * 128) + (kk & 3) * 32, 16, 1024);
         const uint64_t bd = smem_desc(sQ + (kk >> 2) * (16 * 128) + (kk & 3) * 32, 16, 1024);
         mma_f16(tmem, ad, bd, kIdescQK, kk > 0);
       }
@@ -759,7 +778,7 @@ k_attn_tc(const AttnArgs a, const SelArgs sa, unsigned* err) {
       for (int mh = 0; mh < 2; ++mh) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t ad = smem_desc(sV + mh * 2 * (kTile * 128) + kk * 2048, kTile * 128, 1024);
+          const uint64_t ad = smem_desc(uV + mh * 2 * (kTile * 128) + kk * 2048, kTile * 128, 1024);
           const uint64_t bd = smem_desc(sP + (kk >> 2) * (16 * 128) + (kk & 3) * 32, 16, 1024);
           mma_f16(tmem + 16 + 16 * mh, ad, bd, kIdescPV, kk > 0);
         }
@@ -796,76 +815,89 @@ k_attn_tc(const AttnArgs a, const SelArgs sa, unsigned* err) {
     }
   };
 
-  // fp16 with several tiles per CTA (and no overflow cells): the next tile's
-  // K rows are gathered while this tile's softmax and P.V run, its V rows
-  // while the next Q.K^T runs (one cp.async group for K and one for V per
-  // tile; the next tile's cells go to a second list).
-  const bool pipe = kPipe && !kQ8 && !use_ovf && (int)rank + (int)NC < loop_tiles;
-  if constexpr (kPipe && !kQ8) {
+  // fp16 with several tiles per CTA (no overflow cells; not with the fused
+  // selection, whose state sits where the third stage would): warps 4-7
+  // gather, warps 0-3 attend, meeting only at mbarriers.  Loads alternate
+  // (load 2i: the K rows of this CTA's i-th tile, 2i + 1: its V rows) over
+  // three 64 KB stages; a stage's full barrier completes once the gather
+  // warps' copies into it have landed (each gather thread arrives for load
+  // L - 1 after issuing load L, so two loads are in flight per thread), its
+  // empty barrier once the MMA reading it has completed.  The gather warps
+  // list a tile's cells with its K load into a ring of three lists; a list
+  // is overwritten only by the K load three tiles later, which waits for
+  // the V of the tile after it to be consumed.
+  const bool pipe = kPipe && !kQ8 && !kSel && !use_ovf && (int)rank + (int)NC < loop_tiles;
+  if constexpr (kPipe && !kQ8 && !kSel) {
     if (pipe) {
-      const __half* kb = static_cast<const __half*>(a.k_cache);
-      const __half* vb = static_cast<const __half*>(a.v_cache);
-      int* cur = scell;
-      int* nxt = reinterpret_cast<int*>(base + kOffXS);   // free without overflow cells
-      auto load_cells = [&](int tile, int* dst, int tx) {
-        const int c0 = tile * kTile, nvt = min(kTile, cnt - c0);
-        int c = -1;
-        if (tx < nvt) {
-          c = (tile == (int)rank) ? cfirst : list_cell(c0 + tx);
-          if (c < 0 || c >= a.n_cells) {
-            atomicOr(err, kErrCell);
-            c = -1;
+      const uint32_t sX3 = base_s + kOffX3;
+      int* cl1 = reinterpret_cast<int*>(base + kOffCell2);
+      int* cl2 = reinterpret_cast<int*>(base + kOffCell3);
+      auto buf = [&](int x) { return x == 0 ? sK : (x == 1 ? sV : sX3); };
+      auto cl = [&](int x) { return x == 0 ? scell : (x == 1 ? cl1 : cl2); };
+      const uint32_t bfull = base_s + kOffPipeBar, bempty = bfull + 24;
+      const int n_my = (loop_tiles - (int)rank + (int)NC - 1) / (int)NC;   // this CTA's tiles (>= 2)
+      if (tid == 0) {
+        for (int q = 0; q < 3; ++q) {
+          mbar_init(bfull + 8 * q, kTile);
+          mbar_init(bempty + 8 * q, 1);
+        }
+      }
+      __syncthreads();
+      if (warp >= 4) {
+        const int tx = tid - kTile;
+        const __half* kb = static_cast<const __half*>(a.k_cache);
+        const __half* vb = static_cast<const __half*>(a.v_cache);
+        for (int L = 0; L < 2 * n_my; ++L) {
+          const int st = L % 3, use = L / 3, i = L >> 1;
+          if (!mbar_wait(bempty + 8 * st, (uint32_t)((use & 1) ^ 1))) timed_out = true;
+          int* cells = cl(i % 3);
+          if ((L & 1) == 0) {
+            const int c0 = ((int)rank + i * (int)NC) * kTile, nvt = min(kTile, cnt - c0);
+            int c = -1;
+            if (tx < nvt) {
+              c = list_cell(c0 + tx);
+              if (c < 0 || c >= a.n_cells) {
+                atomicOr(err, kErrCell);
+                c = -1;
+              }
+            }
+            cells[tx] = c;
+            bar_half(2);   // every row's cell is listed before any copy reads it
+          }
+          const __half* src = (L & 1) ? vb : kb;
+          const uint32_t dst = buf(st);
+          for (int k = tx; k < kTile * 32; k += kTile) {
+            const int row = k >> 5, c16 = k & 31, c = cells[row];
+            const int64_t off = ((int64_t)(c < 0 ? 0 : c) * G + g) * kHeadDim + c16 * 8;
+            cp_async16(dst + sw128(kTile, row, c16), src + off, c >= 0);
+          }
+          asm volatile("cp.async.commit_group;\n" ::: "memory");
+          if (L > 0) {
+            asm volatile("cp.async.wait_group 1;\n" ::: "memory");   // load L - 1 has landed
+            fence_async_smem();
+            arrive_cta(bfull + 8 * ((L - 1) % 3));
           }
         }
-        dst[tx] = c;
-      };
-      auto issue = [&](uint32_t sdst, const __half* src, const int* cells) {
-        for (int i = tid; i < kTile * 32; i += kThreads) {
-          const int row = i >> 5, c16 = i & 31, c = cells[row];
-          const int64_t off = ((int64_t)(c < 0 ? 0 : c) * G + g) * kHeadDim + c16 * 8;
-          cp_async16(sdst + sw128(kTile, row, c16), src + off, c >= 0);
-        }
-        asm volatile("cp.async.commit_group;\n" ::: "memory");
-      };
-      if (tid < kTile) load_cells((int)rank, cur, tid);
-      __syncthreads();
-      issue(sK, kb, cur);
-      issue(sV, vb, cur);
-      for (int tile = (int)rank; tile < loop_tiles; tile += (int)NC) {
-        const int nv = min(kTile, cnt - tile * kTile);
-        const bool has_next = tile + (int)NC < loop_tiles;
-        asm volatile("cp.async.wait_group 1;\n" ::: "memory");   // this tile's K
+        asm volatile("cp.async.wait_group 0;\n" ::: "memory");
         fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        if (warp < 4) {
+        arrive_cta(bfull + 8 * ((2 * n_my - 1) % 3));
+      } else {
+        for (int i = 0; i < n_my; ++i) {
+          const int tile = (int)rank + i * (int)NC;
+          const int nv = min(kTile, cnt - tile * kTile);
+          const int sk = (2 * i) % 3, sv = (2 * i + 1) % 3;
+          uK = buf(sk);
+          uV = buf(sv);
+          if (!mbar_wait(bfull + 8 * sk, (uint32_t)(((2 * i) / 3) & 1))) timed_out = true;
+          tc_fence_after();
           qk_mma(tile);
-        } else if (has_next) {
-          load_cells(tile + (int)NC, nxt, tid - 128);
+          if (tid == 0) arrive_cta(bempty + 8 * sk);   // Q.K^T has completed: the K stage is free
+          softmax_p(tile, cl(i % 3), nv);
+          if (!mbar_wait(bfull + 8 * sv, (uint32_t)(((2 * i + 1) / 3) & 1))) timed_out = true;
+          tc_fence_after();
+          pv_merge(tile);
+          if (tid == 0) arrive_cta(bempty + 8 * sv);   // P.V has completed: the V stage is free
         }
-        tc_fence_before();
-        __syncthreads();   // K tile free, next cells listed
-        tc_fence_after();
-        if (has_next) issue(sK, kb, nxt);
-        if (warp < 4) softmax_p(tile, cur, nv);
-        if (has_next) {
-          asm volatile("cp.async.wait_group 1;\n" ::: "memory");   // this tile's V
-        } else {
-          asm volatile("cp.async.wait_group 0;\n" ::: "memory");
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        if (warp < 4) pv_merge(tile);
-        tc_fence_before();
-        __syncthreads();   // V tile free, tensor memory read
-        tc_fence_after();
-        if (has_next) issue(sV, vb, nxt);
-        int* sw = cur;
-        cur = nxt;
-        nxt = sw;
       }
     }
   }
@@ -1224,7 +1256,8 @@ cudaError_t pick_cluster(const AttnArgs& a, int* nc_out) {
       if (e != cudaSuccess) return e;
       e = cudaFuncSetAttribute(k_attn_tc<kQ8, false, kSel>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
       if (e != cudaSuccess) return e;
-      e = cudaFuncSetAttribute(k_attn_tc<kQ8, true, kSel>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+      e = cudaFuncSetAttribute(k_attn_tc<kQ8, true, kSel>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem_bytes_of<kQ8, true, kSel>());
       if (e != cudaSuccess) return e;
       e = cudaFuncSetAttribute(k_attn_tc<kQ8, true, kSel>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
       if (e != cudaSuccess) return e;
@@ -1289,7 +1322,9 @@ cudaError_t launch_tc(const AttnArgs& a, const SelArgs& sa, int nc, unsigned* er
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)nc, (unsigned)a.n_kv_heads, (unsigned)a.n_tokens);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem_bytes<kSel>();
+  const int tiles = (int)ceil_div(a.cells_pitch, kTile);
+  const bool piped = 2 * nc <= tiles;   // several tiles per CTA: the pipelined variant
+  cfg.dynamicSmemBytes = piped ? smem_bytes_of<kQ8, true, kSel>() : smem_bytes_of<kQ8, false, kSel>();
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1300,9 +1335,7 @@ cudaError_t launch_tc(const AttnArgs& a, const SelArgs& sa, int nc, unsigned* er
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  // several tiles per CTA: the pipelined variant
-  const int tiles = (int)ceil_div(a.cells_pitch, kTile);
-  if (2 * nc <= tiles) return cudaLaunchKernelEx(&cfg, k_attn_tc<kQ8, true, kSel>, a, sa, err);
+  if (piped) return cudaLaunchKernelEx(&cfg, k_attn_tc<kQ8, true, kSel>, a, sa, err);
   return cudaLaunchKernelEx(&cfg, k_attn_tc<kQ8, false, kSel>, a, sa, err);
 }
 
