@@ -17,6 +17,8 @@
 // the dirty list: the distinct slots, ascending, padded with -1.
 // Everything is read and encoded before the grid-dependency wait (the new
 // rows are inputs, not outputs of the preceding kernel); only the stores wait.
+#include <climits>
+
 #include "pool_row.cuh"
 
 QSA_TS_DECLARE(append)
@@ -121,56 +123,79 @@ k_append(const AppendArgs a, const Turns turns, unsigned* err) {
     for (int i = tid; i <= a.n_seq; i += kAppThreads) s_off_buf[i] = a.seq_blk_off[i];
     s_off = s_off_buf;
   }
+  // every new token's sequence and position, for the re-pool's scan of the
+  // tokens sharing a block (inputs: read before the dependency wait)
+  __shared__ int s_tseq[kAppendMaxTokens], s_tpos[kAppendMaxTokens];
+  for (int u = tid; u < a.n_new; u += kAppThreads) {
+    s_tseq[u] = a.tok_seq[u];
+    s_tpos[u] = a.tok_pos[u];
+  }
   __syncthreads();
   if (dirty_cta) {
-    // ---- the dirty list (n_new <= kAppendMaxTokens, 4 tokens per thread)
+    // ---- the dirty list (n_new <= kAppendMaxTokens): every token's slot
+    // (INT_MAX for an invalid token and past n_new), a bitonic sort of the
+    // next power of two >= n_new, then the first of every run of equal slots
+    // compacted in order: the distinct slots, ascending
     __shared__ int s_slot[kAppendMaxTokens];
     __shared__ unsigned s_warp[kAppWarps];
+    int n2 = 2;
+    while (n2 < a.n_new) n2 <<= 1;
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
       const int u = tid + k * kAppThreads;
-      if (u >= a.n_new) break;
-      int ib = 0;
-      s_slot[u] = token_slot(a, mine[k], s_off, &ib, err, false);
+      if (u >= n2) break;
+      int sl = INT_MAX;
+      if (u < a.n_new) {
+        int ib = 0;
+        const int x = token_slot(a, mine[k], s_off, &ib, err, false);
+        sl = x < 0 ? INT_MAX : x;
+      }
+      s_slot[u] = sl;
     }
     __syncthreads();
-    // token t leads its slot if no earlier token has it; leaders are ranked
-    // by slot (ascending order of the list)
-    __shared__ unsigned char s_lead[kAppendMaxTokens];
-    int lead_slot[kPer];
-    unsigned nlead = 0;
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const int t = tid + k * kAppThreads;
-      int sl = t < a.n_new ? s_slot[t] : -1;
-      for (int u = 0; u < t && sl >= 0; ++u)
-        if (s_slot[u] == sl) sl = -1;
-      lead_slot[k] = sl;
-      if (t < a.n_new) s_lead[t] = sl >= 0 ? 1 : 0;
-      nlead += sl >= 0 ? 1u : 0u;
+    for (int k = 2; k <= n2; k <<= 1) {
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        for (int i = tid; i < n2; i += kAppThreads) {
+          const int l = i ^ j;
+          if (l > i) {
+            const int x = s_slot[i], y = s_slot[l];
+            if ((x > y) == ((i & k) == 0)) {
+              s_slot[i] = y;
+              s_slot[l] = x;
+            }
+          }
+        }
+        __syncthreads();
+      }
     }
-    unsigned tot = nlead;
+    // thread tid takes the contiguous run [tid * per, tid * per + per)
+    const int per = (n2 + kAppThreads - 1) / kAppThreads;   // <= 4
+    const int i0 = min(n2, tid * per), i1 = min(n2, i0 + per);
+    unsigned mine_n = 0;
+    for (int i = i0; i < i1; ++i)
+      mine_n += (s_slot[i] != INT_MAX && (i == 0 || s_slot[i] != s_slot[i - 1])) ? 1u : 0u;
+    unsigned incl = mine_n;
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) tot += __shfl_xor_sync(kFull, tot, o);
-    if (lane == 0) s_warp[warp] = tot;
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned y = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_warp[warp] = incl;
     __syncthreads();
-    unsigned n_lead = 0;
-    for (int w = 0; w < kAppWarps; ++w) n_lead += s_warp[w];
-    int rank[kPer];
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      rank[k] = -1;
-      const int sl = lead_slot[k];
-      if (sl < 0) continue;
-      int below = 0;
-      for (int u = 0; u < a.n_new; ++u) below += (s_lead[u] && s_slot[u] < sl) ? 1 : 0;
-      rank[k] = below;
+    unsigned at = incl - mine_n, n_lead = 0;
+    for (int w2 = 0; w2 < kAppWarps; ++w2) {
+      if (w2 < warp) at += s_warp[w2];
+      n_lead += s_warp[w2];
     }
     grid_dep_wait();
     QSA_TS_IF(append, 2, tid == 0);
-#pragma unroll
-    for (int k = 0; k < kAppendMaxTokens / kAppThreads; ++k)
-      if (rank[k] >= 0 && rank[k] < a.n_dirty) a.dirty[rank[k]] = lead_slot[k];
+    for (int i = i0; i < i1; ++i) {
+      const int sl = s_slot[i];
+      if (sl != INT_MAX && (i == 0 || sl != s_slot[i - 1])) {
+        if (at < (unsigned)a.n_dirty) a.dirty[at] = sl;
+        ++at;
+      }
+    }
     for (int i = (int)n_lead + tid; i < a.n_dirty; i += kAppThreads) a.dirty[i] = -1;
     return;
   }
@@ -255,7 +280,7 @@ k_append(const AppendArgs a, const Turns turns, unsigned* err) {
     bool hit = false;
     int pos_in = 0;
     if (u < a.n_new) {
-      const int su = a.tok_seq[u], pu = a.tok_pos[u];
+      const int su = s_tseq[u], pu = s_tpos[u];
       hit = su == mine[0].s && pu >= 0 && (int64_t)pu / r == jb;
       pos_in = pu - (int)(jb * r);
     }
