@@ -50,12 +50,12 @@ METRIC = "QSA-layer decode tokens/s at 50k/250k ctx (1 and 5 seqs); HBM GB/s vs 
 NCU_CMD = ("ncu --set full --clock-control none -k regex:<kernel> -s 6 -c 1 python bench.py --config {cfg} "
            "--path calls --steps 8 --warmup 3 --secondary none --target none --no-cpu --no-compare --flush-mb 256")
 NCU_TRAFFIC = {
-    ("250k_q8", "score"): {"bytes": 33_290_240, "source": "9f98fca30400e732", "capture": NCU_CMD.format(cfg="250k_q8")},
-    ("250k_q8", "select"): {"bytes": 646_656, "source": "d88a916183a8c2d7", "capture": NCU_CMD.format(cfg="250k_q8")},
-    ("250k_q8", "attn"): {"bytes": 2_314_240, "source": "df3917998e050b11", "capture": NCU_CMD.format(cfg="250k_q8")},
-    ("50k", "score"): {"bytes": 6_689_536, "source": "9f98fca30400e732", "capture": NCU_CMD.format(cfg="50k")},
-    ("50k", "select"): {"bytes": 239_872, "source": "d88a916183a8c2d7", "capture": NCU_CMD.format(cfg="50k")},
-    ("50k", "attn"): {"bytes": 4_279_040, "source": "df3917998e050b11", "capture": NCU_CMD.format(cfg="50k")},
+    ("250k_q8", "score"): {"bytes": 33_289_728, "source": "46a573d3f8a147c1", "capture": NCU_CMD.format(cfg="250k_q8")},
+    ("250k_q8", "select"): {"bytes": 646_656, "source": "e704166f2d949dc4", "capture": NCU_CMD.format(cfg="250k_q8")},
+    ("250k_q8", "attn"): {"bytes": 2_314_752, "source": "6f8e69febea8d1c7", "capture": NCU_CMD.format(cfg="250k_q8")},
+    ("50k", "score"): {"bytes": 6_689_536, "source": "46a573d3f8a147c1", "capture": NCU_CMD.format(cfg="50k")},
+    ("50k", "select"): {"bytes": 240_640, "source": "e704166f2d949dc4", "capture": NCU_CMD.format(cfg="50k")},
+    ("50k", "attn"): {"bytes": 4_279_296, "source": "6f8e69febea8d1c7", "capture": NCU_CMD.format(cfg="50k")},
 }
 KERNEL_SOURCES = {
     "append": ("append.cu", "pool_row.cuh", "qsa_internal.cuh"),
