@@ -187,3 +187,20 @@ def check_step(run: Runner, i: int, *, pool_sample=None, oracle_e2e=True, token_
         assert err <= ATTN_TOL[cfg["kv_type"]], f"token {t}: attention max-rel {err}"
     assert_no_device_errors()
     return res, n_swaps
+
+
+def run_lists(wl, L, lists, q, union):
+    """Attention of len(lists) tokens over explicit cell lists (list t of
+    token t) through qsa_sparse_attn or qsa_sparse_attn_union; returns the
+    fp32 output [T][n_q_heads][head_dim]."""
+    T = len(lists)
+    cells = np.full((T, L.pitch), -1, dtype=np.int32)
+    count = np.zeros(T, dtype=np.int32)
+    for t, c in enumerate(lists):
+        cells[t, :len(c)] = c
+        count[t] = len(c)
+    out = torch.full((T, wl.cfg["n_q_heads"], wl.cfg["head_dim"]), float("nan"), device="cuda")
+    qsa.sparse_attn(L.cfg, torch.from_numpy(q).cuda(), L.k_cache, L.v_cache, L.n_cells,
+                    torch.from_numpy(cells).cuda(), torch.from_numpy(count).cuda(), out, None, union=union)
+    torch.cuda.synchronize()
+    return to_np(out)

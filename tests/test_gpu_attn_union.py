@@ -13,7 +13,7 @@ from qsa_workload import make_workload
 from sparse_attention_long_qsa_gb300 import qsa
 from sparse_attention_long_qsa_gb300.layer import QSALayer, append_rows, step_inputs
 
-from gpu_util import ATTN_TOL, Runner, assert_no_device_errors, check_step, max_rel, to_np
+from gpu_util import ATTN_TOL, Runner, assert_no_device_errors, check_step, max_rel, run_lists, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -22,24 +22,6 @@ def _cache(kv_type, n, seed, top_k=2048):
     wl = make_workload(n_seq=1, prompt_len=n, n_steps=1, seed=seed, kv_type=kv_type, cfg={"top_k": top_k})
     L = QSALayer.from_workload(wl, 0, max_tokens=16)
     return wl, L
-
-
-def _run_lists(wl, L, lists, q, union):
-    """Attention of T tokens over explicit cell lists (list t of token t)."""
-    T = len(lists)
-    pitch = L.pitch
-    cells = np.full((T, pitch), -1, dtype=np.int32)
-    count = np.zeros(T, dtype=np.int32)
-    for t, c in enumerate(lists):
-        cells[t, :len(c)] = c
-        count[t] = len(c)
-    cells_d = torch.from_numpy(cells).cuda()
-    count_d = torch.from_numpy(count).cuda()
-    out = torch.full((T, wl.cfg["n_q_heads"], wl.cfg["head_dim"]), float("nan"), device="cuda")
-    qsa.sparse_attn(L.cfg, torch.from_numpy(q).cuda(), L.k_cache, L.v_cache, L.n_cells, cells_d, count_d, out,
-                    None, union=union)
-    torch.cuda.synchronize()
-    return to_np(out)
 
 
 @pytest.mark.parametrize("kv_type", ["f16", "q8_0"])
@@ -57,8 +39,8 @@ def test_overlap_patterns(kv_type):
     lists = [a, a, a, b, c0, c1, np.zeros(0, np.int32), perm[12000:12300], perm[13000:13777]]
     T = len(lists)
     q = rng.standard_normal((T, 16, 256)).astype(np.float16)
-    out = _run_lists(wl, L, lists, q, union=True)
-    ref_tok = _run_lists(wl, L, lists, q, union=False)
+    out = run_lists(wl, L, lists, q, union=True)
+    ref_tok = run_lists(wl, L, lists, q, union=False)
     tol = ATTN_TOL[kv_type]
     for t in range(T):
         if len(lists[t]) == 0:
@@ -78,7 +60,7 @@ def test_identical_tokens_give_identical_bits():
     lst = rng.permutation(wl.n_cells)[:2051].astype(np.int32)
     q1 = rng.standard_normal((1, 16, 256)).astype(np.float16)
     q = np.concatenate([q1, q1])
-    out = _run_lists(wl, L, [lst, lst], q, union=True)
+    out = run_lists(wl, L, [lst, lst], q, union=True)
     assert np.array_equal(out[0], out[1])
 
 
@@ -147,7 +129,7 @@ def test_invalid_cells_are_flagged_and_masked():
     b_bad[650] = -7
     q = rng.standard_normal((2, 16, 256)).astype(np.float16)
     qsa.debug_check()
-    out = _run_lists(wl, L, [a_bad, b_bad], q, union=True)
+    out = run_lists(wl, L, [a_bad, b_bad], q, union=True)
     st_, flags = qsa.debug_check()
     assert st_ == -6 and (flags & 2)
     for t, lst in enumerate((np.delete(a, 10), np.delete(b, 650))):
