@@ -10,9 +10,10 @@ through invariants (count, causality, uniqueness)."""
 import numpy as np
 import pytest
 
+from oracle import qsa_oracle as O
 from qsa_workload import make_workload
 
-from gpu_util import Runner, check_step
+from gpu_util import Runner, check_pooled, check_step
 
 pytestmark = pytest.mark.gpu
 
@@ -48,3 +49,18 @@ def test_prefill_fullsize():
         assert row.max() <= p                    # cells are positions in this layout
         assert len(np.unique(row)) == len(row)
         assert np.all(cells[t, count[t]:] == -1)
+
+
+def test_every_pooled_slot_at_50k():
+    """The warm-up pool update over the whole 50,000-cell prompt: every one of
+    its 12,500 pooled rows against the oracle (the step tests check the dirty
+    rows and a sample)."""
+    wl = make_workload("50k", seed=0, n_steps=1)
+    run = Runner(wl)
+    gpu = run.pooled()
+    dirty = wl.prompt_dirty()
+    slots = np.asarray([s for s in dirty.tolist() if s >= 0])
+    ora = O.pool_update(wl.cfg, wl.idx_k, wl.blk_cells_state(0), wl.slot_block_idx, slots, wl.norm_w,
+                        np.zeros_like(gpu))
+    assert len(slots) >= 12_500
+    check_pooled(gpu[slots], ora[slots])
