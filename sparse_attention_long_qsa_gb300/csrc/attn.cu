@@ -24,13 +24,17 @@
 //   4. O^T = V^T . P^T with M = 128 dims (two halves), N = 16, K = 128 cells:
 //      16 tcgen05.mma (V is the MN-major operand of the same swizzled tile),
 //   5. merges the tile into a running (max, sum, o) in registers.
+// When a CTA takes several fp16 tiles, warps 4-7 gather them into three
+// rotating K/V stages ahead of warps 0-3, which run steps 2-5 (full/empty
+// mbarriers between the two groups); several q8_0 tiles load the next
+// tile's rows into registers under this tile's steps 2-5.
 // Then every CTA stores its (max, sum, o) slices straight into the shared
 // memory of the CTA owning each range of dims (distributed shared memory), the
 // cluster synchronises once, and CTA r reduces dims [r*256/NC, ...) over all
 // NC partials from its own shared memory (log-sum-exp weights) and writes the
 // fp32 output.  No partials go to global memory and no second kernel runs.
 //
-// Waits on the MMA completion barrier are bounded: on timeout the CTA records
+// Waits on the MMA completion and stage barriers are bounded: on timeout the CTA records
 // an error bit and keeps going through every barrier (its output is then
 // meaningless but nothing hangs).
 #include <atomic>
