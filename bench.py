@@ -52,10 +52,10 @@ NCU_CMD = ("ncu --set full --clock-control none -k regex:<kernel> -s 6 -c 1 pyth
 NCU_TRAFFIC = {
     ("250k_q8", "score"): {"bytes": 33_289_728, "source": "46a573d3f8a147c1", "capture": NCU_CMD.format(cfg="250k_q8")},
     ("250k_q8", "select"): {"bytes": 646_656, "source": "e704166f2d949dc4", "capture": NCU_CMD.format(cfg="250k_q8")},
-    ("250k_q8", "attn"): {"bytes": 2_314_752, "source": "6f8e69febea8d1c7", "capture": NCU_CMD.format(cfg="250k_q8")},
+    ("250k_q8", "attn"): {"bytes": 2_314_496, "source": "433eaed082687001", "capture": NCU_CMD.format(cfg="250k_q8")},
     ("50k", "score"): {"bytes": 6_689_536, "source": "46a573d3f8a147c1", "capture": NCU_CMD.format(cfg="50k")},
     ("50k", "select"): {"bytes": 240_640, "source": "e704166f2d949dc4", "capture": NCU_CMD.format(cfg="50k")},
-    ("50k", "attn"): {"bytes": 4_279_296, "source": "6f8e69febea8d1c7", "capture": NCU_CMD.format(cfg="50k")},
+    ("50k", "attn"): {"bytes": 4_279_296, "source": "433eaed082687001", "capture": NCU_CMD.format(cfg="50k")},
 }
 KERNEL_SOURCES = {
     "append": ("append.cu", "pool_row.cuh", "qsa_internal.cuh"),
