@@ -653,30 +653,24 @@ k_score_tc(const IndexArgs a, float* __restrict__ scores, unsigned* err) {
 // ------------------------------------------------------------------ k_hist
 // Threshold-bin histogram of the scores written by k_score_tc (k_score builds
 // it while scoring): a CTA takes kHistChunk blocks of one token, counts
-// them in shared memory and adds only the bins it touched to the token's
-// histogram.
+// them in shared memory (reductions whose result is not read) and adds its
+// non-zero bins to the token's histogram.
 constexpr int kHistChunk = 8192;
 static_assert(kHistChunk % 1024 == 0, "whole 16-byte loads per thread");
 
 __global__ void __launch_bounds__(256)
 k_hist(const IndexArgs a, void* ws, const float* __restrict__ scores) {
   __shared__ unsigned s_hist[kHistBins];
-  __shared__ unsigned short s_touched[kHistBins];
-  __shared__ unsigned s_ntouched;
   const int t = blockIdx.y, tid = threadIdx.x;
   const Tok tk = token_geometry(a, t, nullptr, false);
   const int64_t j0 = (int64_t)blockIdx.x * kHistChunk;
   const int64_t j1 = min((int64_t)tk.nb, j0 + kHistChunk);
   for (int i = tid; i < kHistBins; i += 256) s_hist[i] = 0u;
-  if (tid == 0) s_ntouched = 0u;
   __syncthreads();
   grid_dep_wait();
   grid_dep_launch();
   const float* srow = scores + (int64_t)t * a.max_blocks;
-  auto add = [&](float x) {
-    const unsigned bin = score_key(x) >> (32 - kHistBits);
-    if (atomicAdd(&s_hist[bin], 1u) == 0u) s_touched[atomicAdd(&s_ntouched, 1u)] = (unsigned short)bin;
-  };
+  auto add = [&](float x) { atomicAdd(&s_hist[score_key(x) >> (32 - kHistBits)], 1u); };
   const float* cs = srow + j0;
   const int n = j1 > j0 ? (int)(j1 - j0) : 0;
   if ((reinterpret_cast<uintptr_t>(cs) & 15u) == 0) {
@@ -705,10 +699,9 @@ k_hist(const IndexArgs a, void* ws, const float* __restrict__ scores) {
   }
   __syncthreads();
   unsigned* gh = hist_of(ws, t);
-  const unsigned nt = s_ntouched;
-  for (unsigned i = tid; i < nt; i += 256) {
-    const unsigned b = s_touched[i];
-    atomicAdd(gh + b, s_hist[b]);
+  for (int i = tid; i < kHistBins; i += 256) {
+    const unsigned c = s_hist[i];
+    if (c) atomicAdd(gh + i, c);
   }
 }
 
@@ -856,15 +849,17 @@ k_select(const IndexArgs a, void* ws, const float* __restrict__ scores,
   }
   asm volatile("cp.async.commit_group;\n" ::: "memory");
 
-  // ---- phase A: classify this CTA's blocks
-  for (int wb = 0; wb * kSelWarps * kSelBatch < nwords; ++wb) {
+  // ---- phase A: classify this CTA's blocks, a warp's next batch of words
+  // in flight while it classifies the current one
+  const int nbatch = (int)ceil_div(nwords, kSelWarps * kSelBatch);
+  for (int wb = 0; wb < nbatch; ++wb) {
     const int wbase = wb * kSelWarps * kSelBatch + warp;
-    float v[kSelBatch];
+    float vn[kSelBatch];
 #pragma unroll
     for (int b = 0; b < kSelBatch; ++b) {
-      const int w = wbase + kSelWarps * b;
+      const int w = wbase + kSelWarps * (kSelBatch + b);
       const int64_t j = j0 + (int64_t)w * 32 + lane;
-      v[b] = (wb == 0) ? v0[b] : ((w < nwords && j < j1) ? __ldcg(srow + j) : -INFINITY);
+      vn[b] = (w < nwords && j < j1) ? __ldcg(srow + j) : -INFINITY;
     }
 #pragma unroll
     for (int b = 0; b < kSelBatch; ++b) {
@@ -872,7 +867,7 @@ k_select(const IndexArgs a, void* ws, const float* __restrict__ scores,
       if (w >= nwords) break;
       const int64_t j = j0 + (int64_t)w * 32 + lane;
       const bool in = j < j1;
-      const uint32_t key = score_key(v[b]);
+      const uint32_t key = score_key(v0[b]);
       const int bin = (int)(key >> (32 - kHistBits));
       const unsigned am = __ballot_sync(kFull, in && bin > thr);
       if (lane == 0) sm.bitmap[w] = am;
@@ -889,6 +884,8 @@ k_select(const IndexArgs a, void* ws, const float* __restrict__ scores,
         }
       }
     }
+#pragma unroll
+    for (int b = 0; b < kSelBatch; ++b) v0[b] = vn[b];
   }
   __syncthreads();
   QSA_TS(index, 13);
