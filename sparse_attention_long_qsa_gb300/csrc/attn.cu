@@ -76,7 +76,8 @@ constexpr uint32_t kOffXS = kOffXV + kOvf * 512;    // fp32 [kOvf][8] scores / p
 constexpr uint32_t kOffXO = kOffXS + kOvf * 8 * 4;  // fp32 [8][256] partial output
 constexpr uint32_t kOffXM = kOffXO + 8 * 256 * 4;   // fp32 [8] max, [8] sum
 constexpr uint32_t kOffXC = kOffXM + 64;            // int [kOvf] cells
-constexpr uint32_t kSmemBytes = kOffXC + kOvf * 4 + 1024;   // + alignment slack
+constexpr uint32_t kOffCellN = kOffXC + kOvf * 4;   // int [128] the next tile's cells (q8_0, several tiles)
+constexpr uint32_t kSmemBytes = kOffCellN + kTile * 4 + 1024;   // + alignment slack
 
 // ---- the selection run by the attention clusters (kSel variants)
 constexpr int kFusedMaxList = 1024;                  // chosen blocks (top_k / r)
@@ -117,7 +118,7 @@ struct SelScratch {
   int slots[kFusedSlots + 4];                // slot ids of this CTA's range
 };
 static_assert(sizeof(SelScratch) <= 2u * kTile * 512u, "selection scratch fits in the K and V tiles");
-constexpr uint32_t kOffFix = (kOffXC + kOvf * 4 + 15u) & ~15u;
+constexpr uint32_t kOffFix = (kOffCellN + kTile * 4 + 15u) & ~15u;
 constexpr uint32_t kSmemBytesSel = kOffFix + (uint32_t)sizeof(SelFix) + 1024;
 static_assert(kSmemBytesSel <= 227u * 1024u, "shared memory of the fused variant");
 
@@ -906,57 +907,68 @@ k_attn_tc(const AttnArgs a, const SelArgs sa, unsigned* err) {
     }
   }
 
-  // q8_0: thread -> (row, half) of the tile: 128 int8 of K and of V plus
-  // their 4 scales each, fetched to registers, then dequantised into the
-  // swizzled fp16 tiles.  Each 8 consecutive threads take one half of 8
-  // consecutive rows, so the 16-byte stores of a quarter warp land on 8
-  // distinct swizzled chunks (all 32 banks); the two halves of one row sit
-  // 16 KB apart on the same banks.
-  const int qrow = (tid & 7) | ((tid >> 4) << 3), qhalf = (tid >> 3) & 1;
+  // q8_0: each half warp takes one row at a time, lane l its 16 int8 at
+  // dims 16 (l % 16) .. +15 (one 16-byte load of K and one of V, so a warp
+  // load covers two whole 256-byte rows) plus the scale of their q8_0 block;
+  // warp w takes rows 16 w + 2 j + l / 16, j = 0..7.  Fetched to registers,
+  // then dequantised into the swizzled fp16 tiles: a warp's 16-byte stores
+  // of one j cover the 8 chunk positions of a 128-byte line 4 times each.
+  const int qc16 = lane & 15, qr0 = 16 * warp + (lane >> 4);
   uint4 qk[8], qv[8];
-  uint2 qks = make_uint2(0, 0), qvs = make_uint2(0, 0);
-  auto q8_fetch = [&](int c) {
-    if (c >= 0) {
-      const int8_t* kq = static_cast<const int8_t*>(a.k_cache);
-      const int8_t* vq = static_cast<const int8_t*>(a.v_cache);
-      const int64_t nq = a.n_cells * (int64_t)G * kHeadDim;
-      const int64_t cg = (int64_t)c * G + g;
-      const uint4* kp = reinterpret_cast<const uint4*>(kq + cg * kHeadDim + qhalf * 128);
-      const uint4* vp = reinterpret_cast<const uint4*>(vq + cg * kHeadDim + qhalf * 128);
+  __half qks[8], qvs[8];    // scales of rows j (not combined in the fetch, so
+                            // nothing waits on a load before the MMAs)
+  unsigned qvalid = 0u;     // bit j: row qr0 + 2j holds a cell
+  auto q8_fetch = [&](const int* cl) {
+    qvalid = 0u;
+    if (a.n_cells <= 0) return;   // no row to read: every row is stored as zeros
+    const int8_t* kq = static_cast<const int8_t*>(a.k_cache);
+    const int8_t* vq = static_cast<const int8_t*>(a.v_cache);
+    const int64_t nq = a.n_cells * (int64_t)G * kHeadDim;
+    const __half* kd = reinterpret_cast<const __half*>(kq + nq);
+    const __half* vd = reinterpret_cast<const __half*>(vq + nq);
+    // every load is issued (an invalid row reads cell 0's, which exists,
+    // and is zeroed when stored), so none waits behind a branch
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        qk[j] = __ldg(kp + j);
-        qv[j] = __ldg(vp + j);
-      }
-      qks = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const __half*>(kq + nq) + cg * 8 + qhalf * 4));
-      qvs = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const __half*>(vq + nq) + cg * 8 + qhalf * 4));
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) qk[j] = qv[j] = make_uint4(0, 0, 0, 0);
-      qks = qvs = make_uint2(0, 0);
+    for (int j = 0; j < 8; ++j) {
+      const int c = cl[qr0 + 2 * j];
+      const int64_t cg = (int64_t)(c < 0 ? 0 : c) * G + g;
+      qk[j] = __ldg(reinterpret_cast<const uint4*>(kq + cg * kHeadDim) + qc16);
+      qv[j] = __ldg(reinterpret_cast<const uint4*>(vq + cg * kHeadDim) + qc16);
+      qks[j] = kd[cg * 8 + (qc16 >> 1)];
+      qvs[j] = vd[cg * 8 + (qc16 >> 1)];
+      qvalid |= (c >= 0 ? 1u : 0u) << j;
     }
   };
   auto q8_store = [&]() {
-    const __half* ksh = reinterpret_cast<const __half*>(&qks);
-    const __half* vsh = reinterpret_cast<const __half*>(&qvs);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      // 16 int8 = dims half*128 + 16j .. +15 -> two 16-byte fp16 chunks
-      const __half2 skf = __half2half2(ksh[j >> 1]), svf = __half2half2(vsh[j >> 1]);
-      const int c16 = qhalf * 16 + 2 * j;
-      *reinterpret_cast<uint4*>(base + kOffK + sw128(kTile, qrow, c16)) = dq8(make_uint2(qk[j].x, qk[j].y), skf);
-      *reinterpret_cast<uint4*>(base + kOffK + sw128(kTile, qrow, c16 + 1)) = dq8(make_uint2(qk[j].z, qk[j].w), skf);
-      *reinterpret_cast<uint4*>(base + kOffV + sw128(kTile, qrow, c16)) = dq8(make_uint2(qv[j].x, qv[j].y), svf);
-      *reinterpret_cast<uint4*>(base + kOffV + sw128(kTile, qrow, c16 + 1)) = dq8(make_uint2(qv[j].z, qv[j].w), svf);
+      // 16 int8 = dims 16 qc16 .. +15 of row qr0 + 2j -> two 16-byte fp16 chunks
+      const __half2 skf = __half2half2(qks[j]), svf = __half2half2(qvs[j]);
+      // lanes 4-7 of each quarter warp store their upper chunk first, so the
+      // 8 lanes of a quarter cover the 8 chunk positions of the line
+      const int row = qr0 + 2 * j, sw = (qc16 >> 2) & 1, ca = 2 * qc16 + sw, cb = 2 * qc16 + 1 - sw;
+      const bool ok = (qvalid >> j) & 1u;
+      const uint4 k0 = ok ? dq8(make_uint2(qk[j].x, qk[j].y), skf) : make_uint4(0, 0, 0, 0);
+      const uint4 k1 = ok ? dq8(make_uint2(qk[j].z, qk[j].w), skf) : make_uint4(0, 0, 0, 0);
+      const uint4 v0 = ok ? dq8(make_uint2(qv[j].x, qv[j].y), svf) : make_uint4(0, 0, 0, 0);
+      const uint4 v1 = ok ? dq8(make_uint2(qv[j].z, qv[j].w), svf) : make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(base + kOffK + sw128(kTile, row, ca)) = sw ? k1 : k0;
+      *reinterpret_cast<uint4*>(base + kOffK + sw128(kTile, row, cb)) = sw ? k0 : k1;
+      *reinterpret_cast<uint4*>(base + kOffV + sw128(kTile, row, ca)) = sw ? v1 : v0;
+      *reinterpret_cast<uint4*>(base + kOffV + sw128(kTile, row, cb)) = sw ? v0 : v1;
     }
   };
   // q8_0 with several tiles per CTA (kPipe): the registers hold the next
-  // tile's rows while this tile's MMAs and softmax run; the row's cell id
-  // is read one tile earlier still, and checked only when it is used, so no
-  // warp waits on it before its MMAs.
-  int qc = -1, qraw = 0;   // the fetched row's checked cell; the next row's raw id
+  // tile's rows while this tile's MMAs and softmax run.  The cell lists of
+  // the current and the next tile alternate between two shared arrays
+  // (`qcur`, `qnext`); thread p < 128 checks row p's id of the next tile
+  // before the barrier that precedes this tile's MMAs, having read it one
+  // tile earlier still, so no warp waits on a list read before its MMAs.
+  int* qcur = scell;
+  int* qnext = reinterpret_cast<int*>(base + kOffCellN);
+  int qraw = 0;   // thread p < 128: row p's raw id two tiles ahead
   auto q8_cell = [&](int tile, int raw) {
-    const int i = tile * kTile + qrow;
+    const int i = tile * kTile + tid;
     if (tile >= loop_tiles || i >= cnt) return -1;
     if (raw < 0 || raw >= a.n_cells) {
       atomicOr(err, kErrCell);
@@ -965,13 +977,16 @@ k_attn_tc(const AttnArgs a, const SelArgs sa, unsigned* err) {
     return raw;
   };
   auto q8_raw = [&](int tile) {
-    const int i = tile * kTile + qrow;
+    const int i = tile * kTile + tid;
     return (tile < loop_tiles && i < cnt) ? list_cell(i) : 0;
   };
   if constexpr (kQ8 && kPipe) {
-    qc = q8_cell((int)rank, q8_raw((int)rank));
-    q8_fetch(qc);
-    qraw = q8_raw((int)rank + (int)NC);
+    if (tid < kTile) {
+      qcur[tid] = q8_cell((int)rank, cfirst);
+      qraw = q8_raw((int)rank + (int)NC);
+    }
+    __syncthreads();
+    q8_fetch(qcur);
   }
 
   if (!pipe)
@@ -979,8 +994,8 @@ k_attn_tc(const AttnArgs a, const SelArgs sa, unsigned* err) {
     const int c0 = tile * kTile;
     const int nv = min(kTile, cnt - c0);
     if constexpr (kQ8 && kPipe) {
-      if (qhalf == 0) scell[qrow] = qc;
       q8_store();
+      if (tid < kTile && tile + (int)NC < loop_tiles) qnext[tid] = q8_cell(tile + (int)NC, qraw);
     } else {
     if (tid < kTile) {
       int c = -1;
@@ -1015,7 +1030,7 @@ k_attn_tc(const AttnArgs a, const SelArgs sa, unsigned* err) {
         asm volatile("cp.async.wait_all;\n" ::: "memory");
       }
     } else {
-      q8_fetch(scell[qrow]);
+      q8_fetch(scell);
       q8_store();
     }
     }
@@ -1030,15 +1045,14 @@ k_attn_tc(const AttnArgs a, const SelArgs sa, unsigned* err) {
     QSA_TS(attn, 4 + 10 * (tile / (int)NC));
     if constexpr (kQ8 && kPipe) {
       if (tile + (int)NC < loop_tiles) {
-        qc = q8_cell(tile + (int)NC, qraw);
-        q8_fetch(qc);
-        qraw = q8_raw(tile + 2 * (int)NC);
+        q8_fetch(qnext);
+        if (tid < kTile) qraw = q8_raw(tile + 2 * (int)NC);
       }
     }
 
     if (warp < 4) {
       qk_mma(tile);
-      softmax_p(tile, scell, nv);
+      softmax_p(tile, (kQ8 && kPipe) ? qcur : scell, nv);
       pv_merge(tile);
     } else if (my_ovf && tile == (int)rank) {
       // Overflow cells on warps 4-7 (128 threads, tx = 0..127); their ids
@@ -1156,6 +1170,11 @@ k_attn_tc(const AttnArgs a, const SelArgs sa, unsigned* err) {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if constexpr (kQ8 && kPipe) {
+      int* const x = qcur;
+      qcur = qnext;
+      qnext = x;
+    }
   }
   // fold the overflow partial into warps 0-3's running state
   if (my_ovf && warp < 4) {

@@ -233,7 +233,6 @@ k_attn_union(const AttnArgs a, unsigned* err) {
   uint32_t phase = 0;
   bool timed_out = false;
   const int mybit = 1 << grp;
-  const int qrow = (tid & 7) | ((tid >> 4) << 3), qhalf = (tid >> 3) & 1;
 
   // fp16: a tile's K and V rows are gathered together (cp.async) at the top
   // of its iteration, the next tile's cells listed meanwhile.  Gathering the
@@ -278,48 +277,58 @@ k_attn_union(const AttnArgs a, unsigned* err) {
       cp_async16(sV + sw128(kUTile, row, c16), vb + off, c >= 0);
     }
   };
-  // q8_0: thread -> (row, half): 128 int8 of K and of V and their 4 scales each
+  // q8_0: each half warp takes one row at a time, lane l its 16 int8 at dims
+  // 16 (l % 16) .. +15 of K and of V and the scale of their q8_0 block (a
+  // warp load covers two whole rows); warp w takes rows 16 w + 2 j + l / 16
+  const int qc16 = tid & 15, qr0 = 16 * (tid >> 5) + ((tid >> 4) & 1);
   uint4 qk[8], qv[8];
-  uint2 qks = make_uint2(0, 0), qvs = make_uint2(0, 0);
-  auto q8_fetch = [&](int c) {
-    if (c >= 0) {
-      const int8_t* kq = static_cast<const int8_t*>(a.k_cache);
-      const int8_t* vq = static_cast<const int8_t*>(a.v_cache);
-      const int64_t nq = a.n_cells * (int64_t)G * kHeadDim;
-      const int64_t cg = (int64_t)c * G + g;
-      const uint4* kp = reinterpret_cast<const uint4*>(kq + cg * kHeadDim + qhalf * 128);
-      const uint4* vp = reinterpret_cast<const uint4*>(vq + cg * kHeadDim + qhalf * 128);
+  __half qks[8], qvs[8];    // scales of rows j (not combined in the fetch, so
+                            // nothing waits on a load before the MMAs)
+  unsigned qvalid = 0u;     // bit j: row qr0 + 2j holds a cell
+  auto q8_fetch = [&](const int* cl) {
+    qvalid = 0u;
+    if (a.n_cells <= 0) return;   // no row to read: every row is stored as zeros
+    const int8_t* kq = static_cast<const int8_t*>(a.k_cache);
+    const int8_t* vq = static_cast<const int8_t*>(a.v_cache);
+    const int64_t nq = a.n_cells * (int64_t)G * kHeadDim;
+    const __half* kd = reinterpret_cast<const __half*>(kq + nq);
+    const __half* vd = reinterpret_cast<const __half*>(vq + nq);
+    // every load is issued (an invalid row reads cell 0's, which exists,
+    // and is zeroed when stored), so none waits behind a branch
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        qk[j] = __ldg(kp + j);
-        qv[j] = __ldg(vp + j);
-      }
-      qks = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const __half*>(kq + nq) + cg * 8 + qhalf * 4));
-      qvs = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const __half*>(vq + nq) + cg * 8 + qhalf * 4));
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) qk[j] = qv[j] = make_uint4(0, 0, 0, 0);
-      qks = qvs = make_uint2(0, 0);
+    for (int j = 0; j < 8; ++j) {
+      const int c = cl[qr0 + 2 * j];
+      const int64_t cg = (int64_t)(c < 0 ? 0 : c) * G + g;
+      qk[j] = __ldg(reinterpret_cast<const uint4*>(kq + cg * kHeadDim) + qc16);
+      qv[j] = __ldg(reinterpret_cast<const uint4*>(vq + cg * kHeadDim) + qc16);
+      qks[j] = kd[cg * 8 + (qc16 >> 1)];
+      qvs[j] = vd[cg * 8 + (qc16 >> 1)];
+      qvalid |= (c >= 0 ? 1u : 0u) << j;
     }
   };
   auto q8_store = [&]() {
-    const __half* ksh = reinterpret_cast<const __half*>(&qks);
-    const __half* vsh = reinterpret_cast<const __half*>(&qvs);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const __half2 skf = __half2half2(ksh[j >> 1]), svf = __half2half2(vsh[j >> 1]);
-      const int c16 = qhalf * 16 + 2 * j;
-      *reinterpret_cast<uint4*>(base + kUOffK + sw128(kUTile, qrow, c16)) = dq8(make_uint2(qk[j].x, qk[j].y), skf);
-      *reinterpret_cast<uint4*>(base + kUOffK + sw128(kUTile, qrow, c16 + 1)) = dq8(make_uint2(qk[j].z, qk[j].w), skf);
-      *reinterpret_cast<uint4*>(base + kUOffV + sw128(kUTile, qrow, c16)) = dq8(make_uint2(qv[j].x, qv[j].y), svf);
-      *reinterpret_cast<uint4*>(base + kUOffV + sw128(kUTile, qrow, c16 + 1)) = dq8(make_uint2(qv[j].z, qv[j].w), svf);
+      const __half2 skf = __half2half2(qks[j]), svf = __half2half2(qvs[j]);
+      // lanes 4-7 of each quarter warp store their upper chunk first, so the
+      // 8 lanes of a quarter cover the 8 chunk positions of the line
+      const int row = qr0 + 2 * j, sw = (qc16 >> 2) & 1, ca = 2 * qc16 + sw, cb = 2 * qc16 + 1 - sw;
+      const bool ok = (qvalid >> j) & 1u;
+      const uint4 k0 = ok ? dq8(make_uint2(qk[j].x, qk[j].y), skf) : make_uint4(0, 0, 0, 0);
+      const uint4 k1 = ok ? dq8(make_uint2(qk[j].z, qk[j].w), skf) : make_uint4(0, 0, 0, 0);
+      const uint4 v0 = ok ? dq8(make_uint2(qv[j].x, qv[j].y), svf) : make_uint4(0, 0, 0, 0);
+      const uint4 v1 = ok ? dq8(make_uint2(qv[j].z, qv[j].w), svf) : make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(base + kUOffK + sw128(kUTile, row, ca)) = sw ? k1 : k0;
+      *reinterpret_cast<uint4*>(base + kUOffK + sw128(kUTile, row, cb)) = sw ? k0 : k1;
+      *reinterpret_cast<uint4*>(base + kUOffV + sw128(kUTile, row, ca)) = sw ? v1 : v0;
+      *reinterpret_cast<uint4*>(base + kUOffV + sw128(kUTile, row, cb)) = sw ? v0 : v1;
     }
   };
 
   if ((int)rank < n_tiles) {
     if (tid < kUTile) list_tile((int)rank, cur, curm);
     __syncthreads();
-    if constexpr (kQ8) q8_fetch(cur[qrow]);
+    if constexpr (kQ8) q8_fetch(cur);
   }
   for (int tile = (int)rank; tile < n_tiles; tile += (int)NC) {
     const bool has_next = tile + (int)NC < n_tiles;
@@ -335,7 +344,7 @@ k_attn_union(const AttnArgs a, unsigned* err) {
     __syncthreads();   // K and V tiles complete; the next tile's cells listed
     tc_fence_after();
     if constexpr (kQ8) {
-      if (has_next) q8_fetch(nxt[qrow]);
+      if (has_next) q8_fetch(nxt);
     }
 
     // 2. S[cell][col] = K . Q^T for the pair's 16 heads
