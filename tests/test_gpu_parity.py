@@ -318,3 +318,25 @@ def test_selection_paths_past_65536_blocks(T):
             np.testing.assert_array_equal(to_np(L.cells[t, :len(want)]), want)
             assert int(L.count[t]) == len(want)
     assert_no_device_errors()
+
+
+@pytest.mark.parametrize("kv_type", ["f16", "q8_0"])
+@pytest.mark.parametrize("T", [1, 2, 5])
+def test_empty_cache_every_cell_invalid(kv_type, T):
+    """n_cells = 0 with full cell lists (every id out of range): the ids are
+    reported, no row is read and the outputs are zero — one tile per CTA (1
+    token), the union of a pair (2), and several tiles per CTA (5 tokens:
+    the pipelined variants)."""
+    wl = make_workload(n_seq=1, prompt_len=600, n_steps=1, seed=12, kv_type=kv_type)
+    L = QSALayer.from_workload(wl, 0, max_tokens=T)
+    pitch = L.pitch
+    cells = torch.arange(pitch, dtype=torch.int32, device="cuda").repeat(T, 1).contiguous()
+    count = torch.full((T,), pitch, dtype=torch.int32, device="cuda")
+    q = torch.randn((T, 16, 256), device="cuda").to(torch.float16)
+    for union in ([False, True] if T == 2 else [False]):
+        out = torch.full((T, 16, 256), float("nan"), dtype=torch.float32, device="cuda")
+        qsa.debug_check()
+        qsa.sparse_attn(L.cfg, q, L.k_cache, L.v_cache, 0, cells, count, out, None, union=union)
+        st, flags = qsa.debug_check()
+        assert st == -6 and (flags & 2)
+        assert torch.count_nonzero(out).item() == 0
