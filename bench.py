@@ -52,10 +52,10 @@ NCU_CMD = ("ncu --set full --clock-control none -k regex:<kernel> -s 6 -c 1 pyth
 NCU_TRAFFIC = {
     ("250k_q8", "score"): {"bytes": 33_289_984, "source": "985a4039b05cb744", "capture": NCU_CMD.format(cfg="250k_q8")},
     ("250k_q8", "select"): {"bytes": 647_424, "source": "63a10328a35246e4", "capture": NCU_CMD.format(cfg="250k_q8")},
-    ("250k_q8", "attn"): {"bytes": 2_318_592, "source": "e243dfaf101ffa66", "capture": NCU_CMD.format(cfg="250k_q8")},
+    ("250k_q8", "attn"): {"bytes": 2_318_336, "source": "77a789af3a3d43c7", "capture": NCU_CMD.format(cfg="250k_q8")},
     ("50k", "score"): {"bytes": 6_689_792, "source": "985a4039b05cb744", "capture": NCU_CMD.format(cfg="50k")},
     ("50k", "select"): {"bytes": 239_872, "source": "63a10328a35246e4", "capture": NCU_CMD.format(cfg="50k")},
-    ("50k", "attn"): {"bytes": 4_279_296, "source": "e243dfaf101ffa66", "capture": NCU_CMD.format(cfg="50k")},
+    ("50k", "attn"): {"bytes": 4_279_296, "source": "77a789af3a3d43c7", "capture": NCU_CMD.format(cfg="50k")},
 }
 KERNEL_SOURCES = {
     "append": ("append.cu", "pool_row.cuh", "qsa_internal.cuh"),
@@ -63,7 +63,8 @@ KERNEL_SOURCES = {
     "score": ("index.cu", "index_util.cuh", "tc_util.cuh", "qsa_internal.cuh"),
     "hist": ("index.cu", "index_util.cuh", "qsa_internal.cuh"),
     "select": ("index.cu", "index_util.cuh", "qsa_internal.cuh"),
-    "attn": ("attn.cu", "attn_util.cuh", "index_util.cuh", "tc_util.cuh", "qsa_internal.cuh"),
+    "attn": ("attn.cu", "attn_pf.cu", "attn_pf.cuh", "attn_util.cuh", "index_util.cuh", "tc_util.cuh",
+             "qsa_internal.cuh"),
     "select_attn": ("attn.cu", "attn_util.cuh", "index_util.cuh", "tc_util.cuh", "qsa_internal.cuh"),
 }
 FLUSH_BYTES = [1 << 30]   # L2 flush buffer (--flush-mb)

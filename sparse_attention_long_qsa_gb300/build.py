@@ -22,7 +22,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build", "qsa")
 LIB = os.path.join(PKG, "libqsa.so")
-SOURCES = ["api.cu", "pool.cu", "index.cu", "attn.cu", "attn_union.cu", "append.cu"]
+SOURCES = ["api.cu", "pool.cu", "index.cu", "attn.cu", "attn_pf.cu", "attn_union.cu", "append.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -41,6 +41,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "attn_pf.cuh"
 #include "attn_util.cuh"
 #include "index_util.cuh"
 #include "qsa_internal.cuh"
@@ -1367,6 +1368,9 @@ cudaError_t launch_plain(const AttnArgs& a, unsigned* err, cudaStream_t stream) 
   int nc = 1;
   cudaError_t e = pick_cluster<kQ8, false>(a, &nc);
   if (e != cudaSuccess) return e;
+  // many tokens (one CTA per (token, KV head) and several tiles each), fp16:
+  // the variant that puts two CTAs on an SM
+  if (!kQ8 && nc == 1 && attn_pf_eligible(a)) return launch_attn_pf(a, err, stream);
   return launch_tc<kQ8, false>(a, SelArgs{}, nc, err, stream);
 }
 
