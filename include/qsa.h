@@ -282,9 +282,13 @@ qsa_status qsa_index_topk_noalloc(const qsa_config* cfg, int32_t n_tokens,
  * compute Q.K^T and P.V on tcgen05 tensor cores (fp16 operands, K/V q8_0
  * rows dequantised to fp16 after the gather, fp32 accumulation), and merge
  * their partial (max, sum, o) through distributed shared memory with
- * log-sum-exp weights.  count[t] == 0 gives zeros.  A cell outside
- * [0, n_cells) is masked and flagged.  The call needs no workspace
- * (qsa_sparse_attn_workspace_size returns 0; `workspace` may be NULL). */
+ * log-sum-exp weights.  For fp16 K/V and calls with many tokens (where one
+ * CTA per (token, KV head) is the cluster size the cost model gives) the
+ * clusters are of two CTAs taking 64-cell tiles, small enough that two
+ * share an SM; the result is the same within the stated tolerance.
+ * count[t] == 0 gives zeros.  A cell outside [0, n_cells) is masked and
+ * flagged.  The call needs no workspace (qsa_sparse_attn_workspace_size
+ * returns 0; `workspace` may be NULL). */
 size_t qsa_sparse_attn_workspace_size(const qsa_config* cfg, int32_t n_tokens);
 qsa_status qsa_sparse_attn(const qsa_config* cfg, int32_t n_tokens,
                            const void* q, const void* k_cache, const void* v_cache,
