@@ -321,12 +321,13 @@ def test_selection_paths_past_65536_blocks(T):
 
 
 @pytest.mark.parametrize("kv_type", ["f16", "q8_0"])
-@pytest.mark.parametrize("T", [1, 2, 5])
+@pytest.mark.parametrize("T", [1, 2, 5, 512])
 def test_empty_cache_every_cell_invalid(kv_type, T):
     """n_cells = 0 with full cell lists (every id out of range): the ids are
     reported, no row is read and the outputs are zero — one tile per CTA (1
-    token), the union of a pair (2), and several tiles per CTA (5 tokens:
-    the pipelined variants)."""
+    token), the union of a pair (2), several tiles per CTA (5 tokens: the
+    pipelined variants) and one CTA per (token, KV head) (512 tokens: the
+    two-CTAs-per-SM fp16 variant, the pipelined q8_0 one)."""
     wl = make_workload(n_seq=1, prompt_len=600, n_steps=1, seed=12, kv_type=kv_type)
     L = QSALayer.from_workload(wl, 0, max_tokens=T)
     pitch = L.pitch
