@@ -98,10 +98,14 @@ def test_multi_token_select_cluster_sizes(T):
         assert np.all(res["cells"][t, :cnt] <= st.tok_pos[t])
 
 
-@pytest.mark.parametrize("n_seq,tps,kv_type", [(3, 3, "f16"), (2, 6, "q8_0"), (2, 12, "f16")])
+@pytest.mark.parametrize("n_seq,tps,kv_type", [(3, 3, "f16"), (2, 6, "q8_0"), (2, 12, "f16"),
+                                              (3, 170, "f16"), (2, 256, "q8_0")])
 def test_batched_verify_several_sequences(n_seq, tps, kv_type):
     """Several tokens per sequence for several sequences (token-tiled scoring
-    with more than one sequence in a token tile, shuffled slots and cells)."""
+    with more than one sequence in a token tile, shuffled slots and cells);
+    510-512 tokens: one selection CTA and one attention CTA per (token, KV
+    head) in the cost models, i.e. the two-CTAs-per-SM fp16 attention and the
+    pipelined q8_0 one over several sequences."""
     wl = make_workload(n_seq=n_seq, prompt_len=[4001 + 997 * s for s in range(n_seq)], n_steps=2,
                        tokens_per_step=tps, seed=40 + tps, shuffled=True, kv_type=kv_type)
     assert "hist" in qsa.index_topk_kernels(n_seq * tps, n_seq)
