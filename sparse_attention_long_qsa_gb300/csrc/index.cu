@@ -36,7 +36,10 @@
 //             ties resolve to the lower block index.  Finally every CTA writes
 //             the member cells of its chosen blocks at its offset in the
 //             token's list (blocks ascending), CTA 0 appends the tail cells
-//             and clears the histogram for the next call.
+//             and clears the histogram for the next call.  A call with more
+//             selection CTAs than SMs (a prefill ubatch) runs two CTAs per SM
+//             (64 registers a thread, no slot-id cache), so one CTA's
+//             classification loads overlap the other's serial phases.
 #include <algorithm>
 #include <atomic>
 #include <cstring>
@@ -76,6 +79,10 @@ constexpr int kCentralBlocks = kSelMaxWords * 32 / 2;   // tokens up to 65536 bl
 constexpr int kRankMax = 1024;            // threshold-bin keys resolved by direct ranking
 static_assert(kRankMax <= kSelLocalCand, "the cut-off digit's keys reuse the candidate list");
 constexpr int kSelList = 2048;            // chosen blocks a CTA lists before expanding
+// dynamic shared memory of k_select: the chosen-block list, then (one CTA
+// per SM only) the slot-id cache, 0-3 ints of alignment shift included
+constexpr size_t kSelDynBytes = sizeof(int32_t) * (kSelList + kSelSlots + 4);
+constexpr size_t kSelDynBytes2 = sizeof(int32_t) * kSelList;
 
 // ----------------------------------------------------------------- k_score
 // Rows are read by groups of 8 lanes: lane `sub` of a group holds dims
@@ -725,13 +732,17 @@ struct SelSmem {
   int tail_cells[8];
 };
 
-__global__ void __launch_bounds__(kSelThreads, 1)
+// kCtasPerSm = 2 (calls with more CTAs than SMs): two CTAs share an SM (64
+// registers a thread) and the launch gives only the chosen-block list as
+// dynamic shared memory, so the slot ids are read from global memory.
+template <int kCtasPerSm>
+__global__ void __launch_bounds__(kSelThreads, kCtasPerSm)
 k_select(const IndexArgs a, void* ws, const float* __restrict__ scores,
          int32_t* __restrict__ cells, int32_t* __restrict__ count, unsigned* err) {
   QSA_TS_SCOPE_LAST(index, 19);
   __shared__ SelSmem sm;
   extern __shared__ __align__(16) int32_t s_dyn[];
-  int* s_list = s_dyn + kSelSlots + 4;     // chosen blocks of this CTA, ascending
+  int* s_list = s_dyn;                     // chosen blocks of this CTA, ascending (kSelList)
   const int t = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t rank = cluster_rank(), NC = cluster_size();
@@ -765,10 +776,10 @@ k_select(const IndexArgs a, void* ws, const float* __restrict__ scores,
   }
   // this CTA's slot ids (an input): copied into shared memory now, waited for
   // before they are read; 16-byte copies where the list is aligned
-  const bool slots_cached = per <= kSelSlots;
-  // s_slots[j - j0] = slots[j]; the array starts 0-3 ints into the buffer so
+  const bool slots_cached = kCtasPerSm == 1 && per <= kSelSlots;
+  // s_slots[j - j0] = slots[j]; the array starts 0-3 ints past the list so
   // that it shares the block list's alignment modulo 16 bytes
-  int32_t* s_slots = s_dyn + ((reinterpret_cast<uintptr_t>(slots + j0) >> 2) & 3);
+  int32_t* s_slots = s_dyn + kSelList + ((reinterpret_cast<uintptr_t>(slots + j0) >> 2) & 3);
   if (slots_cached && j1 > j0) {
     const int64_t n = j1 - j0;
     const int64_t head = min(n, (int64_t)((4 - ((reinterpret_cast<uintptr_t>(slots + j0) >> 2) & 3)) & 3));
@@ -789,15 +800,19 @@ k_select(const IndexArgs a, void* ws, const float* __restrict__ scores,
   // First batch of this warp's scores in flight while the threshold bin is
   // found from the token's histogram (every CTA of the cluster).
   unsigned* gh = hist_of(ws, t);
+  // Word w of this CTA's range holds blocks j0 + 32 w + lane.  Words are
+  // dealt round-robin to the warps (word warp + kSelWarps * b of a batch), so
+  // a lane's b-th load of a batch sits kStride * b blocks past its first one
+  // and exists while that offset is below the blocks left (rem); a range
+  // holds at most kSelMaxWords words, so the offsets fit 32 bits.
+  constexpr int kStride = kSelWarps * 32;
+  const int nloc = j1 > j0 ? (int)(j1 - j0) : 0;
   const float* srow = scores + (int64_t)t * a.max_blocks;
-  // words are dealt round-robin to the warps: word warp + kSelWarps * b
+  const float* lp = srow + j0 + warp * 32 + lane;
+  int rem = nloc - (warp * 32 + lane);
   float v0[kSelBatch];
 #pragma unroll
-  for (int b = 0; b < kSelBatch; ++b) {
-    const int w = warp + kSelWarps * b;
-    const int64_t j = j0 + (int64_t)w * 32 + lane;
-    v0[b] = (w < nwords && j < j1) ? __ldcg(srow + j) : -INFINITY;
-  }
+  for (int b = 0; b < kSelBatch; ++b) v0[b] = b * kStride < rem ? __ldcg(lp + b * kStride) : -INFINITY;
   // the tail block's slot (its member cells are copied once it arrives)
   const int tslot = (rank == 0 && tid < tail) ? slots[tk.nb_full] : -1;
   {
@@ -852,26 +867,24 @@ k_select(const IndexArgs a, void* ws, const float* __restrict__ scores,
   // ---- phase A: classify this CTA's blocks, a warp's next batch of words
   // in flight while it classifies the current one
   const int nbatch = (int)ceil_div(nwords, kSelWarps * kSelBatch);
+  const bool collect = fast && thr >= 0;
   for (int wb = 0; wb < nbatch; ++wb) {
     const int wbase = wb * kSelWarps * kSelBatch + warp;
+    const int wrem = nwords - wbase;   // the warp's b-th word of the batch exists while kSelWarps * b < wrem
+    const float* ln = lp + kStride * kSelBatch;
+    const int rn = rem - kStride * kSelBatch;
     float vn[kSelBatch];
 #pragma unroll
-    for (int b = 0; b < kSelBatch; ++b) {
-      const int w = wbase + kSelWarps * (kSelBatch + b);
-      const int64_t j = j0 + (int64_t)w * 32 + lane;
-      vn[b] = (w < nwords && j < j1) ? __ldcg(srow + j) : -INFINITY;
-    }
+    for (int b = 0; b < kSelBatch; ++b) vn[b] = b * kStride < rn ? __ldcg(ln + b * kStride) : -INFINITY;
 #pragma unroll
     for (int b = 0; b < kSelBatch; ++b) {
-      const int w = wbase + kSelWarps * b;
-      if (w >= nwords) break;
-      const int64_t j = j0 + (int64_t)w * 32 + lane;
-      const bool in = j < j1;
+      if (kSelWarps * b >= wrem) break;
+      const bool in = b * kStride < rem;
       const uint32_t key = score_key(v0[b]);
       const int bin = (int)(key >> (32 - kHistBits));
       const unsigned am = __ballot_sync(kFull, in && bin > thr);
-      if (lane == 0) sm.bitmap[w] = am;
-      if (fast && thr >= 0) {
+      if (lane == 0) sm.bitmap[wbase + kSelWarps * b] = am;
+      if (collect) {
         const bool isc = in && bin == thr;
         const unsigned cm = __ballot_sync(kFull, isc);
         if (cm) {
@@ -880,12 +893,15 @@ k_select(const IndexArgs a, void* ws, const float* __restrict__ scores,
           if (lane == leader) basei = atomicAdd(&sm.ncand, (unsigned)__popc(cm));
           basei = __shfl_sync(kFull, basei, leader);
           const unsigned idx = basei + __popc(cm & ((1u << lane) - 1u));
+          const int64_t j = j0 + (int64_t)(wbase + kSelWarps * b) * 32 + lane;
           if (isc && idx < (unsigned)kSelLocalCand) sm.cand[idx] = cand_key(key, j);
         }
       }
     }
 #pragma unroll
     for (int b = 0; b < kSelBatch; ++b) v0[b] = vn[b];
+    lp = ln;
+    rem = rn;
   }
   __syncthreads();
   QSA_TS(index, 13);
@@ -1277,11 +1293,14 @@ int score_chunk(int T, int64_t max_blocks, int sms) {
   return (int)chunk;
 }
 
-// CTAs per selection cluster.  One k_select CTA fills an SM (512 threads,
+// CTAs per selection cluster.  One k_select<1> CTA fills an SM (512 threads,
 // ~118 KB of shared memory).  A CTA costs about 5 us of its own (histogram,
-// barriers, ordering, expansion) plus ~3 us per 62,500 blocks it classifies,
-// so few tokens take large clusters (one wave either way) and many tokens
-// take small clusters (fewer waves); a CTA holds at most kSelMaxWords words.
+// barriers, ordering, expansion) plus ~3 us per 62,500 blocks it classifies
+// from L2, so few tokens take large clusters (one wave either way) and many
+// tokens take small clusters (fewer waves); a CTA holds at most kSelMaxWords
+// words.  The waves are counted at one CTA per SM also where the launch
+// then takes k_select<2> (two per SM: a 512-token ubatch at 250,000 cells,
+// one-CTA clusters, 68 us instead of 87 us with one per SM).
 // 16-CTA clusters are taken only while the call's selection CTAs leave half
 // of the SMs free: the attention CTAs launched behind the selection (one per
 // SM) then become resident while it runs (measured: a 1-token step 0.3 us
@@ -1326,10 +1345,13 @@ cudaError_t index_setup(int* sms) {
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(k_score<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScoreSmem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k_select, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(sizeof(int32_t) * (kSelSlots + 4 + kSelList)));
+    e = cudaFuncSetAttribute(k_select<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSelDynBytes);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k_select, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    e = cudaFuncSetAttribute(k_select<1>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_select<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSelDynBytes2);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_select<2>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(k_score_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
     if (e != cudaSuccess) return e;
@@ -1422,14 +1444,18 @@ cudaError_t launch_index_topk(const IndexArgs& a, int32_t* cells, int32_t* count
   if (e != cudaSuccess) return e;
   e = index_setup(&sms);
   if (e != cudaSuccess) return e;
-  const size_t slot_bytes = sizeof(int32_t) * (kSelSlots + 4 + kSelList);
   IndexArgs b = a;
   b.max_blocks = a.max_blocks > 0 ? a.max_blocks : 1;
   float* sc = scores_of(ws, a.max_tokens);
   prof_before(kKFinal, stream);
   const int nc = select_cluster(a.n_tokens, b.max_blocks, sms);
-  e = launch_pdl(k_select, dim3((unsigned)nc, (unsigned)a.n_tokens), dim3(kSelThreads), slot_bytes, stream,
-                 (unsigned)nc, b, ws, (const float*)sc, cells, count, err);
+  const dim3 grid((unsigned)nc, (unsigned)a.n_tokens);
+  if ((int64_t)a.n_tokens * nc > (int64_t)sms)
+    e = launch_pdl(k_select<2>, grid, dim3(kSelThreads), kSelDynBytes2, stream,
+                   (unsigned)nc, b, ws, (const float*)sc, cells, count, err);
+  else
+    e = launch_pdl(k_select<1>, grid, dim3(kSelThreads), kSelDynBytes, stream,
+                   (unsigned)nc, b, ws, (const float*)sc, cells, count, err);
   prof_after(kKFinal, stream);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -280,7 +280,7 @@ def test_q8_bad_indices_in_later_tiles_are_masked_and_flagged():
     assert qsa.debug_check()[0] == 0
 
 
-@pytest.mark.parametrize("T", [1, 40])
+@pytest.mark.parametrize("T", [1, 40, 160])
 def test_selection_paths_past_65536_blocks(T):
     """Past 65,536 blocks per token the selection cannot finish in CTA 0 of
     the cluster.  Pooled rows c_s * v make every score c_s times one factor
@@ -289,8 +289,10 @@ def test_selection_paths_past_65536_blocks(T):
     a bin of exactly K keys: K = 600 ranks them directly across the cluster,
     1,500 runs radix rounds over the kept candidates, 5,000 radix rounds that
     re-scan the scores.  One token takes an 8-CTA cluster; 40 tokens take
-    2-CTA clusters whose ranges exceed the cached slot ids.  Each choice
-    equals a stable sort of the GPU's own scores."""
+    2-CTA clusters whose ranges exceed the cached slot ids; 160 tokens take
+    one CTA each, more CTAs than SMs (two CTAs per SM, the slot ids read
+    from global memory).  Each choice equals a stable sort of the GPU's own
+    scores."""
     wl = make_workload(n_seq=1, prompt_len=280_000, n_steps=1, tokens_per_step=T, seed=300 + T)
     L = QSALayer.from_workload(wl, 0)
     L.set_cells(*append_rows(wl, 0))
