@@ -50,11 +50,11 @@ METRIC = "QSA-layer decode tokens/s at 50k/250k ctx (1 and 5 seqs); HBM GB/s vs 
 NCU_CMD = ("ncu --set full --clock-control none -k regex:<kernel> -s 6 -c 1 python bench.py --config {cfg} "
            "--path calls --steps 8 --warmup 3 --secondary none --target none --no-cpu --no-compare --flush-mb 256")
 NCU_TRAFFIC = {
-    ("250k_q8", "score"): {"bytes": 33_289_984, "source": "985a4039b05cb744", "capture": NCU_CMD.format(cfg="250k_q8")},
-    ("250k_q8", "select"): {"bytes": 647_424, "source": "63a10328a35246e4", "capture": NCU_CMD.format(cfg="250k_q8")},
+    ("250k_q8", "score"): {"bytes": 33_290_496, "source": "9307ab22e5a2fb45", "capture": NCU_CMD.format(cfg="250k_q8")},
+    ("250k_q8", "select"): {"bytes": 647_680, "source": "148ee2a21a8bb81c", "capture": NCU_CMD.format(cfg="250k_q8")},
     ("250k_q8", "attn"): {"bytes": 2_318_336, "source": "77a789af3a3d43c7", "capture": NCU_CMD.format(cfg="250k_q8")},
-    ("50k", "score"): {"bytes": 6_689_792, "source": "985a4039b05cb744", "capture": NCU_CMD.format(cfg="50k")},
-    ("50k", "select"): {"bytes": 239_872, "source": "63a10328a35246e4", "capture": NCU_CMD.format(cfg="50k")},
+    ("50k", "score"): {"bytes": 6_690_048, "source": "9307ab22e5a2fb45", "capture": NCU_CMD.format(cfg="50k")},
+    ("50k", "select"): {"bytes": 239_360, "source": "148ee2a21a8bb81c", "capture": NCU_CMD.format(cfg="50k")},
     ("50k", "attn"): {"bytes": 4_279_296, "source": "77a789af3a3d43c7", "capture": NCU_CMD.format(cfg="50k")},
 }
 KERNEL_SOURCES = {
